@@ -1,0 +1,581 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta-rule library on GB300.
+
+Headline: the batched GDN decode step (B=64, Hk=16, Hv=32, Dk=Dv=128, fp32 state of 134 MB), in
+state GB/s (state bytes read + written per step / time per step).  The same JSON line also carries
+the other operations measured in the same run: the Comba decode step (B=256, H=32, K=V=128), the
+varlen chunked prefill (T=15360 over lengths 4096+2048+1024+8192, Hk=16, Hv=32, K=V=128, C=64) in
+tokens/s, and the fused decode window (N=32, h_k=16, h_v=48, ntok=8) in verify and commit mode.
+
+Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a barrier and a device
+synchronise, CUDA events on the stream the kernels run on, max over ranks.  Every step reads state
+last touched more than an L2's worth of traffic earlier (two interleaved decode chains, rotated
+window states, inputs larger than L2).  Under torchrun each rank runs its own replica of the
+workload (weak scaling; the operations have no exchange step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gdn,reference}]
+
+--impl reference times the CPU oracle (the plain C implementation the tests trust) on the same
+workload, a bounded sample of it per step, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gdn_inputs as gi  # noqa: E402
+
+METRIC = "decode state GB/s (% HBM peak); prefill tokens/s (% roofline), 1xGB300"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------------------------------------
+# Algorithmic work of each operation (bytes that must cross HBM at least once; flops of the
+# contractions).  The Comba formula is the one of the KBench spec (flops_src).
+# ------------------------------------------------------------------------------------------------
+def decode_state_bytes(B, Hk, Hv, Dk, Dv):
+    return 2 * B * Hv * Dv * Dk * 4
+
+
+def decode_bytes(B, Hk, Hv, Dk, Dv):
+    tokens = 2 * B * Hk * Dk * 2 + B * Hv * Dv * 2 + B * Hv * 4 + B * Hv * 2
+    return decode_state_bytes(B, Hk, Hv, Dk, Dv) + tokens + B * Hv * Dv * 2  # + y (bf16)
+
+
+def comba_bytes(B, H, K, V):
+    return 2 * B * H * K * V * 4 + B * H * (6 * K + 4 * V + 6)
+
+
+def prefill_bytes(seqlens, Hk, Hv, K, V):
+    T, n = sum(seqlens), len(seqlens)
+    return (2 * T * Hk * K * 2 + T * Hv * V * 2 + 2 * T * Hv * 2 + T * Hv * V * 2
+            + 2 * n * Hv * V * K * 4 + n * 8 + (n + 1) * 8 + 2 * Hv * 4)
+
+
+def prefill_flops(seqlens, Hv, K, V, C):
+    chunks = sum((s + C - 1) // C for s in seqlens)
+    T = sum(seqlens)
+    return T * Hv * 2 * (3 * C * K + 2 * C * V + 3 * K * V) + chunks * Hv * C ** 3 // 3
+
+
+def window_bytes(N, h_k, h_v, D, ntok, commit: bool):
+    C = (2 * h_k + h_v) * D
+    state = N * D * h_v * D * 4
+    act = (N * ntok * C + N * C * 3 + 2 * N * ntok * h_v + 2 * N * ntok * h_v * D) * 4
+    weights = (C * 4 + 2 * h_v + D) * 4
+    return state + act + weights + ((state + N * C * 3 * 4) if commit else 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# Environment helpers
+# ------------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the kernel
+    source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(os.path.join(ROOT, source), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == kernel and parts[1] == sha:
+                    return int(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed regions run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), max=float(f[2]), util=float(f[4]),
+                                 reasons=[n for n, v in zip(
+                                     ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                      "sw_power_cap"), f[5:9]) if v.lower() == "active"]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if r["util"] > 0] or rows
+        reasons = sorted({x for r in loaded for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------------------------------------
+# Distributed plumbing (replicas; one process per GPU)
+# ------------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda_ok() else "gloo"
+            if backend == "nccl":
+                import torch
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local_rank) if _cuda_ok() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU measurements
+# ------------------------------------------------------------------------------------------------
+def _timed(torch, dist, steps, fn):
+    """Run fn(i) for i in range(steps) between barriers and synchronises; return seconds (max over
+    ranks) measured with CUDA events on the current stream."""
+    dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        fn(i)
+    end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return dist.max(start.elapsed_time(end) / 1e3)
+
+
+def bench_decode(torch, gdn, dist, steps, warmup, seed):
+    c = gi.GDN_DECODE_BATCHED
+    B, Hk, Hv, Dk, Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
+    dev = torch.device("cuda")
+    g = gi.rng(seed)
+    b16, f32 = torch.bfloat16, torch.float32
+
+    def tok():
+        t = gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv)
+        return tuple(torch.from_numpy(t[n]).to(dt).to(dev) for n, dt in
+                     (("q", b16), ("k", b16), ("v", b16), ("g", f32), ("beta", b16)))
+
+    # two independent chains (A: s0 <-> s1, B: s2 <-> s3), interleaved, so that every step reads a
+    # state last written two steps (> 2 x 134 MB of traffic) earlier
+    states = [torch.zeros((B, Hv, Dv, Dk), dtype=f32, device=dev) for _ in range(4)]
+    y = torch.empty((B, Hv, Dv), dtype=b16, device=dev)
+    for w in range(c["warmup"]):          # 16 warm-up steps of the recurrence, fresh draws
+        gdn.gdn_decode_step(states[w % 2], *tok(), state_out=states[1 - w % 2], y=y)
+    states[0].copy_(states[c["warmup"] % 2])
+    states[2].copy_(states[0])
+    t = tok()                             # the measured draw, reused by every timed step
+
+    def step(i):
+        chain, parity = (i % 2) * 2, (i // 2) % 2
+        src, dst = states[chain + parity], states[chain + 1 - parity]
+        gdn.gdn_decode_step(src, *t, state_out=dst, y=y)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+
+    # end to end through the public API: per step, the token inputs come from pinned host memory
+    # and y goes back to pinned host memory; the state stays resident in HBM (a serving cache)
+    host_in = [x.cpu().pin_memory() for x in t]
+    dev_in = [torch.empty_like(x) for x in t]
+    host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e_step(i):
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        chain, parity = (i % 2) * 2, (i // 2) % 2
+        gdn.gdn_decode_step(states[chain + parity], *dev_in, state_out=states[chain + 1 - parity],
+                            y=y)
+        host_y.copy_(y, non_blocking=True)
+
+    for i in range(warmup):
+        e2e_step(i)
+    e2e_secs = _timed(torch, dist, steps, e2e_step)
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = host_y.numel() * host_y.element_size()
+    return dict(secs=secs, e2e_secs=e2e_secs, h2d=h2d, d2h=d2h,
+                state_bytes=decode_state_bytes(B, Hk, Hv, Dk, Dv),
+                alg_bytes=decode_bytes(B, Hk, Hv, Dk, Dv), shape=(B, Hk, Hv, Dk, Dv))
+
+
+def bench_comba(torch, gdn, dist, steps, warmup, seed):
+    c = gi.COMBA_DECODE
+    B, H, K, V = c["B"], c["H"], c["K"], c["V"]
+    dev = torch.device("cuda")
+    g = gi.rng(seed + 1)
+    b16, f32 = torch.bfloat16, torch.float32
+
+    def tok():
+        t = gi.comba_decode_token(g, B, H, K, V)
+        return tuple(torch.from_numpy(t[n]).to(dt).to(dev) for n, dt in
+                     (("q", b16), ("k", b16), ("v", b16), ("p", b16), ("beta", b16),
+                      ("g_log", f32)))
+
+    states = [torch.zeros((B, H, K, V), dtype=f32, device=dev) for _ in range(4)]
+    o = torch.empty((B, H, V), dtype=b16, device=dev)
+    for w in range(c["warmup"]):
+        gdn.comba_decode_step(states[w % 2], *tok(), state_new=states[1 - w % 2], o=o)
+    states[0].copy_(states[c["warmup"] % 2])
+    states[2].copy_(states[0])
+    t = tok()
+
+    def step(i):
+        chain, parity = (i % 2) * 2, (i // 2) % 2
+        gdn.comba_decode_step(states[chain + parity], *t, state_new=states[chain + 1 - parity], o=o)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, alg_bytes=comba_bytes(B, H, K, V), shape=(B, H, K, V))
+
+
+def bench_prefill(torch, gdn, dist, steps, warmup, seed):
+    c = gi.GDN_PREFILL
+    Hk, Hv, K, V, C = c["Hk"], c["Hv"], c["K"], c["V"], c["chunk"]
+    x = gi.gdn_prefill_inputs(gi.rng(seed + 2), c["seqlens"], Hk, Hv, K, V, c["pool"])
+    dev = torch.device("cuda")
+    b16, f32 = torch.bfloat16, torch.float32
+    d = {n: torch.from_numpy(x[n]).to(dt).to(dev) for n, dt in
+         (("q", b16), ("k", b16), ("v", b16), ("a", b16), ("b", b16), ("A_log", f32),
+          ("dt_bias", f32), ("state_pool", f32), ("cache_indices", torch.int64),
+          ("cu_seqlens", torch.int64))}
+    T = x["T"]
+    out = torch.empty((T, Hv, V), dtype=b16, device=dev)
+    ws = torch.empty(max(1, gdn.gdn_prefill_workspace_size(len(c["seqlens"]), T, Hk, Hv, K, V, C)),
+                     dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                d["state_pool"], d["cache_indices"], d["cu_seqlens"], C, out=out,
+                                workspace=ws, dev_status=status)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, T=T, alg_bytes=prefill_bytes(c["seqlens"], Hk, Hv, K, V),
+                flops=prefill_flops(c["seqlens"], Hv, K, V, C))
+
+
+def bench_window(torch, gdn, dist, steps, warmup, seed, commit):
+    c = gi.GDN_WINDOW
+    N, h_k, h_v, D, ntok = c["N"], c["h_k"], c["h_v"], c["D"], c["ntok"]
+    x = gi.gdn_window_inputs(gi.rng(seed + 3), N, h_k, h_v, D, ntok)
+    dev = torch.device("cuda")
+    f32 = torch.float32
+    d = {n: torch.from_numpy(np.ascontiguousarray(x[n])).to(f32).to(dev) for n in x}
+    # rotate three state copies (3 x 100 MB) and three history pairs so that no read hits L2
+    states = [d["state"].clone() for _ in range(3)]
+    hists = [d["hist"].clone() for _ in range(3)]
+    hist_out = [torch.empty_like(d["hist"]) for _ in range(3)]
+    y = torch.empty((N, ntok, h_v, D), dtype=f32, device=dev)
+    code = 1 if commit else 0
+
+    def step(i):
+        j = i % 3
+        gdn.gdn_window_fused(states[j], hists[j], hist_out[j], d["qkv"], d["alpha"], d["beta"],
+                             d["z"], d["conv_w"], d["dt"], d["ssm_a"], d["gamma"], h_k, code, y=y)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, alg_bytes=window_bytes(N, h_k, h_v, D, ntok, commit))
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (the baseline; also the reference arm)
+# ------------------------------------------------------------------------------------------------
+class OracleDecodeSample:
+    """The oracle's decode step on the batched workload's shapes, timed on a bounded sample of
+    batch rows, in parallel over rows (each row: Hv heads of Dv x Dk)."""
+
+    def __init__(self, threads: int):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        c = gi.GDN_DECODE_BATCHED
+        self.B, self.Hk, self.Hv, self.Dk, self.Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
+        g = gi.rng(0)
+        self.t = gi.gdn_decode_token(g, self.B, self.Hk, self.Hv, self.Dk, self.Dv)
+        self.S = (g.standard_normal((self.B, self.Hv, self.Dv, self.Dk)) * 0.1)
+        self.threads = threads
+        self.next_row = 0
+
+    def _row(self, b):
+        sl = slice(b, b + 1)
+        t = self.t
+        self.oracle.gdn_decode(self.S[sl], t["q"][sl], t["k"][sl], t["v"][sl], t["g"][sl],
+                               t["beta"][sl], self.Dk ** -0.5)
+
+    def run(self, seconds_target: float):
+        """Returns (state GB/s, cores, description, seconds)."""
+        rows = 0
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(max_workers=self.threads) as ex:
+            while time.perf_counter() - t0 < seconds_target:
+                list(ex.map(self._row, [(self.next_row + i) % self.B for i in range(self.threads)]))
+                self.next_row += self.threads
+                rows += self.threads
+        secs = time.perf_counter() - t0
+        state_bytes = rows * decode_state_bytes(1, self.Hk, self.Hv, self.Dk, self.Dv)
+        desc = (f"{rows} batch rows (each {self.Hv} heads of {self.Dv}x{self.Dk}) of the "
+                f"B={self.B} decode step, fp64 oracle, {self.threads} threads over rows, "
+                f"{secs:.2f} s")
+        return state_bytes / secs / 1e9, self.threads, desc, secs
+
+
+# ------------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work of the oracle baseline (rank 0, N=1)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        return main_reference(args)
+
+    import torch
+    import gated_deltanet_delta_gb300 as gdn
+    from gated_deltanet_delta_gb300 import build as gbuild
+
+    dist = Dist()
+    gbuild.build()
+    gdn.load()
+    torch.cuda.set_device(dist.local_rank)
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    seed = dist.rank
+
+    sampler = ClockSampler(dist.local_rank)
+    with sampler:
+        dec = bench_decode(torch, gdn, dist, args.steps, args.warmup, seed)
+        extra = {}
+        for name, fn in (("comba", lambda: bench_comba(torch, gdn, dist, args.steps, args.warmup,
+                                                         seed)),
+                         ("prefill", lambda: bench_prefill(torch, gdn, dist,
+                                                           max(3, args.steps // 10),
+                                                           args.warmup, seed)),
+                         ("window_verify", lambda: bench_window(torch, gdn, dist, args.steps,
+                                                                args.warmup, seed, False)),
+                         ("window_commit", lambda: bench_window(torch, gdn, dist, args.steps,
+                                                                args.warmup, seed, True))):
+            try:
+                extra[name] = fn()
+            except gdn.GdnError as e:
+                extra[name] = {"unavailable": str(e)}
+    clocks = sampler.summary()
+
+    N, K = dist.world, args.steps
+    ms = dec["secs"] / K * 1e3
+    value = N * dec["state_bytes"] * K / dec["secs"] / 1e9
+    e2e_value = N * dec["state_bytes"] * K / dec["e2e_secs"] / 1e9
+    per_launch = dec["secs"] / K
+    achieved = dec["alg_bytes"] / per_launch / 1e9
+    peak_note = "of measured" if peak_src == "measured" else "of fallback"
+
+    ops = {}
+    if "secs" in extra.get("comba", {}):
+        cb = extra["comba"]
+        t1 = cb["secs"] / K
+        gbs = cb["alg_bytes"] / t1 / 1e9
+        ops["comba_decode"] = {
+            "workload": gi.COMBA_DECODE["name"], "value": N * gbs, "unit": "GB/s",
+            "us_per_step": t1 * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "note": peak_note,
+                         "traffic": profiled_traffic("comba_decode_kernel",
+                                                     "gated_deltanet_delta_gb300/csrc/comba.cuh")}}
+    elif "comba" in extra:
+        ops["comba_decode"] = extra["comba"]
+    if "secs" in extra.get("prefill", {}):
+        pf = extra["prefill"]
+        steps_pf = max(3, args.steps // 10)
+        t1 = pf["secs"] / steps_pf
+        t_hbm = pf["alg_bytes"] / (hbm_peak * 1e9)
+        t_tc = pf["flops"] / (tf_peak * 1e12)
+        roof = max(t_hbm, t_tc)
+        ops["prefill_chunked"] = {
+            "workload": gi.GDN_PREFILL["name"], "value": N * pf["T"] / t1, "unit": "tokens/s",
+            "us_per_call": t1 * 1e6,
+            "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                         "achieved": (pf["alg_bytes"] / t1 / 1e9) if t_hbm >= t_tc
+                         else (pf["flops"] / t1 / 1e12),
+                         "peak": hbm_peak if t_hbm >= t_tc else tf_peak,
+                         "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
+                         "frac": roof / t1, "note": peak_note,
+                         "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
+                         "traffic": None}}
+    elif "prefill" in extra:
+        ops["prefill_chunked"] = extra["prefill"]
+    for key in ("window_verify", "window_commit"):
+        w = extra.get(key, {})
+        if "secs" in w:
+            t1 = w["secs"] / K
+            gbs = w["alg_bytes"] / t1 / 1e9
+            ops[key] = {"workload": gi.GDN_WINDOW["name"], "value": N * gbs, "unit": "GB/s",
+                        "us_per_call": t1 * 1e6,
+                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": gbs / hbm_peak, "note": peak_note,
+                                     "traffic": None}}
+        elif key in extra:
+            ops[key] = w
+
+    cpu = None
+    if dist.rank == 0 and N == 1:
+        gbs, cores, desc, _ = OracleDecodeSample(os.cpu_count() or 1).run(args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    B, Hk, Hv, Dk, Dv = dec["shape"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": N, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": gi.GDN_DECODE_BATCHED["name"], "B": B, "Hk": Hk, "Hv": Hv,
+                   "Dk": Dk, "Dv": Dv, "state_bytes_per_step": dec["state_bytes"],
+                   "l2": "inputs larger than L2: two interleaved chains over four 134 MB states",
+                   "parallelism": f"replicas x{N}"},
+        "hbm_frac": value / N / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "note": peak_note,
+                     "traffic": profiled_traffic("gdn_decode_kernel",
+                                                 "gated_deltanet_delta_gb300/csrc/decode.cuh")},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
+                "d2h_bytes_per_step": dec["d2h"]},
+        "gpu_launches": K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "ops": ops,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def main_reference(args):
+    """The reference arm: the CPU oracle, timed on this host's cores, each step a bounded sample
+    of the batched decode workload.  Under torchrun only rank 0 works and prints."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    per_step = max(0.05, min(1.0, 60.0 / max(1, args.steps + args.warmup)))
+    sample = OracleDecodeSample(threads)
+    for _ in range(args.warmup):
+        sample.run(per_step)
+    vals, secs = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        v, cores, desc, s = sample.run(per_step)
+        vals.append(v)
+        secs += s
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": gi.GDN_DECODE_BATCHED["name"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+// api.cu -- the C ABI of libgdn (declared in include/gdn.h): host-side validation, choice of kernel
+// configuration, launch, and error reporting.  No device memory is allocated here.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gdn.h"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// Two byte ranges overlap without being identical.
+bool partial_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    if (pa == pb) return false;
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool any_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    return na > 0 && nb > 0 && pa < pb + nb && pb < pa + na;
+}
+
+gdn_status launched(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    g_last_error[0] = '\0';
+    return GDN_OK;
+}
+
+#define REQUIRE(cond, status, ...)                    \
+    do {                                              \
+        if (!(cond)) return fail(status, __VA_ARGS__); \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* gdn_last_error(void) { return g_last_error; }
+
+// ------------------------------------------------------------------------------------------------
+gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* q, const void* k,
+                           const void* v, const float* g, const void* beta, void* y,
+                           gdn_dtype y_dtype, int B, int Hk, int Hv, int Dk, int Dv, float scale,
+                           gdn_stream_t stream) {
+    REQUIRE(B >= 0 && Hk >= 1 && Hv >= 1 && Dk >= 1 && Dv >= 1, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: sizes must be B >= 0 and Hk, Hv, Dk, Dv >= 1 (got B=%d Hk=%d Hv=%d "
+            "Dk=%d Dv=%d)", B, Hk, Hv, Dk, Dv);
+    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG, "gdn_decode_step: Hv (%d) must be a multiple of Hk (%d)",
+            Hv, Hk);
+    REQUIRE(y_dtype == GDN_BF16 || y_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: y_dtype must be GDN_BF16 or GDN_F32");
+    REQUIRE(Dk == 64 || Dk == 128, GDN_ERR_UNSUPPORTED, "gdn_decode_step: Dk must be 64 or 128 (got %d)",
+            Dk);
+    if (B == 0) return GDN_OK;
+    REQUIRE(state_in && state_out && q && k && v && g && beta && y, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: null pointer");
+    const size_t sbytes = size_t(B) * Hv * Dv * Dk * sizeof(float);
+    REQUIRE(!partial_overlap(state_in, sbytes, state_out, sbytes), GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: state_out partially overlaps state_in");
+    REQUIRE(aligned(state_in, 16) && aligned(state_out, 16), GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: state buffers must be 16-byte aligned");
+    REQUIRE(aligned(q, 8) && aligned(k, 8), GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: q and k must be 8-byte aligned");
+    REQUIRE(aligned(y, y_dtype == GDN_F32 ? 4 : 2) && aligned(v, 2) && aligned(beta, 2) && aligned(g, 4),
+            GDN_ERR_INVALID_ARG, "gdn_decode_step: misaligned v, beta, g or y");
+    const size_t yb = size_t(B) * Hv * Dv * (y_dtype == GDN_F32 ? 4 : 2);
+    REQUIRE(!any_overlap(y, yb, state_out, sbytes), GDN_ERR_INVALID_ARG,
+            "gdn_decode_step: y overlaps state_out");
+    const long long heads = (long long)B * Hv;
+    REQUIRE(heads * ((Dv + 31) / 32) < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_decode_step: grid too large");
+
+    gdn::DecodeArgs a;
+    a.state_in = state_in;
+    a.state_out = state_out;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.g = g;
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.y = y;
+    a.y_f32 = y_dtype == GDN_F32;
+    a.Hk = Hk;
+    a.Hv = Hv;
+    a.Dv = Dv;
+    a.scale = scale;
+    a.tiles = 0;
+    gdn::launch_decode(a, B, Dk, static_cast<cudaStream_t>(stream));
+    return launched("gdn_decode_step");
+}
+
+// ------------------------------------------------------------------------------------------------
+gdn_status comba_decode_step(const float* state, float* state_new, const void* q, const void* k,
+                             const void* v, const void* p, const void* beta, const float* g,
+                             void* o, gdn_dtype o_dtype, int B, int H, int K, int V, float scale,
+                             gdn_stream_t stream) {
+    REQUIRE(B >= 0 && H >= 1 && K >= 1 && V >= 1, GDN_ERR_INVALID_ARG,
+            "comba_decode_step: sizes must be B >= 0 and H, K, V >= 1 (got B=%d H=%d K=%d V=%d)", B, H,
+            K, V);
+    REQUIRE(o_dtype == GDN_BF16 || o_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
+            "comba_decode_step: o_dtype must be GDN_BF16 or GDN_F32");
+    REQUIRE((K == 64 || K == 128) && (V == 64 || V == 128), GDN_ERR_UNSUPPORTED,
+            "comba_decode_step: K and V must each be 64 or 128 (got K=%d V=%d)", K, V);
+    if (B == 0) return GDN_OK;
+    REQUIRE(state && state_new && q && k && v && p && beta && g && o, GDN_ERR_INVALID_ARG,
+            "comba_decode_step: null pointer");
+    const size_t sbytes = size_t(B) * H * K * V * sizeof(float);
+    REQUIRE(!partial_overlap(state, sbytes, state_new, sbytes), GDN_ERR_INVALID_ARG,
+            "comba_decode_step: state_new partially overlaps state");
+    REQUIRE(aligned(state, 16) && aligned(state_new, 16), GDN_ERR_INVALID_ARG,
+            "comba_decode_step: state buffers must be 16-byte aligned");
+    REQUIRE(aligned(q, 8) && aligned(k, 8) && aligned(p, 8) && aligned(v, 8), GDN_ERR_INVALID_ARG,
+            "comba_decode_step: q, k, p and v must be 8-byte aligned");
+    REQUIRE(aligned(o, o_dtype == GDN_F32 ? 16 : 8) && aligned(beta, 2) && aligned(g, 4),
+            GDN_ERR_INVALID_ARG, "comba_decode_step: misaligned o, beta or g");
+    const size_t ob = size_t(B) * H * V * (o_dtype == GDN_F32 ? 4 : 2);
+    REQUIRE(!any_overlap(o, ob, state_new, sbytes), GDN_ERR_INVALID_ARG,
+            "comba_decode_step: o overlaps state_new");
+    REQUIRE((long long)B * H < (1LL << 31), GDN_ERR_UNSUPPORTED, "comba_decode_step: grid too large");
+
+    gdn::CombaArgs a;
+    a.state = state;
+    a.state_new = state_new;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.p = static_cast<const uint16_t*>(p);
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.g = g;
+    a.o = o;
+    a.o_f32 = o_dtype == GDN_F32;
+    a.scale = scale;
+    gdn::launch_comba(a, B * H, K, V, static_cast<cudaStream_t>(stream));
+    return launched("comba_decode_step");
+}
+
+}  // extern "C"
+
+extern "C" {
+
+size_t gdn_prefill_workspace_size(int, int64_t, int, int, int, int, int) { return 0; }
+
+gdn_status gdn_prefill_chunked(const void*, const void*, const void*, const void*, const void*,
+                               const float*, const float*, float*, int, const int64_t*,
+                               const int64_t*, int, int64_t, int, int, int, int, int, float, void*,
+                               void*, size_t, int32_t*, gdn_stream_t) {
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: not available yet");
+}
+
+gdn_status gdn_window_fused(float*, const float*, float*, const float*, const float*, const float*,
+                            const float*, const float*, const float*, const float*, const float*,
+                            float*, int, int, int, int, unsigned, float, gdn_stream_t) {
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_window_fused: not available yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,27 @@
+// decode.cu -- launch configurations of the GDN decode kernel (kernel in decode.cuh).
+#include "launch.h"
+
+namespace gdn {
+
+namespace {
+
+template <int DK, int TPR, int RPT, int NT>
+void run(DecodeArgs a, int B, cudaStream_t stream) {
+    constexpr int rows = decode_rows_per_cta<DK, TPR, RPT, NT>();
+    a.tiles = (a.Dv + rows - 1) / rows;
+    const unsigned grid = unsigned(B) * unsigned(a.Hv) * unsigned(a.tiles);
+    gdn_decode_kernel<DK, TPR, RPT, NT><<<grid, NT, 0, stream>>>(a);
+}
+
+}  // namespace
+
+// Dk = 128: a row is 32 float4 over 8 lanes (4 each); two rows per thread, 64 rows per CTA.
+// Dk = 64: a row is 16 float4 over 4 lanes (4 each); two rows per thread, 128 rows per CTA.
+void launch_decode(DecodeArgs a, int B, int Dk, cudaStream_t stream) {
+    if (Dk == 128)
+        run<128, 8, 2, 256>(a, B, stream);
+    else
+        run<64, 4, 2, 256>(a, B, stream);
+}
+
+}  // namespace gdn

@@ -1,0 +1,16 @@
+// launch.h -- internal launchers, one per operation, called by the C ABI (api.cu) after it has
+// validated the arguments.  Each picks the kernel configuration for the shape and launches it on
+// `stream`; the caller checks cudaGetLastError().
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "comba.cuh"
+#include "decode.cuh"
+
+namespace gdn {
+
+void launch_decode(DecodeArgs a, int B, int Dk, cudaStream_t stream);
+void launch_comba(const CombaArgs& a, int heads, int K, int V, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,190 @@
+/*
+ * gdn.h -- C ABI of the GB300 gated delta-rule library (libgdn.so).
+ *
+ * Four operations of the gated delta-rule recurrence, each a set of hand-written CUDA kernels for
+ * sm_103a:
+ *   gdn_decode_step      one-token GDN step with key sharing (Hv value heads over Hk key heads)
+ *   comba_decode_step    one-token Comba step (state read with key p, written with key k)
+ *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
+ *   gdn_window_fused     fused decode window: conv + SiLU, L2 norm, gates, recurrence over ntok
+ *                        tokens, gated RMSNorm, with verify / commit / partial commit
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer to dense, contiguous, row-major memory in the layout
+ *     given beside it.  "bf16" is IEEE bfloat16 (the upper half of a float32); "f32" is IEEE float.
+ *   - The caller owns every buffer, including the prefill workspace.  The library allocates no
+ *     device memory and keeps no global state besides a per-device table of kernel attributes.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *     Results are valid once the stream has been synchronised.
+ *   - Arguments are validated on the host before anything is launched.  A rejected call returns
+ *     GDN_ERR_INVALID_ARG or GDN_ERR_UNSUPPORTED and writes nothing.  A failed launch returns
+ *     GDN_ERR_CUDA.  gdn_last_error() gives a human-readable reason for the last failure on the
+ *     calling thread.
+ *   - Sizes of zero are legal no-ops (nothing is launched; pointers may then be NULL).
+ *
+ * Sources (page title and section) of what each operation computes:
+ *   [gated_delta.rs]  metaltile-std, src/ffai/gated_delta.rs: module doc "Recurrence per step",
+ *                     "Layouts", "DISPATCH INVARIANTS".
+ *   [comba spec]      KBench, specs/comba_decode_step.py: signature, spec_md, contract_md,
+ *                     precision_md.
+ *   [gdn_chunkwise]   pymllm, gdn_chunkwise: module doc "Algorithm (per chunk of C tokens)",
+ *                     gdn_extend_chunkwise parameters.
+ *   [gdn.metal]       regolith, baseline-kernels/gdn.metal: header comment and GdnArgs.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad layout or overlap */
+    GDN_ERR_UNSUPPORTED = 2, /* a valid request outside the shapes the kernels are built for */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (see gdn_last_error) */
+    GDN_ERR_TIMEOUT = 4      /* reserved for bounded device-side waits that gave up */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/* A cudaStream_t, passed opaquely so that this header needs no CUDA header. */
+typedef void* gdn_stream_t;
+
+/* Bits of the device status word of gdn_prefill_chunked. */
+#define GDN_STATUS_BAD_CACHE_INDEX 1 /* a cache_indices entry outside [0, pool_size) */
+#define GDN_STATUS_BAD_SEQLENS 2     /* cu_seqlens[n] < 0, decreasing, or beyond T */
+
+/*
+ * gdn_decode_step -- one GDN decode step for B sequences.  [gated_delta.rs] "Recurrence per step":
+ *     S' = g S;  kv = S' k (sum over Dk);  delta = (v - kv) beta;  S_new = S' + delta (x) k;
+ *     y = scale * S_new q (sum over Dk).
+ * Value head hv reads key head hv / (Hv / Hk) ([gated_delta.rs] DISPATCH INVARIANTS).
+ *
+ *   state_in   f32  [B, Hv, Dv, Dk]  (Dk contiguous)      read
+ *   state_out  f32  [B, Hv, Dv, Dk]                       written; may equal state_in (in place),
+ *                                                         must not partially overlap it
+ *   q, k       bf16 [B, Hk, Dk]                           k is used as given (no normalisation)
+ *   v          bf16 [B, Hv, Dv]
+ *   g          f32  [B, Hv]   linear forget gate (not its log)
+ *   beta       bf16 [B, Hv]
+ *   y          [B, Hv, Dv] of y_dtype (GDN_BF16: round to nearest even; GDN_F32)
+ *   scale      readout scale (Dk^-0.5 is the usual choice; 1 reproduces the page exactly)
+ * Supported: Dk in {64, 128}, Dv a positive multiple of 8, Hk >= 1, Hv % Hk == 0.
+ * All state arithmetic is f32; bf16 inputs are widened exactly.
+ */
+gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* q, const void* k,
+                           const void* v, const float* g, const void* beta, void* y,
+                           gdn_dtype y_dtype, int B, int Hk, int Hv, int Dk, int Dv, float scale,
+                           gdn_stream_t stream);
+
+/*
+ * comba_decode_step -- one Comba decode step for B sequences.  [comba spec] spec_md:
+ *     S = exp(g) S;  u = beta (v - S^T p);  S_new = S + k u^T;  o = S_new^T (scale q).
+ * The state is read with p and written with k.
+ *
+ *   state      f32  [B, H, K, V]  (V contiguous)          read
+ *   state_new  f32  [B, H, K, V]                          written; may equal state (in place),
+ *                                                         must not partially overlap it
+ *   q, k, p    bf16 [B, H, K]
+ *   v          bf16 [B, H, V]
+ *   beta       bf16 [B, H]
+ *   g          f32  [B, H]   log-decay (<= 0 in use; any finite value is accepted)
+ *   o          [B, H, V] of o_dtype (GDN_BF16 or GDN_F32)
+ *   scale      query scale ([comba spec]: K^-0.5 when the caller has no other value)
+ * Supported: K in {32, 64, 128}, V a positive multiple of 32 up to 128 ... see gdn_last_error for
+ * the exact reason of an GDN_ERR_UNSUPPORTED.
+ */
+gdn_status comba_decode_step(const float* state, float* state_new, const void* q, const void* k,
+                             const void* v, const void* p, const void* beta, const float* g,
+                             void* o, gdn_dtype o_dtype, int B, int H, int K, int V, float scale,
+                             gdn_stream_t stream);
+
+/*
+ * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_chunked needs for these
+ * sizes (0 when it needs none).  Pure host function; returns 0 for invalid sizes.
+ */
+size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                  int chunk_size);
+
+/*
+ * gdn_prefill_chunked -- varlen prefill of num_seqs sequences, chunkwise WY form.
+ * [gdn_chunkwise] module doc, steps 1-3, and gdn_extend_chunkwise parameters.  Per sequence n
+ * (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and value head h (key head h / (Hv / Hk)):
+ *     S <- state_pool[cache_indices[n], h];  per token t:
+ *     log g_t = -exp(A_log[h]) softplus(a_t + dt_bias[h]) (softplus threshold 20);
+ *     beta_t = sigmoid(b_t);  k^ = k / sqrt(|k|^2 + 1e-6);  q^ = scale q / sqrt(|q|^2 + 1e-6);
+ *     S <- g_t S (I - beta_t k^ k^^T) + beta_t v_t k^^T;  out_t = S q^;
+ *     state_pool[cache_indices[n], h] <- S.
+ * computed chunk by chunk (chunk_size tokens, chunks restart at each sequence start, the last one
+ * may be short) with the WY representation; the inter-chunk carry is f32.
+ *
+ *   q, k           bf16 [T, Hk, K]    not pre-normalised
+ *   v              bf16 [T, Hv, V]
+ *   a, b           bf16 [T, Hv]       raw gate inputs (before softplus / sigmoid)
+ *   A_log, dt_bias f32  [Hv]
+ *   state_pool     f32  [pool_size, Hv, V, K]  updated IN PLACE at the referenced slots only;
+ *                                     other slots are not touched
+ *   cache_indices  int64 [num_seqs]   distinct slots; duplicates give an undefined result
+ *   cu_seqlens     int64 [num_seqs + 1]
+ *   out            bf16 [T, Hv, V]    tokens of skipped sequences are not written
+ *   workspace      device buffer of at least gdn_prefill_workspace_size(...) bytes (or NULL
+ *                  when that size is 0); contents need not be initialised
+ *   dev_status     device int32, zeroed by the caller; the kernels OR in GDN_STATUS_* bits for a
+ *                  sequence they skip (slot out of range, malformed bounds)
+ *   scale          query scale (K^-0.5 when the caller has no other value)
+ * Supported: K = V = 128, chunk_size = 64, Hv % Hk == 0.
+ */
+gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
+                               const void* b, const float* A_log, const float* dt_bias,
+                               float* state_pool, int pool_size, const int64_t* cache_indices,
+                               const int64_t* cu_seqlens, int num_seqs, int64_t T, int Hk, int Hv,
+                               int K, int V, int chunk_size, float scale, void* out,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               gdn_stream_t stream);
+
+/*
+ * gdn_window_fused -- fused decode window over ntok tokens for N independent sequences.
+ * [gdn.metal] header comment, per token:
+ *     conv: s = h0 w0 + h1 w1 + h2 w2 + x_t w3 (history oldest first), SiLU(s); history shifts;
+ *     q, k: x / sqrt(sum x^2 + eps) (the page's rsqrt(sum/128 + eps/128) / sqrt(128));
+ *     gate = exp(softplus(alpha + dt) ssm_a) (softplus threshold 20);  beta = sigmoid(beta_raw);
+ *     kv_j = sum_i S[i][j] k_i;  delta_j = (v_j - gate kv_j) beta;  S[i][j] = gate S[i][j] + k_i delta_j;
+ *     o_j = (sum_i S[i][j] q_i) / sqrt(128);  y_j = o_j rsqrt(mean(o^2) + eps) gamma_j sigmoid(z_j).
+ * Value head h reads key head h % h_k.  Head dim is 128; C = (2 h_k + h_v) * 128 channels.
+ *
+ *   state     f32 [N, 128, h_v, 128]  (key row i, head h, value column j)  read; written in place
+ *                                     only when committing
+ *   hist      f32 [N, C, 3]   conv history, oldest first                    read
+ *   hist_out  f32 [N, C, 3]   committed history; must not overlap hist      written only when
+ *                                                                           committing
+ *   qkv       f32 [N, ntok, C]  q of key head hk at hk*128, k at (h_k+hk)*128, v of head h at
+ *                                (2 h_k + h)*128
+ *   alpha, beta  f32 [N, ntok, h_v]
+ *   z, y      f32 [N, ntok, h_v, 128]
+ *   conv_w    f32 [C, 4];  dt, ssm_a  f32 [h_v];  gamma  f32 [128]   shared by all sequences
+ *   commit    0: verify (nothing but y written); 1: commit state and history after the last token;
+ *             0x100 | k (1 <= k <= ntok): commit after token k (y still computed for all tokens)
+ *   eps       1e-6 on the page
+ * Supported: 1 <= ntok <= 8, h_k >= 1, h_v >= 1.
+ */
+gdn_status gdn_window_fused(float* state, const float* hist, float* hist_out, const float* qkv,
+                            const float* alpha, const float* beta, const float* z,
+                            const float* conv_w, const float* dt, const float* ssm_a,
+                            const float* gamma, float* y, int N, int h_k, int h_v, int ntok,
+                            unsigned commit, float eps, gdn_stream_t stream);
+
+/* Static description of a status code. */
+const char* gdn_status_string(gdn_status status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

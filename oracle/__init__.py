@@ -103,24 +103,6 @@ def gdn_decode(state, q, k, v, g, beta, scale: float):
     return state_new, y
 
 
-def gdn_decode_heads(state, q, k, v, g, beta, scale: float, heads):
-    """The decode step for a sample of (b, hv) heads only; returns ({(b,hv): (S_new, y)})."""
-    B, Hv, Dv, Dk = state.shape
-    Hk = q.shape[1]
-    lib = _load()
-    out = {}
-    for (b, hv) in heads:
-        hk = hv // (Hv // Hk)
-        S = _f64(state[b, hv])
-        qq, kk, vv = _f64(q[b, hk]), _f64(k[b, hk]), _f64(v[b, hv])
-        Sn = np.empty_like(S)
-        y = np.empty(Dv)
-        lib.oracle_gdn_decode_head(Dk, Dv, _p(S), _p(qq), _p(kk), _p(vv), float(g[b, hv]),
-                                   float(beta[b, hv]), float(scale), _p(Sn), _p(y))
-        out[(b, hv)] = (Sn, y)
-    return out
-
-
 # ------------------------------------------------------------------------------------------------
 # Comba decode step: state [B,H,K,V], q,k,p [B,H,K], v [B,H,V], beta, g_log [B,H]
 # ------------------------------------------------------------------------------------------------
@@ -133,21 +115,6 @@ def comba_decode(state, q, k, v, p, beta, g_log, scale: float):
                                        _p(beta), _p(g_log), float(scale), _p(state_new), _p(o)),
            "comba_decode")
     return state_new, o
-
-
-def comba_decode_heads(state, q, k, v, p, beta, g_log, scale: float, heads):
-    B, H, K, V = state.shape
-    lib = _load()
-    out = {}
-    for (b, h) in heads:
-        S = _f64(state[b, h])
-        Sn = np.empty_like(S)
-        o = np.empty(V)
-        lib.oracle_comba_decode_head(K, V, _p(S), _p(_f64(q[b, h])), _p(_f64(k[b, h])),
-                                     _p(_f64(v[b, h])), _p(_f64(p[b, h])), float(beta[b, h]),
-                                     float(g_log[b, h]), float(scale), _p(Sn), _p(o))
-        out[(b, h)] = (Sn, o)
-    return out
 
 
 # ------------------------------------------------------------------------------------------------

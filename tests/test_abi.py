@@ -1,0 +1,72 @@
+"""The C ABI without a GPU: libgdn.so builds, loads and exports every function include/gdn.h
+declares, and host-side validation rejects bad arguments before anything is launched (these calls
+return before the first CUDA call, so they run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_delta_gb300 as gdn
+from gated_deltanet_delta_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "gdn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(\w+)\s*\(", text)) - {"defined"}
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert declared == set(gdn.ABI_SYMBOLS), declared ^ set(gdn.ABI_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert gdn.status_string(s)
+
+
+N = None
+P = ctypes.c_void_p(16)  # a non-null, 16-byte aligned dummy (never dereferenced by these calls)
+
+
+def test_decode_validation(lib):
+    f = lib.gdn_decode_step
+    # Hv not a multiple of Hk
+    assert f(P, P, P, P, P, P, P, P, 0, 1, 3, 4, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    assert "multiple" in gdn.last_error()
+    # unsupported Dk
+    assert f(P, P, P, P, P, P, P, P, 0, 1, 1, 1, 96, 128, 1.0, N) == gdn.GDN_ERR_UNSUPPORTED
+    # null pointer
+    assert f(N, P, P, P, P, P, P, P, 0, 1, 1, 1, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    # bad output dtype code
+    assert f(P, P, P, P, P, P, P, P, 7, 1, 1, 1, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    # partially overlapping state buffers
+    assert f(ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 512), P, P, P, P, P, P, 0, 1, 1, 1,
+             128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    # misaligned state
+    assert f(ctypes.c_void_p(4100), ctypes.c_void_p(4100), P, P, P, P, P, P, 0, 1, 1, 1, 128, 128,
+             1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    # B = 0 is a no-op even with null pointers
+    assert f(N, N, N, N, N, N, N, N, 0, 0, 1, 1, 128, 128, 1.0, N) == gdn.GDN_OK
+
+
+def test_comba_validation(lib):
+    f = lib.comba_decode_step
+    assert f(P, P, P, P, P, P, P, P, P, 0, 1, 1, 96, 128, 1.0, N) == gdn.GDN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, P, N, 0, 1, 1, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 64), P, P, P, P, P, P, P, 0, 1,
+             1, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
+    assert f(N, N, N, N, N, N, N, N, N, 0, 0, 4, 128, 128, 1.0, N) == gdn.GDN_OK
