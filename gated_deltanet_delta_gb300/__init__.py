@@ -235,6 +235,8 @@ def gdn_window_fused(state, hist, hist_out, qkv, alpha, beta, z, conv_w, dt, ssm
     commit: 0 verify, 1 commit after the last token, 0x100|k commit after token k.  Returns y."""
     torch = _torch()
     N, D, h_v, _ = state.shape
+    if D != 128:
+        raise ValueError(f"gdn_window_fused: the head dim is 128, got state of shape {tuple(state.shape)}")
     ntok = qkv.shape[1]
     C = (2 * h_k + h_v) * D
     f32 = torch.float32

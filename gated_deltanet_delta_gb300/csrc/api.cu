@@ -173,10 +173,68 @@ gdn_status gdn_prefill_chunked(const void*, const void*, const void*, const void
     return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: not available yet");
 }
 
-gdn_status gdn_window_fused(float*, const float*, float*, const float*, const float*, const float*,
-                            const float*, const float*, const float*, const float*, const float*,
-                            float*, int, int, int, int, unsigned, float, gdn_stream_t) {
-    return fail(GDN_ERR_UNSUPPORTED, "gdn_window_fused: not available yet");
-}
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+extern "C" gdn_status gdn_window_fused(float* state, const float* hist, float* hist_out,
+                                       const float* qkv, const float* alpha, const float* beta,
+                                       const float* z, const float* conv_w, const float* dt,
+                                       const float* ssm_a, const float* gamma, float* y, int N,
+                                       int h_k, int h_v, int ntok, unsigned commit, float eps,
+                                       gdn_stream_t stream) {
+    REQUIRE(N >= 0 && h_k >= 1 && h_v >= 1, GDN_ERR_INVALID_ARG,
+            "gdn_window_fused: sizes must be N >= 0 and h_k, h_v >= 1 (got N=%d h_k=%d h_v=%d)", N, h_k,
+            h_v);
+    REQUIRE(ntok >= 1 && ntok <= gdn::kWinMaxTok, GDN_ERR_UNSUPPORTED,
+            "gdn_window_fused: ntok must be in [1, %d] (got %d)", gdn::kWinMaxTok, ntok);
+    REQUIRE(h_k <= h_v, GDN_ERR_UNSUPPORTED,
+            "gdn_window_fused: h_k (%d) must not exceed h_v (%d)", h_k, h_v);
+    int commit_at = -1;
+    if (commit == 0u) commit_at = 0;
+    else if (commit == 1u) commit_at = ntok;
+    else if ((commit >> 8) == 1u && (commit & 0xffu) >= 1u && int(commit & 0xffu) <= ntok)
+        commit_at = int(commit & 0xffu);
+    REQUIRE(commit_at >= 0, GDN_ERR_INVALID_ARG,
+            "gdn_window_fused: commit must be 0, 1 or 0x100|k with 1 <= k <= ntok (got 0x%x)", commit);
+    if (N == 0) return GDN_OK;
+    REQUIRE(state && hist && hist_out && qkv && alpha && beta && z && conv_w && dt && ssm_a && gamma &&
+                y, GDN_ERR_INVALID_ARG, "gdn_window_fused: null pointer");
+    const size_t C = size_t(2 * h_k + h_v) * gdn::kWinD;
+    const size_t hbytes = size_t(N) * C * 3 * sizeof(float);
+    REQUIRE(!any_overlap(hist, hbytes, hist_out, hbytes), GDN_ERR_INVALID_ARG,
+            "gdn_window_fused: hist_out must not overlap hist (the q/k history is read by several heads)");
+    const size_t sbytes = size_t(N) * gdn::kWinD * h_v * gdn::kWinD * sizeof(float);
+    const size_t ybytes = size_t(N) * ntok * h_v * gdn::kWinD * sizeof(float);
+    REQUIRE(!any_overlap(y, ybytes, state, sbytes) && !any_overlap(y, ybytes, hist_out, hbytes) &&
+                !any_overlap(state, sbytes, hist_out, hbytes),
+            GDN_ERR_INVALID_ARG, "gdn_window_fused: y, state and hist_out must not overlap");
+    REQUIRE(aligned(state, 16) && aligned(conv_w, 16), GDN_ERR_INVALID_ARG,
+            "gdn_window_fused: state and conv_w must be 16-byte aligned");
+    REQUIRE(aligned(hist, 4) && aligned(hist_out, 4) && aligned(qkv, 4) && aligned(alpha, 4) &&
+                aligned(beta, 4) && aligned(z, 4) && aligned(dt, 4) && aligned(ssm_a, 4) &&
+                aligned(gamma, 4) && aligned(y, 4),
+            GDN_ERR_INVALID_ARG, "gdn_window_fused: float arrays must be 4-byte aligned");
+    REQUIRE(2LL * N * h_v < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_window_fused: grid too large");
+
+    gdn::WindowArgs a;
+    a.state = state;
+    a.hist = hist;
+    a.hist_out = hist_out;
+    a.qkv = qkv;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.z = z;
+    a.conv_w = conv_w;
+    a.dt = dt;
+    a.ssm_a = ssm_a;
+    a.gamma = gamma;
+    a.y = y;
+    a.h_k = h_k;
+    a.h_v = h_v;
+    a.ntok = ntok;
+    a.commit_at = commit_at;
+    a.eps = eps;
+    gdn::launch_window(a, N, static_cast<cudaStream_t>(stream));
+    return launched("gdn_window_fused");
+}

@@ -1,4 +1,5 @@
 // comba.cu -- launch configurations of the Comba decode kernel (kernel in comba.cuh).
+#include "comba.cuh"
 #include "launch.h"
 
 namespace gdn {

@@ -15,22 +15,9 @@
 #pragma once
 
 #include "common.cuh"
+#include "kernel_args.h"
 
 namespace gdn {
-
-struct CombaArgs {
-    const float* state;
-    float* state_new;
-    const uint16_t* q;
-    const uint16_t* k;
-    const uint16_t* v;
-    const uint16_t* p;
-    const uint16_t* beta;
-    const float* g;
-    void* o;
-    int o_f32;
-    float scale;
-};
 
 template <int K, int V, int NT>
 __global__ void __launch_bounds__(NT) comba_decode_kernel(const CombaArgs a) {

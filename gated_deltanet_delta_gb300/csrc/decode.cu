@@ -1,4 +1,5 @@
 // decode.cu -- launch configurations of the GDN decode kernel (kernel in decode.cuh).
+#include "decode.cuh"
 #include "launch.h"
 
 namespace gdn {

@@ -17,23 +17,9 @@
 #pragma once
 
 #include "common.cuh"
+#include "kernel_args.h"
 
 namespace gdn {
-
-struct DecodeArgs {
-    const float* state_in;
-    float* state_out;
-    const uint16_t* q;
-    const uint16_t* k;
-    const uint16_t* v;
-    const float* g;
-    const uint16_t* beta;
-    void* y;
-    int y_f32;
-    int Hk, Hv, Dv;
-    int tiles;  // row tiles per head
-    float scale;
-};
 
 template <int DK, int TPR, int RPT, int NT>
 __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeArgs a) {

@@ -1,0 +1,60 @@
+// kernel_args.h -- argument blocks of the kernels (passed by value) and the window's fixed sizes.
+// Shared by the kernel headers and by the launchers; holds no device code.
+#pragma once
+
+#include <stdint.h>
+
+namespace gdn {
+
+struct DecodeArgs {
+    const float* state_in;
+    float* state_out;
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const float* g;
+    const uint16_t* beta;
+    void* y;
+    int y_f32;
+    int Hk, Hv, Dv;
+    int tiles;  // row tiles per head
+    float scale;
+};
+
+struct CombaArgs {
+    const float* state;
+    float* state_new;
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const uint16_t* p;
+    const uint16_t* beta;
+    const float* g;
+    void* o;
+    int o_f32;
+    float scale;
+};
+
+struct WindowArgs {
+    float* state;
+    const float* hist;
+    float* hist_out;
+    const float* qkv;
+    const float* alpha;
+    const float* beta;
+    const float* z;
+    const float* conv_w;
+    const float* dt;
+    const float* ssm_a;
+    const float* gamma;
+    float* y;
+    int h_k, h_v, ntok, commit_at;
+    float eps;
+};
+
+constexpr int kWinD = 128;       // head dim
+constexpr int kWinHalf = 64;     // columns per CTA
+constexpr int kWinThreads = 128;
+constexpr int kWinMaxTok = 8;
+
+}  // namespace gdn

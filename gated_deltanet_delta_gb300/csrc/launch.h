@@ -5,12 +5,12 @@
 
 #include <cuda_runtime.h>
 
-#include "comba.cuh"
-#include "decode.cuh"
+#include "kernel_args.h"
 
 namespace gdn {
 
 void launch_decode(DecodeArgs a, int B, int Dk, cudaStream_t stream);
 void launch_comba(const CombaArgs& a, int heads, int K, int V, cudaStream_t stream);
+void launch_window(const WindowArgs& a, int N, cudaStream_t stream);
 
 }  // namespace gdn

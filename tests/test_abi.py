@@ -70,3 +70,17 @@ def test_comba_validation(lib):
     assert f(ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 64), P, P, P, P, P, P, P, 0, 1,
              1, 128, 128, 1.0, N) == gdn.GDN_ERR_INVALID_ARG
     assert f(N, N, N, N, N, N, N, N, N, 0, 0, 4, 128, 128, 1.0, N) == gdn.GDN_OK
+
+
+def test_window_validation(lib):
+    f = lib.gdn_window_fused
+    args = [P] * 12
+    assert f(*args, 1, 2, 4, 9, 1, 1e-6, N) == gdn.GDN_ERR_UNSUPPORTED     # ntok > 8
+    assert f(*args, 1, 4, 2, 2, 1, 1e-6, N) == gdn.GDN_ERR_UNSUPPORTED     # h_k > h_v
+    assert f(*args, 1, 2, 4, 3, 0x104, 1e-6, N) == gdn.GDN_ERR_INVALID_ARG  # commit after token 4 of 3
+    assert f(*args, 1, 2, 4, 3, 2, 1e-6, N) == gdn.GDN_ERR_INVALID_ARG      # unknown commit code
+    assert f(*([N] * 12), 0, 2, 4, 3, 1, 1e-6, N) == gdn.GDN_OK            # N = 0
+    # hist_out aliasing hist
+    h = ctypes.c_void_p(1 << 24)
+    a = [P, h, h] + [P] * 9
+    assert f(*a, 1, 2, 4, 3, 1, 1e-6, N) == gdn.GDN_ERR_INVALID_ARG
