@@ -162,19 +162,73 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 
 }  // extern "C"
 
-extern "C" {
-
-size_t gdn_prefill_workspace_size(int, int64_t, int, int, int, int, int) { return 0; }
-
-gdn_status gdn_prefill_chunked(const void*, const void*, const void*, const void*, const void*,
-                               const float*, const float*, float*, int, const int64_t*,
-                               const int64_t*, int, int64_t, int, int, int, int, int, float, void*,
-                               void*, size_t, int32_t*, gdn_stream_t) {
-    return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: not available yet");
+// ------------------------------------------------------------------------------------------------
+extern "C" size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                             int chunk_size) {
+    (void)num_seqs; (void)T; (void)Hk; (void)Hv; (void)K; (void)V; (void)chunk_size;
+    return 0;  // the chunk state lives in shared memory and TMEM
 }
 
+extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
+                                          const void* b, const float* A_log, const float* dt_bias,
+                                          float* state_pool, int pool_size,
+                                          const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                          int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                          int chunk_size, float scale, void* out, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status,
+                                          gdn_stream_t stream) {
+    (void)workspace; (void)workspace_bytes;
+    REQUIRE(num_seqs >= 0 && T >= 0 && pool_size >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1,
+            GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: sizes must be num_seqs, T, pool_size >= 0 and Hk, Hv, K, V >= 1");
+    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: Hv (%d) must be a multiple of Hk (%d)", Hv, Hk);
+    REQUIRE(K == 128 && V == 128, GDN_ERR_UNSUPPORTED,
+            "gdn_prefill_chunked: K and V must be 128 (got K=%d V=%d)", K, V);
+    REQUIRE(chunk_size == 64, GDN_ERR_UNSUPPORTED,
+            "gdn_prefill_chunked: chunk_size must be 64 (got %d)", chunk_size);
+    if (num_seqs == 0) return GDN_OK;
+    REQUIRE(cache_indices && cu_seqlens && dev_status && A_log && dt_bias && state_pool,
+            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: null pointer");
+    REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: null token pointer");
+    REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(state_pool, 16),
+            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: q, k, v and state_pool must be 16-byte aligned");
+    REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(out, 2) && aligned(A_log, 4) &&
+                aligned(dt_bias, 4) && aligned(dev_status, 4) && aligned(cache_indices, 8) &&
+                aligned(cu_seqlens, 8),
+            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: misaligned argument");
+    const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
+    REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: out overlaps state_pool");
+    REQUIRE((long long)num_seqs * Hv < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: grid too large");
 
-}  // extern "C"
+    gdn::PrefillArgs p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.a = static_cast<const uint16_t*>(a);
+    p.b = static_cast<const uint16_t*>(b);
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.state_pool = state_pool;
+    p.cache_indices = cache_indices;
+    p.cu_seqlens = cu_seqlens;
+    p.out = static_cast<uint16_t*>(out);
+    p.status = dev_status;
+    p.T = T;
+    p.pool_size = pool_size;
+    p.num_seqs = num_seqs;
+    p.Hk = Hk;
+    p.Hv = Hv;
+    p.scale = scale;
+    p.eps = 1e-6f;
+    const cudaError_t e = gdn::launch_prefill(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "gdn_prefill_chunked: launch failed: %s", cudaGetErrorString(e));
+    g_last_error[0] = '\0';
+    return GDN_OK;
+}
+
 
 // ------------------------------------------------------------------------------------------------
 extern "C" gdn_status gdn_window_fused(float* state, const float* hist, float* hist_out,

@@ -52,6 +52,24 @@ struct WindowArgs {
     float eps;
 };
 
+struct PrefillArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const uint16_t* a;
+    const uint16_t* b;
+    const float* A_log;
+    const float* dt_bias;
+    float* state_pool;
+    const int64_t* cache_indices;
+    const int64_t* cu_seqlens;
+    uint16_t* out;
+    int32_t* status;
+    long long T;
+    int pool_size, num_seqs, Hk, Hv;
+    float scale, eps;
+};
+
 constexpr int kWinD = 128;       // head dim
 constexpr int kWinHalf = 64;     // columns per CTA
 constexpr int kWinThreads = 128;

@@ -1,0 +1,160 @@
+"""GPU parity of gdn_prefill_chunked (through the C ABI) against the sequential CPU oracle.
+
+Tolerances (max |gpu - oracle| / max |oracle| per tensor): outputs (bf16) <= 5e-3, final state
+<= 2e-3.  Integer behaviour is bit-exact: cache_indices gather and scatter, cu_seqlens segmentation,
+and pool slots that no sequence references stay bitwise untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_inputs as gi
+import gated_deltanet_delta_gb300 as gdn
+import oracle
+from gpu_util import dev, host, library
+from parity import max_rel_err
+
+pytestmark = pytest.mark.gpu
+OUT_TOL, STATE_TOL = 5e-3, 2e-3
+SENTINEL = -1000.0  # exactly representable in bf16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    library()
+
+
+def _to_dev(x):
+    b16, f32, i64 = torch.bfloat16, torch.float32, torch.int64
+    return {n: dev(x[n], dt) for n, dt in (("q", b16), ("k", b16), ("v", b16), ("a", b16),
+                                           ("b", b16), ("A_log", f32), ("dt_bias", f32),
+                                           ("state_pool", f32), ("cache_indices", i64),
+                                           ("cu_seqlens", i64))}
+
+
+def _gpu(d, scale, out_fill=SENTINEL):
+    T, Hv = d["v"].shape[0], d["v"].shape[1]
+    out = torch.full((T, Hv, 128), out_fill, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                            d["state_pool"], d["cache_indices"], d["cu_seqlens"], 64, scale=scale,
+                            out=out, dev_status=status)
+    torch.cuda.synchronize()
+    return out, int(status.item())
+
+
+def _check_all(x, d, out, scale):
+    pool_ref, out_ref, st = oracle.gdn_prefill(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"],
+                                               x["dt_bias"], x["state_pool"], x["cache_indices"],
+                                               x["cu_seqlens"], scale)
+    assert st == 0
+    pool = host(d["state_pool"])
+    ci = [int(c) for c in x["cache_indices"]]
+    cu = x["cu_seqlens"]
+    o = host(out)
+    for n, slot in enumerate(ci):
+        if cu[n + 1] > cu[n]:
+            assert max_rel_err(o[cu[n]:cu[n + 1]], out_ref[cu[n]:cu[n + 1]]) <= OUT_TOL, n
+            assert max_rel_err(pool[slot], pool_ref[slot]) <= STATE_TOL, n
+        else:
+            assert np.array_equal(pool[slot], x["state_pool"][slot].astype(np.float64))
+    for s in range(pool.shape[0]):
+        if s not in ci:
+            assert np.array_equal(pool[s], x["state_pool"][s].astype(np.float64)), s
+
+
+@pytest.mark.parametrize("mild", [False, True])
+@pytest.mark.parametrize("seqlens", [[1], [63], [65, 100], [64, 0, 130, 1, 7]])
+def test_small_varlen(seqlens, mild):
+    x = gi.gdn_prefill_inputs(gi.rng(sum(seqlens) + mild), seqlens, 2, 4, 128, 128,
+                              pool=len(seqlens) + 3, mild_gates=mild)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_long_mild_sequence_carries_the_state():
+    # 40 chunks with slow decay: the carried state matters for every chunk
+    x = gi.gdn_prefill_inputs(gi.rng(3), [2560 + 17], 1, 2, 128, 128, pool=2, mild_gates=True)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_full_workload_sampled_units():
+    # T = 15360 over 4096 + 2048 + 1024 + 8192 tokens, Hk=16, Hv=32: the whole call on the GPU,
+    # the oracle on a sample of (sequence, value head) units, including the 8192-token sequence.
+    c = gi.GDN_PREFILL
+    x = gi.gdn_prefill_inputs(gi.rng(0), c["seqlens"], c["Hk"], c["Hv"], c["K"], c["V"],
+                              c["pool"])
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    o, pool = host(out), host(d["state_pool"])
+    cu, ci = x["cu_seqlens"], x["cache_indices"]
+    for (n, h) in [(0, 0), (1, 17), (2, 31), (3, 0), (3, 5), (3, 31)]:
+        sl = slice(cu[n], cu[n + 1])
+        S, o_ref = oracle.gdn_prefill_unit(x["q"][sl], x["k"][sl], x["v"][sl], x["a"][sl],
+                                           x["b"][sl], x["A_log"][h], x["dt_bias"][h],
+                                           x["state_pool"][ci[n], h], h, scale)
+        assert max_rel_err(o[sl, h], o_ref) <= OUT_TOL, (n, h)
+        assert max_rel_err(pool[ci[n], h], S) <= STATE_TOL, (n, h)
+    for s in range(c["pool"]):
+        if s not in set(int(i) for i in ci):
+            assert np.array_equal(pool[s], x["state_pool"][s].astype(np.float64))
+
+
+def test_split_call_equals_one_call():
+    # one sequence as one call, and as two calls that carry the state through the pool
+    x = gi.gdn_prefill_inputs(gi.rng(9), [200], 1, 2, 128, 128, pool=1, mild_gates=True)
+    scale = 128 ** -0.5
+    d1 = _to_dev(x)
+    out1, _ = _gpu(d1, scale)
+    d2 = _to_dev(x)
+    first = dict(d2, cu_seqlens=dev(np.array([0, 128]), torch.int64))
+    outa, _ = _gpu(first, scale)
+    second = {k: (v[128:].contiguous() if k in ("q", "k", "v", "a", "b") else v) for k, v in d2.items()}
+    second["cu_seqlens"] = dev(np.array([0, 72]), torch.int64)
+    outb, _ = _gpu(second, scale)
+    both = torch.cat([outa[:128], outb], dim=0)
+    o1, o2 = host(out1), host(both)
+    assert max_rel_err(o2, o1) <= OUT_TOL
+    assert max_rel_err(host(d2["state_pool"]), host(d1["state_pool"])) <= STATE_TOL
+
+
+def test_bad_slots_and_bounds_are_flagged_and_skipped():
+    x = gi.gdn_prefill_inputs(gi.rng(11), [70, 30], 1, 2, 128, 128, pool=3)
+    scale = 128 ** -0.5
+    x["cache_indices"] = np.array([5, 1], dtype=np.int64)   # 5 is outside the pool of 3
+    d = _to_dev(x)
+    out, st = _gpu(d, scale)
+    assert st & gdn.STATUS_BAD_CACHE_INDEX
+    o = host(out)
+    assert np.all(o[:70] == SENTINEL)              # skipped sequence: out not written
+    pool = host(d["state_pool"])
+    assert np.array_equal(pool[0], x["state_pool"][0].astype(np.float64))
+    assert np.array_equal(pool[2], x["state_pool"][2].astype(np.float64))
+    pool_ref, out_ref, _ = oracle.gdn_prefill(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"],
+                                              x["dt_bias"], x["state_pool"], x["cache_indices"],
+                                              x["cu_seqlens"], scale)
+    assert max_rel_err(o[70:], out_ref[70:]) <= OUT_TOL
+    assert max_rel_err(pool[1], pool_ref[1]) <= STATE_TOL
+    x["cache_indices"] = np.array([0, 1], dtype=np.int64)
+    x["cu_seqlens"] = np.array([0, 80, 60], dtype=np.int64)  # decreasing bound
+    d = _to_dev(x)
+    _, st = _gpu(d, scale)
+    assert st & gdn.STATUS_BAD_SEQLENS
+
+
+def test_rejections():
+    x = gi.gdn_prefill_inputs(gi.rng(12), [10], 1, 2, 128, 128, pool=1)
+    d = _to_dev(x)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                d["state_pool"], d["cache_indices"], d["cu_seqlens"], 128)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
