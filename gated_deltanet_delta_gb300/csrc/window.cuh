@@ -12,16 +12,21 @@
 // 0x100|k: token k; 0: never).
 //
 // GB300 mapping.  A CTA of 128 threads owns one (n, h) head's 128 x 64 half of the state (columns
-// 64*half ..): thread (c, rg) holds column group c (4 columns, one float4) of the 16 rows rg, rg+8,
-// ..., in registers for the whole window, so the 64 KB head state is read from HBM once and written
-// at most once.  A warp's load covers two 256-byte row pieces.  The reductions over the rows (kv, o)
-// run serially in registers, then over the two row groups of a warp with one shuffle, then over the
-// four warps through shared memory.  The two halves of a head form a thread-block cluster of 2: the
-// output RMSNorm needs sum_j o_j^2 over all 128 columns, so each half keeps its o_t and partial sums
-// for every token in shared memory and the pair exchanges the partial sums once, through
-// distributed shared memory, after the last token.  Each CTA convolves the 256 q/k channels of key
-// head hk and its own 64 v channels (thread t: q channel t, k channel t, v channel t < 64), with
-// histories and taps in registers, and prefetches the next token's inputs a token ahead.
+// 64*half ..): thread (c, rg) holds column group c (4 columns) of the 16 consecutive rows
+// 16rg .. 16rg+15 in registers for the whole window, so the 64 KB head state is read from HBM once
+// and written at most once; a warp's load covers two 256-byte row pieces.  The kernel is bound by
+// instruction issue, not by memory, so the per-element work is cut to three packed f32x2 FMAs per
+// two elements and token: the state is held as c * R with a per-head scalar c (the gate multiplies
+// c, and R += k (rk delta / c) is the rank-1 update; c is folded back into R when it drops below
+// 2^-40), and the L2 norms of q and k are applied to the reduced sums instead of every row.  The
+// reductions over the rows (kv, o) run serially in registers, then over the two row groups of a
+// warp with one shuffle, then over the four warps through shared memory.  The two halves of a head
+// form a thread-block cluster of 2: the output RMSNorm needs sum_j o_j^2 over all 128 columns, so
+// each half keeps its o_t and partial sums for every token in shared memory and the pair exchanges
+// the partial sums once, through distributed shared memory, after the last token.  Each CTA
+// convolves the 256 q/k channels of key head hk and its own 64 v channels (thread t: q channel t,
+// k channel t, v channel t < 64), with histories and taps in registers, and prefetches the next
+// token's inputs a token ahead.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -31,9 +36,14 @@
 
 namespace gdn {
 
-__device__ __forceinline__ float silu_f32(float s) { return s / (1.0f + expf(-s)); }
+__device__ __forceinline__ float silu_f32(float s) { return __fdividef(s, 1.0f + __expf(-s)); }
 __device__ __forceinline__ float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float softplus_f32(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+// The state of a head half is kept as c * R (c a per-head scalar, R in registers): the gate then
+// scales c, not every element, and the rank-1 update becomes R += k (rk delta / c).  When c drops
+// below kWinRenorm it is folded back into R.
+constexpr float kWinRenorm = 9.094947e-13f;  // 2^-40
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     gdn_window_kernel(const WindowArgs a) {
@@ -41,7 +51,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     constexpr int D = kWinD, CG = kWinHalf / 4, RG = kWinThreads / CG, NR = D / RG;
     static_assert(CG == 16 && RG == 8 && NR == 16, "window tile");
 
-    __shared__ float qraw[D], kraw[D], vraw[kWinHalf];
+    __shared__ __align__(16) float qraw[D];
+    __shared__ __align__(16) float kraw[D];
+    __shared__ __align__(16) float vraw[kWinHalf];
     __shared__ float part_q[4], part_k[4], gb[2];
     __shared__ float4 red_kv[4][CG], red_o[4][CG];
     __shared__ float osm[kWinMaxTok][kWinHalf];
@@ -58,13 +70,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     const int C = (2 * a.h_k + a.h_v) * D;
     const int ntok = a.ntok;
 
-    // ---- the state half in registers: rows rg + RG*m, columns half*64 + 4c .. +3
+    // ---- the state half in registers: rows rg*16 .. rg*16+15, columns half*64 + 4c .. +3
     const size_t row_stride = size_t(a.h_v) * D;  // floats between consecutive rows i
     float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + half * kWinHalf + 4 * c;
-    float4 s[NR];
+    float2 R[NR][2];
 #pragma unroll
-    for (int m = 0; m < NR; ++m)
-        s[m] = ld_stream(reinterpret_cast<const float4*>(sbase + size_t(rg + RG * m) * row_stride));
+    for (int m = 0; m < NR; ++m) {
+        const float4 x = ld_stream(reinterpret_cast<const float4*>(sbase + size_t(rg * NR + m) * row_stride));
+        R[m][0] = make_float2(x.x, x.y);
+        R[m][1] = make_float2(x.z, x.w);
+    }
+    float cs = 1.0f;  // S = cs * R
 
     // ---- this thread's conv channels: q and k of key head hk, and (tid < 64) one v channel
     const int ch_q = hk * D + tid;
@@ -143,17 +159,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         const float rk = rsqrtf(((part_k[0] + part_k[1]) + (part_k[2] + part_k[3])) + a.eps);
         const float rq = rsqrtf(((part_q[0] + part_q[1]) + (part_q[2] + part_q[3])) + a.eps);
         const float gate = gb[0], beta = gb[1];
+        const float4* k4 = reinterpret_cast<const float4*>(kraw + rg * NR);
+        const float4* q4 = reinterpret_cast<const float4*>(qraw + rg * NR);
 
-        // kv over this thread's rows, then over the warp's two row groups and the four warps
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+        // kv = cs rk sum_i R_ij k_i: this thread's 16 rows, the warp's two row groups, four warps
+        float2 kva = make_float2(0.f, 0.f), kvb = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < NR; ++m) {
-            const float ki = kraw[rg + RG * m] * rk;
-            kv.x = fmaf(s[m].x, ki, kv.x);
-            kv.y = fmaf(s[m].y, ki, kv.y);
-            kv.z = fmaf(s[m].z, ki, kv.z);
-            kv.w = fmaf(s[m].w, ki, kv.w);
+        for (int m4 = 0; m4 < NR / 4; ++m4) {
+            const float4 kk = k4[m4];
+            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 k2 = make_float2(kr[u], kr[u]);
+                kva = __ffma2_rn(R[m4 * 4 + u][0], k2, kva);
+                kvb = __ffma2_rn(R[m4 * 4 + u][1], k2, kvb);
+            }
         }
+        float4 kv = make_float4(kva.x, kva.y, kvb.x, kvb.y);
         kv.x += __shfl_xor_sync(kFullMask, kv.x, 16);
         kv.y += __shfl_xor_sync(kFullMask, kv.y, 16);
         kv.z += __shfl_xor_sync(kFullMask, kv.z, 16);
@@ -168,30 +190,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             kv.w = (r0.w + r1.w) + (r2.w + r3.w);
         }
         const float4 vv = reinterpret_cast<const float4*>(vraw)[c];
-        const float4 dl = make_float4((vv.x - gate * kv.x) * beta, (vv.y - gate * kv.y) * beta,
-                                      (vv.z - gate * kv.z) * beta, (vv.w - gate * kv.w) * beta);
-
-        // rank-1 update with the gate, and the readout partial
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float gk = gate * cs * rk;  // gate * kv_j = gk * (reduced sum)
+        // delta_j = (v_j - gate kv_j) beta;  the update R += k (rk delta / cs'), cs' = gate cs
+        float cn = gate * cs;
+        if (cn < kWinRenorm) {  // uniform over the CTA: fold cs' into R
 #pragma unroll
-        for (int m = 0; m < NR; ++m) {
-            const int i = rg + RG * m;
-            const float ki = kraw[i] * rk;
-            const float qi = qraw[i] * rq;
-            s[m].x = fmaf(gate, s[m].x, ki * dl.x);
-            s[m].y = fmaf(gate, s[m].y, ki * dl.y);
-            s[m].z = fmaf(gate, s[m].z, ki * dl.z);
-            s[m].w = fmaf(gate, s[m].w, ki * dl.w);
-            o.x = fmaf(s[m].x, qi, o.x);
-            o.y = fmaf(s[m].y, qi, o.y);
-            o.z = fmaf(s[m].z, qi, o.z);
-            o.w = fmaf(s[m].w, qi, o.w);
+            for (int m = 0; m < NR; ++m) {
+                const float2 c2 = make_float2(cn, cn);
+                R[m][0] = __fmul2_rn(R[m][0], c2);
+                R[m][1] = __fmul2_rn(R[m][1], c2);
+            }
+            cn = 1.0f;
+        }
+        const float ek = beta * rk / cn;
+        const float2 ea = make_float2((vv.x - gk * kv.x) * ek, (vv.y - gk * kv.y) * ek);
+        const float2 eb = make_float2((vv.z - gk * kv.z) * ek, (vv.w - gk * kv.w) * ek);
+        cs = cn;
+
+        // rank-1 update and the readout partial sum_i R_ij q_i
+        float2 oa = make_float2(0.f, 0.f), ob = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m4 = 0; m4 < NR / 4; ++m4) {
+            const float4 kk = k4[m4];
+            const float4 qq = q4[m4];
+            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+            const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int m = m4 * 4 + u;
+                const float2 k2 = make_float2(kr[u], kr[u]);
+                const float2 q2 = make_float2(qr[u], qr[u]);
+                R[m][0] = __ffma2_rn(k2, ea, R[m][0]);
+                R[m][1] = __ffma2_rn(k2, eb, R[m][1]);
+                oa = __ffma2_rn(R[m][0], q2, oa);
+                ob = __ffma2_rn(R[m][1], q2, ob);
+            }
         }
         if (t + 1 == a.commit_at) {
 #pragma unroll
             for (int m = 0; m < NR; ++m)
-                st_stream(reinterpret_cast<float4*>(sbase + size_t(rg + RG * m) * row_stride), s[m]);
+                st_stream(reinterpret_cast<float4*>(sbase + size_t(rg * NR + m) * row_stride),
+                          make_float4(cs * R[m][0].x, cs * R[m][0].y, cs * R[m][1].x, cs * R[m][1].y));
         }
+        float4 o = make_float4(oa.x, oa.y, ob.x, ob.y);
         o.x += __shfl_xor_sync(kFullMask, o.x, 16);
         o.y += __shfl_xor_sync(kFullMask, o.y, 16);
         o.z += __shfl_xor_sync(kFullMask, o.z, 16);
@@ -203,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             if (lane < CG) {
                 const float4 r0 = red_o[0][lane], r1 = red_o[1][lane], r2 = red_o[2][lane],
                              r3 = red_o[3][lane];
-                const float sc = 0.08838834764831845f;  // 1 / sqrt(128)
+                const float sc = cs * rq * 0.08838834764831845f;  // cs rq / sqrt(128)
                 const float4 ot = make_float4(((r0.x + r1.x) + (r2.x + r3.x)) * sc,
                                               ((r0.y + r1.y) + (r2.y + r3.y)) * sc,
                                               ((r0.z + r1.z) + (r2.z + r3.z)) * sc,
