@@ -499,7 +499,8 @@ def main():
                          "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
                          "frac": roof / t1, "note": peak_note,
                          "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
-                         "traffic": None}}
+                         "traffic": profiled_traffic("gdn_prefill_kernel",
+                                                     "gated_deltanet_delta_gb300/csrc/prefill.cuh")}}
     elif "prefill" in extra:
         ops["prefill_chunked"] = extra["prefill"]
     for key in ("window_verify", "window_commit"):
@@ -511,7 +512,10 @@ def main():
                         "us_per_call": t1 * 1e6,
                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
                                      "unit": "GB/s", "frac": gbs / hbm_peak, "note": peak_note,
-                                     "traffic": None}}
+                                     "traffic": profiled_traffic(
+                                         "gdn_window_kernel",
+                                         "gated_deltanet_delta_gb300/csrc/window.cuh")
+                                     if key == "window_verify" else None}}
         elif key in extra:
             ops[key] = w
 

@@ -2,6 +2,7 @@
 // streaming loads and stores, warp reductions).  Nothing here is specific to one operation.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,6 +25,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
     if ((u & 0x7fffffffu) > 0x7f800000u) return uint16_t((u >> 16) | 0x40u);  // quiet NaN
     u += 0x7fffu + ((u >> 16) & 1u);
     return uint16_t(u >> 16);
+}
+
+// Two floats rounded to bf16 (nearest even, hardware conversion) packed as (lo, hi) halves.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Streaming 16-byte load / store: the state is touched once per call, so it is not kept in L1 and

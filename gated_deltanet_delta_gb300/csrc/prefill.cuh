@@ -15,9 +15,11 @@
 // with D_ts = e^{G_t-G_s} for s <= t (0 above the diagonal), gamma_t = e^{G_t}, D_L = D_{L-1,.}.
 // The page's w recursion is read untransposed and its "U^T K" as U K^T (the [V, K] state layout).
 //
-// GB300 mapping.  One CTA of 128 threads per (sequence, value head); thread i <-> TMEM lane i.  The
-// fp32 state S (V x K = 128 x 128) lives in TMEM for the whole sequence and reaches HBM only at the
-// start (gather from the pool slot) and at the end (scatter back).  Every contraction is a
+// GB300 mapping.  One CTA of 256 threads per (sequence, value head); threads i and i + 128 share
+// TMEM lane i (each takes half of the columns).  The fp32 state S (V x K = 128 x 128) lives in TMEM
+// for the whole sequence and reaches HBM only at the start (gather from the pool slot) and at the
+// end (scatter back).  The next chunk's q, k, v rows are loaded into registers while the current
+// chunk's state-dependent MMAs run.  Every contraction is a
 // tcgen05.mma with M = 128 (the transposed forms keep V or the feature index on M):
 //     G   = [K; Q] K^T              M=128 (64 k rows + 64 q rows), N=64,  K=128   bf16 (exact inputs)
 //     W^T = K^T Tw^T,  U^T = V^T Tu^T   M=128, N=64, K=64   (Tw = T diag(beta gamma rk), Tu = T diag(beta))
@@ -41,9 +43,10 @@
 namespace gdn {
 
 namespace pf {
-constexpr int C = 64;    // chunk size
-constexpr int D = 128;   // K = V = 128
-constexpr int NT = 128;  // threads per CTA
+constexpr int C = 64;     // chunk size
+constexpr int D = 128;    // K = V = 128
+constexpr int NT = 256;   // threads per CTA
+constexpr int LST = 65;   // row stride (floats) of the fp32 Lm and T matrices: column walks are conflict-free
 // dynamic shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;       // [K;Q] tile: two 64-feature halves of 16 KB, each 64 k rows + 64 q rows
 constexpr uint32_t OFF_V = 32768;    // V tile: two halves of 8 KB (64 token rows)
@@ -52,10 +55,10 @@ constexpr uint32_t OFF_W = 81920;    // W as MN-major B operand: 128 feature row
 constexpr uint32_t OFF_T4 = 98304;   // Tw hi, Tw lo, Tu hi, Tu lo (8 KB each); later Delta~ hi, lo (16 KB each)
 constexpr uint32_t OFF_DL = 131072;  // Delta^T hi, lo (16 KB each): 128 v rows x 64 s
 constexpr uint32_t OFF_M = 163840;   // M hi, lo (8 KB each): 64 t rows x 64 s
-constexpr uint32_t OFF_L = 180224;   // fp32 [64][64] strictly lower Lm
-constexpr uint32_t OFF_T = 196608;   // fp32 [64][64] T = (I + Lm)^-1
-constexpr uint32_t OFF_X = 212992;   // fp32 [16][48] scratch of the blockwise inverse
-constexpr uint32_t SMEM_USED = 216064;
+constexpr uint32_t OFF_L = 180224;   // fp32 [64][LST] strictly lower Lm
+constexpr uint32_t OFF_T = OFF_L + 64 * LST * 4;  // fp32 [64][LST] T = (I + Lm)^-1
+constexpr uint32_t OFF_X = OFF_T + 64 * LST * 4;  // fp32 [16][48] scratch of the blockwise inverse
+constexpr uint32_t SMEM_USED = OFF_X + 16 * 48 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 // TMEM columns (fp32, 128 lanes)
 constexpr uint32_t TM_S = 0, TM_G = 128, TM_W = 192, TM_U = 256, TM_P = 320, TM_MD = 384;
@@ -65,22 +68,19 @@ constexpr uint32_t kWaitLimit = 1u << 26;  // mbarrier polls before giving up (s
 
 // Pack 8 floats to 8 bf16 (round to nearest even) in a uint4.
 __device__ __forceinline__ uint4 pack_bf16x8(const float* x) {
-    uint4 r;
-    r.x = uint32_t(f32_to_bf16_rne(x[0])) | (uint32_t(f32_to_bf16_rne(x[1])) << 16);
-    r.y = uint32_t(f32_to_bf16_rne(x[2])) | (uint32_t(f32_to_bf16_rne(x[3])) << 16);
-    r.z = uint32_t(f32_to_bf16_rne(x[4])) | (uint32_t(f32_to_bf16_rne(x[5])) << 16);
-    r.w = uint32_t(f32_to_bf16_rne(x[6])) | (uint32_t(f32_to_bf16_rne(x[7])) << 16);
-    return r;
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
 }
 // Split 8 floats into bf16 high parts and bf16 low parts (x - hi, rounded).
 __device__ __forceinline__ void split_bf16x8(const float* x, uint4& hi, uint4& lo) {
-    float h[8], l[8];
+    hi = pack_bf16x8(x);
+    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    float l[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        h[i] = bf16_to_f32(f32_to_bf16_rne(x[i]));
-        l[i] = x[i] - h[i];
+    for (int i = 0; i < 4; ++i) {
+        l[2 * i] = x[2 * i] - __uint_as_float(hw[i] << 16);
+        l[2 * i + 1] = x[2 * i + 1] - __uint_as_float(hw[i] & 0xffff0000u);
     }
-    hi = pack_bf16x8(h);
     lo = pack_bf16x8(l);
 }
 __device__ __forceinline__ float bf16_sumsq8(const uint4& p) {
@@ -89,13 +89,23 @@ __device__ __forceinline__ float bf16_sumsq8(const uint4& p) {
     return fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w,
            fmaf(b.x, b.x, fmaf(b.y, b.y, fmaf(b.z, b.z, b.w * b.w)))))));
 }
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+    float a[16], b[16];
+    tc::ld16(taddr, a);
+    tc::ld16(taddr + 16, b);
+    tc::wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = a[i];
+        v[16 + i] = b[i];
+    }
+}
 
 __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArgs a) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ double Gd[C];
-    __shared__ float betas[C], rks[C], rqs[C], gams[C], dls[C];
-    __shared__ double scan_total;
+    __shared__ float Gf[C], betas[C], rks[C], rqs[C], gams[C], dls[C];
+    __shared__ float scan_total;
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(8) uint64_t mbar;
 
@@ -103,6 +113,8 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
     const int h = blockIdx.x - n * a.Hv;
     const int hk = h / (a.Hv / a.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & 127;   // the TMEM lane this thread reads and writes
+    const int half = tid >> 7;   // which half of the columns
 
     // ---- sequence bounds and pool slot (uniform over the CTA; bad ones are flagged and skipped)
     const long long bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
@@ -126,22 +138,22 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
 
     if (warp == 0) tc::tmem_alloc(&tmem_slot, TM_COLS);
     if (tid == 0) tc::mbar_init(&mbar, 1);
+    // T's blocks above the diagonal stay zero for the whole kernel
+    for (int i = tid; i < C * LST; i += NT) Ts[i] = 0.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = tmem_slot;
-    const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lane base
+    const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
     uint32_t phase = 0;
     bool timed_out = false;
 
-    // wait for the MMAs committed so far; returns false (on every thread) after a timeout
     auto mma_wait = [&]() -> bool {
         const bool ok = tc::mbar_wait(&mbar, phase, kWaitLimit);
         phase ^= 1u;
         tc::fence_after();
         return __syncthreads_and(ok ? 1 : 0) != 0;
     };
-    // make this thread's shared-memory and TMEM writes visible to the MMAs issued next
     auto publish = [&]() {
         tc::wait_st();
         tc::fence_proxy_async();
@@ -150,95 +162,105 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
         tc::fence_after();
     };
 
-    // ---- gather the state from its pool slot: row v = tid -> TMEM (fp32) and S0 tile (bf16)
+    // ---- gather the state from its pool slot: row v, columns 64*half .. -> TMEM and S0 (bf16)
     float* Sg = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * D * D;
     {
-        const float4* row = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(tid) * D);
+        const float4* src = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row) * D + 64 * half);
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
+        for (int c16 = 0; c16 < 4; ++c16) {
             float v[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 f = row[c16 * 4 + j];
+                const float4 f = src[c16 * 4 + j];
                 v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
             }
-            tc::st16(tm + lrow + TM_S + c16 * 16, v);
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(tid, 2 * c16, 128)) = pack_bf16x8(v);
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(tid, 2 * c16 + 1, 128)) = pack_bf16x8(v + 8);
+            tc::st16(trow + TM_S + 64 * half + c16 * 16, v);
+            const int c8 = 8 * half + 2 * c16;
+            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8, 128)) = pack_bf16x8(v);
+            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + 1, 128)) = pack_bf16x8(v + 8);
         }
     }
-    publish();
 
     const float a_mul = expf(a.A_log[h]);
     const float dtb = a.dt_bias[h];
     const size_t qk_stride = static_cast<size_t>(a.Hk) * D;  // elements between tokens of q, k
     const size_t vo_stride = static_cast<size_t>(a.Hv) * D;  // elements between tokens of v, out
 
+    // q, k, v rows of one chunk in registers: thread (rp, ch) holds 16-byte chunk ch of rows rp + 16p
+    const int rp = tid >> 4, ch = tid & 15;
+    uint4 kr[4], qr[4], vr[4];
+    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < 64)
+    auto load_tiles = [&](long long c0) {
+        const long long L = Tn - c0 < C ? Tn - c0 : C;
+        if (tid < L) {
+            const size_t gi = static_cast<size_t>(bos + c0 + tid) * a.Hv + h;
+            a_raw = a.a[gi];
+            b_raw = a.b[gi];
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int s = p * 16 + rp;
+            if (s < L) {
+                const size_t t = static_cast<size_t>(bos + c0 + s);
+                kr[p] = *reinterpret_cast<const uint4*>(a.k + t * qk_stride + hk * D + ch * 8);
+                qr[p] = *reinterpret_cast<const uint4*>(a.q + t * qk_stride + hk * D + ch * 8);
+                vr[p] = *reinterpret_cast<const uint4*>(a.v + t * vo_stride + h * D + ch * 8);
+            } else {
+                kr[p] = qr[p] = vr[p] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    };
+    load_tiles(0);
+    publish();
+
     for (long long c0 = 0; c0 < Tn && !timed_out; c0 += C) {
         const int L = static_cast<int>(Tn - c0 < C ? Tn - c0 : C);
         const long long tok0 = bos + c0;
 
-        // ---- 1. k, q, v tiles (zero past the sequence end) and the row norms
-        {
-            const int rp = tid >> 4, ch = tid & 15;
-            uint4 kr[8], qr[8], vr[8];
+        // ---- 1. this chunk's tiles (already in registers) to shared memory, and the row norms
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int s = p * 8 + rp;
-                if (s < L) {
-                    const size_t t = static_cast<size_t>(tok0 + s);
-                    kr[p] = *reinterpret_cast<const uint4*>(a.k + t * qk_stride + hk * D + ch * 8);
-                    qr[p] = *reinterpret_cast<const uint4*>(a.q + t * qk_stride + hk * D + ch * 8);
-                    vr[p] = *reinterpret_cast<const uint4*>(a.v + t * vo_stride + h * D + ch * 8);
-                } else {
-                    kr[p] = qr[p] = vr[p] = make_uint4(0u, 0u, 0u, 0u);
-                }
+        for (int p = 0; p < 4; ++p) {
+            const int s = p * 16 + rp;
+            *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(s, ch, 128)) = kr[p];
+            *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(64 + s, ch, 128)) = qr[p];
+            *reinterpret_cast<uint4*>(sm + OFF_V + tc::sw_chunk(s, ch, 64)) = vr[p];
+            float sk = bf16_sumsq8(kr[p]), sq = bf16_sumsq8(qr[p]);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                sk += __shfl_xor_sync(kFullMask, sk, o);
+                sq += __shfl_xor_sync(kFullMask, sq, o);
             }
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int s = p * 8 + rp;
-                *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(s, ch, 128)) = kr[p];
-                *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(64 + s, ch, 128)) = qr[p];
-                *reinterpret_cast<uint4*>(sm + OFF_V + tc::sw_chunk(s, ch, 64)) = vr[p];
-                float sk = bf16_sumsq8(kr[p]), sq = bf16_sumsq8(qr[p]);
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) {
-                    sk += __shfl_xor_sync(kFullMask, sk, o);
-                    sq += __shfl_xor_sync(kFullMask, sq, o);
-                }
-                if (ch == 0) {
-                    rks[s] = rsqrtf(sk + a.eps);
-                    rqs[s] = rsqrtf(sq + a.eps);
-                }
+            if (ch == 0) {
+                rks[s] = rsqrtf(sk + a.eps);
+                rqs[s] = rsqrtf(sq + a.eps);
             }
         }
-        // ---- 2. gates and their in-chunk cumulative sum (double, so that G_t - G_s is exact)
+        // ---- 2. gates and their in-chunk cumulative sum
         if (tid < C) {
             const int t = tid;
             float ell = 0.f, be = 0.f;
             if (t < L) {
-                const size_t gi = static_cast<size_t>(tok0 + t) * a.Hv + h;
-                const float x = bf16_to_f32(a.a[gi]) + dtb;
-                const float sp = x > 20.f ? x : log1pf(expf(x));
+                const float x = bf16_to_f32(a_raw) + dtb;
+                const float sp = x > 20.f ? x : log1pf(__expf(x));
                 ell = -a_mul * sp;
-                be = 1.f / (1.f + expf(-bf16_to_f32(a.b[gi])));
+                be = __frcp_rn(1.f + __expf(-bf16_to_f32(b_raw)));
             }
-            double g = ell;
+            float g = ell;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(kFullMask, g, o);
+                const float y = __shfl_up_sync(kFullMask, g, o);
                 if (lane >= o) g += y;
             }
             if (t == 31) scan_total = g;
             asm volatile("bar.sync 1, 64;" ::: "memory");
             if (t >= 32) g += scan_total;
-            Gd[t] = g;
+            Gf[t] = g;
             betas[t] = be;
         }
         __syncthreads();
         if (tid < C) {
-            gams[tid] = expf(static_cast<float>(Gd[tid]));
-            dls[tid] = tid < L ? expf(static_cast<float>(Gd[L - 1] - Gd[tid])) : 0.f;
+            gams[tid] = __expf(Gf[tid]);
+            dls[tid] = tid < L ? __expf(Gf[L - 1] - Gf[tid]) : 0.f;
         }
         publish();
 
@@ -255,76 +277,88 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
         }
         if (!mma_wait()) { timed_out = true; break; }
 
-        // ---- 4. Lm (rows t < 64, fp32) and M (rows 64 + t, bf16 hi / lo) from G
+        // ---- 4. Lm (lanes t < 64, fp32) and M (lanes 64 + t, bf16 hi / lo) from G, 32 columns each
         {
-            float g[64];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v16[16];
-                tc::ld16(tm + lrow + TM_G + j * 16, v16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) g[j * 16 + i] = v16[i];
-            }
-            tc::wait_ld();
-            if (tid < C) {
-                const int t = tid;
+            float g[32];
+            ld32(trow + TM_G + 32 * half, g);
+            const int s0 = 32 * half;
+            if (row < C) {
+                const int t = row;
                 const float bt = betas[t] * rks[t];
-                const double Gt = Gd[t];
+                const float Gt = Gf[t];
 #pragma unroll
-                for (int s = 0; s < C; ++s)
-                    Ls[t * C + s] = s < t ? bt * rks[s] * g[s] * __expf(static_cast<float>(Gt - Gd[s])) : 0.f;
+                for (int i = 0; i < 32; ++i) {
+                    const int s = s0 + i;
+                    Ls[t * LST + s] = s < t ? bt * rks[s] * g[i] * __expf(Gt - Gf[s]) : 0.f;
+                }
             } else {
-                const int t = tid - C;
-                const double Gt = Gd[t];
+                const int t = row - C;
+                const float Gt = Gf[t];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     float m8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int s = c * 8 + i;
-                        m8[i] = s <= t ? rks[s] * g[s] * __expf(static_cast<float>(Gt - Gd[s])) : 0.f;
+                        const int s = s0 + c * 8 + i;
+                        m8[i] = s <= t ? rks[s] * g[c * 8 + i] * __expf(Gt - Gf[s]) : 0.f;
                     }
                     uint4 hi, lo;
                     split_bf16x8(m8, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + OFF_M + tc::sw_chunk(t, c, 64)) = hi;
-                    *reinterpret_cast<uint4*>(sm + OFF_M + 8192 + tc::sw_chunk(t, c, 64)) = lo;
+                    *reinterpret_cast<uint4*>(sm + OFF_M + tc::sw_chunk(t, 4 * half + c, 64)) = hi;
+                    *reinterpret_cast<uint4*>(sm + OFF_M + 8192 + tc::sw_chunk(t, 4 * half + c, 64)) = lo;
                 }
             }
-            for (int i = tid; i < C * C; i += NT) Ts[i] = 0.f;
         }
         __syncthreads();
 
-        // ---- 5. T = (I + Lm)^-1: 16 x 16 diagonal blocks, then the off-diagonal block rows
+        // ---- 5. T = (I + Lm)^-1: 16 x 16 diagonal blocks by column-parallel forward substitution,
+        //         then block row I from T_IJ = -T_II sum_{J<=K<I} Lm_IK T_KJ
         if (tid < C) {
             const int blk = tid >> 4, j = tid & 15;
-            const float* Lb = Ls + (16 * blk) * C + 16 * blk;
+            const float* Lb = Ls + (16 * blk) * LST + 16 * blk;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int s = 0; s < i; ++s) acc = fmaf(-Lb[i * C + s], x[s], acc);
+                for (int s = 0; s < i; ++s) acc = fmaf(-Lb[i * LST + s], x[s], acc);
                 x[i] = (i < j) ? 0.f : acc;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Ts[(16 * blk + i) * C + 16 * blk + j] = x[i];
+            for (int i = 0; i < 16; ++i) Ts[(16 * blk + i) * LST + 16 * blk + j] = x[i];
         }
         __syncthreads();
+#pragma unroll
         for (int I = 1; I < 4; ++I) {
-            const int W = 16 * I;  // columns to the left of block row I
-            for (int e = tid; e < 16 * W; e += NT) {
+            const int W = 16 * I;  // columns left of block row I
+#pragma unroll
+            for (int rep = 0; rep < I; ++rep) {
+                const int e = rep * NT + tid;  // 16 * W = 256 * I elements
                 const int r = e / W, jc = e - r * W;
-                float acc = 0.f;
-                for (int k2 = jc & ~15; k2 < W; ++k2) acc = fmaf(Ls[(W + r) * C + k2], Ts[k2 * C + jc], acc);
-                Xs[r * 48 + jc] = acc;
+                const float* Lr = Ls + (W + r) * LST;
+                float acc0 = 0.f, acc1 = 0.f;
+                for (int kb = jc >> 4; kb < I; ++kb) {
+#pragma unroll
+                    for (int u = 0; u < 16; u += 2) {
+                        acc0 = fmaf(Lr[16 * kb + u], Ts[(16 * kb + u) * LST + jc], acc0);
+                        acc1 = fmaf(Lr[16 * kb + u + 1], Ts[(16 * kb + u + 1) * LST + jc], acc1);
+                    }
+                }
+                Xs[r * 48 + jc] = acc0 + acc1;
             }
             __syncthreads();
-            for (int e = tid; e < 16 * W; e += NT) {
-                const int r = e / W, jc = e - r * W;
-                float acc = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2) acc = fmaf(Ts[(W + r) * C + W + k2], Xs[k2 * 48 + jc], acc);
-                Ts[(W + r) * C + jc] = -acc;
+            for (int rep = 0; rep < I; ++rep) {
+                const int e = rep * NT + tid;
+                const int r = e / W, jc = e - r * W;
+                const float* Tr = Ts + (W + r) * LST + W;
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; u += 2) {
+                    acc0 = fmaf(Tr[u], Xs[u * 48 + jc], acc0);
+                    acc1 = fmaf(Tr[u + 1], Xs[(u + 1) * 48 + jc], acc1);
+                }
+                Ts[(W + r) * LST + jc] = -(acc0 + acc1);
             }
             __syncthreads();
         }
@@ -332,21 +366,22 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
         // ---- 6. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major)
         {
             const int t = tid & (C - 1);
-            const bool w_side = tid < C;
+            const bool w_side = ((tid >> 6) & 1) == 0;
             const uint32_t base = OFF_T4 + (w_side ? 0u : 16384u);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
+                const int cc = 4 * half + c;
                 float x8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int s = c * 8 + i;
+                    const int s = cc * 8 + i;
                     const float w = w_side ? betas[s] * gams[s] * rks[s] : betas[s];
-                    x8[i] = Ts[t * C + s] * w;
+                    x8[i] = Ts[t * LST + s] * w;
                 }
                 uint4 hi, lo;
                 split_bf16x8(x8, hi, lo);
-                *reinterpret_cast<uint4*>(sm + base + tc::sw_chunk(t, c, 64)) = hi;
-                *reinterpret_cast<uint4*>(sm + base + 8192 + tc::sw_chunk(t, c, 64)) = lo;
+                *reinterpret_cast<uint4*>(sm + base + tc::sw_chunk(t, cc, 64)) = hi;
+                *reinterpret_cast<uint4*>(sm + base + 8192 + tc::sw_chunk(t, cc, 64)) = lo;
             }
         }
         publish();
@@ -369,24 +404,19 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
         }
         if (!mma_wait()) { timed_out = true; break; }
 
-        // ---- 8. W (bf16) as the MN-major B operand: row f = tid holds W[t][f] for t = 0..63
+        // ---- 8. W (bf16) as the MN-major B operand: lane f holds W[t][f], t = 32*half ..
         {
-            float w64[64];
+            float w32[32];
+            ld32(trow + TM_W + 32 * half, w32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v16[16];
-                tc::ld16(tm + lrow + TM_W + j * 16, v16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) w64[j * 16 + i] = v16[i];
-            }
-            tc::wait_ld();
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(sm + OFF_W + tc::sw_chunk(tid, c, 128)) = pack_bf16x8(w64 + 8 * c);
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(sm + OFF_W + tc::sw_chunk(row, 4 * half + c, 128)) =
+                    pack_bf16x8(w32 + 8 * c);
         }
         publish();
 
-        // ---- 9. Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated) and P^T = S0 Q^T
+        // ---- 9. Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated) and P^T = S0 Q^T;
+        //         the next chunk's rows are fetched meanwhile
         if (tid == 0) {
             const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
             const uint32_t idp = tc::idesc_bf16(128, 64, 0, 0, 0);
@@ -400,42 +430,42 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
             }
             tc::commit(&mbar);
         }
+        if (c0 + C < Tn) load_tiles(c0 + C);
         if (!mma_wait()) { timed_out = true; break; }
 
-        // ---- 10. Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), row v = tid;
+        // ---- 10. Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 32 s each;
         //          the state is scaled by gamma_L in TMEM before the update accumulates onto it
         {
-            float d64[64];
+            float d32[32];
+            ld32(trow + TM_U + 32 * half, d32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v16[16];
-                tc::ld16(tm + lrow + TM_U + j * 16, v16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) d64[j * 16 + i] = v16[i];
-            }
-            tc::wait_ld();
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
+                const int cc = 4 * half + c;
                 uint4 hi, lo;
-                split_bf16x8(d64 + 8 * c, hi, lo);
-                *reinterpret_cast<uint4*>(sm + OFF_DL + tc::sw_chunk(tid, c, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + OFF_DL + 16384 + tc::sw_chunk(tid, c, 128)) = lo;
+                split_bf16x8(d32 + 8 * c, hi, lo);
+                *reinterpret_cast<uint4*>(sm + OFF_DL + tc::sw_chunk(row, cc, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + OFF_DL + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
                 float x8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x8[i] = d64[8 * c + i] * dls[8 * c + i] * rks[8 * c + i];
+                for (int i = 0; i < 8; ++i) x8[i] = d32[8 * c + i] * dls[8 * cc + i] * rks[8 * cc + i];
                 split_bf16x8(x8, hi, lo);
-                *reinterpret_cast<uint4*>(sm + OFF_T4 + tc::sw_chunk(tid, c, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + OFF_T4 + 16384 + tc::sw_chunk(tid, c, 128)) = lo;
+                *reinterpret_cast<uint4*>(sm + OFF_T4 + tc::sw_chunk(row, cc, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + OFF_T4 + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
             }
             const float gL = gams[L - 1];
+            float s32[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float v16[16];
-                tc::ld16(tm + lrow + TM_S + j * 16, v16);
-                tc::wait_ld();
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t col = TM_S + 64 * half + 32 * j;
+                ld32(trow + col, s32);
+                float lo16[16], hi16[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v16[i] *= gL;
-                tc::st16(tm + lrow + TM_S + j * 16, v16);
+                for (int i = 0; i < 16; ++i) {
+                    lo16[i] = s32[i] * gL;
+                    hi16[i] = s32[16 + i] * gL;
+                }
+                tc::st16(trow + col, lo16);
+                tc::st16(trow + col + 16, hi16);
             }
         }
         publish();
@@ -463,34 +493,32 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
         }
         if (!mma_wait()) { timed_out = true; break; }
 
-        // ---- 12. outputs o_t = gamma_t rq_t scale P_t + rq_t scale (M Delta)_t, column v = tid;
+        // ---- 12. outputs o_t = gamma_t rq_t scale P_t + rq_t scale (M Delta)_t (lane v, 32 tokens);
         //          the new state to bf16 for the next chunk
         {
+            float p32[32], m32[32];
+            ld32(trow + TM_P + 32 * half, p32);
+            ld32(trow + TM_MD + 32 * half, m32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float p16[16], m16[16];
-                tc::ld16(tm + lrow + TM_P + j * 16, p16);
-                tc::ld16(tm + lrow + TM_MD + j * 16, m16);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = j * 16 + i;
-                    if (t < L) {
-                        const float rq = rqs[t] * a.scale;
-                        const float o = fmaf(p16[i], gams[t] * rq, m16[i] * rq);
-                        a.out[static_cast<size_t>(tok0 + t) * vo_stride + h * D + tid] = f32_to_bf16_rne(o);
-                    }
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * half + i;
+                if (t < L) {
+                    const float rq = rqs[t] * a.scale;
+                    const float o = fmaf(p32[i], gams[t] * rq, m32[i] * rq);
+                    a.out[static_cast<size_t>(tok0 + t) * vo_stride + h * D + row] =
+                        static_cast<uint16_t>(pack_bf16x2(o, 0.f) & 0xffffu);
                 }
             }
             if (c0 + C < Tn) {
+                float s32[32];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float v16[16];
-                    tc::ld16(tm + lrow + TM_S + j * 16, v16);
-                    tc::wait_ld();
-                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(tid, 2 * j, 128)) = pack_bf16x8(v16);
-                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(tid, 2 * j + 1, 128)) =
-                        pack_bf16x8(v16 + 8);
+                for (int j = 0; j < 2; ++j) {
+                    ld32(trow + TM_S + 64 * half + 32 * j, s32);
+                    const int c8 = 8 * half + 4 * j;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + c, 128)) =
+                            pack_bf16x8(s32 + 8 * c);
                 }
             }
         }
@@ -500,16 +528,15 @@ __global__ void __launch_bounds__(pf::NT, 1) gdn_prefill_kernel(const PrefillArg
     if (timed_out) {
         if (tid == 0) atomicOr(a.status, 4);
     } else {
-        // ---- scatter the final state back to its pool slot (row v = tid)
-        float4* row = reinterpret_cast<float4*>(Sg + static_cast<size_t>(tid) * D);
+        // ---- scatter the final state back to its pool slot (row v, columns 64*half ..)
+        float4* dst = reinterpret_cast<float4*>(Sg + static_cast<size_t>(row) * D + 64 * half);
+        float s32[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float v16[16];
-            tc::ld16(tm + lrow + TM_S + j * 16, v16);
-            tc::wait_ld();
+        for (int j = 0; j < 2; ++j) {
+            ld32(trow + TM_S + 64 * half + 32 * j, s32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                row[j * 4 + i] = make_float4(v16[4 * i], v16[4 * i + 1], v16[4 * i + 2], v16[4 * i + 3]);
+            for (int i = 0; i < 8; ++i)
+                dst[8 * j + i] = make_float4(s32[4 * i], s32[4 * i + 1], s32[4 * i + 2], s32[4 * i + 3]);
         }
     }
     tc::fence_before();
