@@ -201,7 +201,8 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
     const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
     REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG,
             "gdn_prefill_chunked: out overlaps state_pool");
-    REQUIRE((long long)num_seqs * Hv < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: grid too large");
+    REQUIRE((long long)num_seqs * Hv < (1LL << 31) && T < (1LL << 31) - 64, GDN_ERR_UNSUPPORTED,
+            "gdn_prefill_chunked: grid or token count too large");
 
     gdn::PrefillArgs p;
     p.q = static_cast<const uint16_t*>(q);
@@ -224,7 +225,9 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
     p.scale = scale;
     p.eps = 1e-6f;
     const cudaError_t e = gdn::launch_prefill(p, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "gdn_prefill_chunked: launch failed: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "gdn_prefill_chunked: launch failed (TMA descriptors or kernel): %s",
+                    cudaGetErrorString(e));
     g_last_error[0] = '\0';
     return GDN_OK;
 }

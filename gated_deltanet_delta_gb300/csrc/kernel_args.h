@@ -2,6 +2,7 @@
 // Shared by the kernel headers and by the launchers; holds no device code.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace gdn {
@@ -68,6 +69,12 @@ struct PrefillArgs {
     long long T;
     int pool_size, num_seqs, Hk, Hv;
     float scale, eps;
+};
+
+// TMA descriptors of the prefill's q [T, Hk, 128], k [T, Hk, 128] and v [T, Hv, 128] (bf16): boxes of
+// 64 features x 1 head x 64 tokens with the 128-byte swizzle.
+struct PrefillMaps {
+    CUtensorMap q, k, v;
 };
 
 constexpr int kWinD = 128;       // head dim

@@ -51,11 +51,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     constexpr int D = kWinD, CG = kWinHalf / 4, RG = kWinThreads / CG, NR = D / RG;
     static_assert(CG == 16 && RG == 8 && NR == 16, "window tile");
 
-    __shared__ __align__(16) float qraw[D];
-    __shared__ __align__(16) float kraw[D];
-    __shared__ __align__(16) float vraw[kWinHalf];
-    __shared__ float part_q[4], part_k[4], gb[2];
-    __shared__ float4 red_kv[4][CG], red_o[4][CG];
+    // per-token buffers are double-buffered by token parity, so that a token needs two barriers:
+    // one after the conv outputs are written, one after the kv partial sums are written
+    __shared__ __align__(16) float qraw[2][D];
+    __shared__ __align__(16) float kraw[2][D];
+    __shared__ __align__(16) float vraw[2][kWinHalf];
+    __shared__ float part_q[2][4], part_k[2][4], gb[2][2];
+    __shared__ float4 red_kv[4][CG], red_o[2][4][CG];
     __shared__ float osm[kWinMaxTok][kWinHalf];
     __shared__ float ss[kWinMaxTok];
 
@@ -81,6 +83,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         R[m][1] = make_float2(x.z, x.w);
     }
     float cs = 1.0f;  // S = cs * R
+    float rq_last = 0.f, cs_last = 0.f;  // the previous token's q norm and state scale
 
     // ---- this thread's conv channels: q and k of key head hk, and (tid < 64) one v channel
     const int ch_q = hk * D + tid;
@@ -105,6 +108,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
 
     const float* x_n = a.qkv + size_t(n) * ntok * C;
     float xq = x_n[ch_q], xk = x_n[ch_k], xv = has_v ? x_n[ch_v] : 0.f;
+
+    // warp 0 finishes token u's readout (after the barrier that follows its partial sums): lanes
+    // 0..15 sum the four warps' partials of 4 columns each, the warp sums o^2 for the RMSNorm
+    auto finish_readout = [&](int u, float rq_u, float cs_u) {
+        if (warp != 0) return;
+        const int bu = u & 1;
+        float e = 0.f;
+        if (lane < CG) {
+            const float4 r0 = red_o[bu][0][lane], r1 = red_o[bu][1][lane], r2 = red_o[bu][2][lane],
+                         r3 = red_o[bu][3][lane];
+            const float sc = cs_u * rq_u * 0.08838834764831845f;  // cs rq / sqrt(128)
+            const float4 ot = make_float4(((r0.x + r1.x) + (r2.x + r3.x)) * sc,
+                                          ((r0.y + r1.y) + (r2.y + r3.y)) * sc,
+                                          ((r0.z + r1.z) + (r2.z + r3.z)) * sc,
+                                          ((r0.w + r1.w) + (r2.w + r3.w)) * sc);
+            reinterpret_cast<float4*>(osm[u])[lane] = ot;
+            e = ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w;
+        }
+        e = group_sum<32>(e);
+        if (lane == 0) ss[u] = e;
+    };
 
     for (int t = 0; t < ntok; ++t) {
         // next token's conv inputs, ahead of this token's barriers
@@ -140,27 +164,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         xq = nq; xk = nk; xv = nv;
 
         // raw q, k, v to shared memory; sums of squares per warp; gate and beta on thread 0
-        qraw[tid] = cq;
-        kraw[tid] = ck;
-        if (has_v) vraw[tid] = cv;
+        const int b = t & 1;
+        qraw[b][tid] = cq;
+        kraw[b][tid] = ck;
+        if (has_v) vraw[b][tid] = cv;
         const float sq = group_sum<32>(cq * cq);
         const float sk = group_sum<32>(ck * ck);
         if (lane == 0) {
-            part_q[warp] = sq;
-            part_k[warp] = sk;
+            part_q[b][warp] = sq;
+            part_k[b][warp] = sk;
         }
         if (tid == 0) {
             const size_t gi = (size_t(n) * ntok + t) * a.h_v + h;
-            gb[0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
-            gb[1] = sigmoid_f32(a.beta[gi]);
+            gb[b][0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
+            gb[b][1] = sigmoid_f32(a.beta[gi]);
         }
         __syncthreads();
+        if (t > 0) finish_readout(t - 1, rq_last, cs_last);
 
-        const float rk = rsqrtf(((part_k[0] + part_k[1]) + (part_k[2] + part_k[3])) + a.eps);
-        const float rq = rsqrtf(((part_q[0] + part_q[1]) + (part_q[2] + part_q[3])) + a.eps);
-        const float gate = gb[0], beta = gb[1];
-        const float4* k4 = reinterpret_cast<const float4*>(kraw + rg * NR);
-        const float4* q4 = reinterpret_cast<const float4*>(qraw + rg * NR);
+        const float rk = rsqrtf(((part_k[b][0] + part_k[b][1]) + (part_k[b][2] + part_k[b][3])) + a.eps);
+        const float rq = rsqrtf(((part_q[b][0] + part_q[b][1]) + (part_q[b][2] + part_q[b][3])) + a.eps);
+        const float gate = gb[b][0], beta = gb[b][1];
+        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rg * NR);
+        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rg * NR);
 
         // kv = cs rk sum_i R_ij k_i: this thread's 16 rows, the warp's two row groups, four warps
         float2 kva = make_float2(0.f, 0.f), kvb = make_float2(0.f, 0.f);
@@ -189,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             kv.z = (r0.z + r1.z) + (r2.z + r3.z);
             kv.w = (r0.w + r1.w) + (r2.w + r3.w);
         }
-        const float4 vv = reinterpret_cast<const float4*>(vraw)[c];
+        const float4 vv = reinterpret_cast<const float4*>(vraw[b])[c];
         const float gk = gate * cs * rk;  // gate * kv_j = gk * (reduced sum)
         // delta_j = (v_j - gate kv_j) beta;  the update R += k (rk delta / cs'), cs' = gate cs
         float cn = gate * cs;
@@ -206,6 +232,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         const float2 ea = make_float2((vv.x - gk * kv.x) * ek, (vv.y - gk * kv.y) * ek);
         const float2 eb = make_float2((vv.z - gk * kv.z) * ek, (vv.w - gk * kv.w) * ek);
         cs = cn;
+        rq_last = rq;
+        cs_last = cs;
 
         // rank-1 update and the readout partial sum_i R_ij q_i
         float2 oa = make_float2(0.f, 0.f), ob = make_float2(0.f, 0.f);
@@ -237,25 +265,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         o.y += __shfl_xor_sync(kFullMask, o.y, 16);
         o.z += __shfl_xor_sync(kFullMask, o.z, 16);
         o.w += __shfl_xor_sync(kFullMask, o.w, 16);
-        if (lane < 16) red_o[warp][c] = o;
-        __syncthreads();
-        if (warp == 0) {  // lanes 0..15 finish the readout of 4 columns each; the warp sums o^2
-            float e = 0.f;
-            if (lane < CG) {
-                const float4 r0 = red_o[0][lane], r1 = red_o[1][lane], r2 = red_o[2][lane],
-                             r3 = red_o[3][lane];
-                const float sc = cs * rq * 0.08838834764831845f;  // cs rq / sqrt(128)
-                const float4 ot = make_float4(((r0.x + r1.x) + (r2.x + r3.x)) * sc,
-                                              ((r0.y + r1.y) + (r2.y + r3.y)) * sc,
-                                              ((r0.z + r1.z) + (r2.z + r3.z)) * sc,
-                                              ((r0.w + r1.w) + (r2.w + r3.w)) * sc);
-                reinterpret_cast<float4*>(osm[t])[lane] = ot;
-                e = ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w;
-            }
-            e = group_sum<32>(e);
-            if (lane == 0) ss[t] = e;
-        }
+        if (lane < 16) red_o[b][warp][c] = o;
     }
+    __syncthreads();
+    finish_readout(ntok - 1, rq_last, cs_last);
 
     // the gated RMSNorm needs both halves' sums of o^2: exchange them once through the cluster
     cluster.sync();
