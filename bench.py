@@ -288,6 +288,84 @@ def bench_decode(torch, gdn, dist, steps, warmup, seed):
                 alg_bytes=decode_bytes(B, Hk, Hv, Dk, Dv), shape=(B, Hk, Hv, Dk, Dv))
 
 
+def bench_decode_multi(torch, gdn, dist, steps, warmup, seed, T=8):
+    """T consecutive decode tokens per call on the batched decode shapes (state on chip across
+    the tokens): the speculative-window-sized multi-token path."""
+    c = gi.GDN_DECODE_BATCHED
+    B, Hk, Hv, Dk, Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
+    dev = torch.device("cuda")
+    g = gi.rng(seed + 5)
+    b16, f32 = torch.bfloat16, torch.float32
+    toks = [gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv) for _ in range(T)]
+    st = {n: torch.from_numpy(np.stack([t[n] for t in toks], axis=1)).to(dt).to(dev)
+          for n, dt in (("q", b16), ("k", b16), ("v", b16), ("g", f32), ("beta", b16))}
+    states = [(torch.randn((B, Hv, Dv, Dk), device=dev) * 0.1) for _ in range(4)]
+    y = torch.empty((B, T, Hv, Dv), dtype=b16, device=dev)
+
+    def step(i):
+        chain, parity = (i % 2) * 2, (i // 2) % 2
+        gdn.gdn_decode_multi(states[chain + parity], st["q"], st["k"], st["v"], st["g"], st["beta"],
+                             state_out=states[chain + 1 - parity], y=y)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    tok_bytes = T * (2 * B * Hk * Dk * 2 + B * Hv * Dv * 2 + B * Hv * 6 + B * Hv * Dv * 2)
+    return dict(secs=secs, T=T, B=B, alg_bytes=decode_state_bytes(B, Hk, Hv, Dk, Dv) + tok_bytes)
+
+
+def bench_decode_pooled(torch, gdn, dist, steps, warmup, seed, pool=128):
+    """The batched decode step on a pooled state: 64 batch rows scattered over a 128-slot pool."""
+    c = gi.GDN_DECODE_BATCHED
+    B, Hk, Hv, Dk, Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
+    dev = torch.device("cuda")
+    g = gi.rng(seed + 6)
+    b16, f32 = torch.bfloat16, torch.float32
+    t = gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv)
+    d = [torch.from_numpy(t[n]).to(dt).to(dev) for n, dt in
+         (("q", b16), ("k", b16), ("v", b16), ("g", f32), ("beta", b16))]
+    pools = [torch.randn((pool, Hv, Dv, Dk), device=dev) * 0.1 for _ in range(2)]
+    idx = torch.from_numpy(g.choice(pool, size=B, replace=False).astype(np.int64)).to(dev)
+    y = torch.empty((B, Hv, Dv), dtype=b16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        gdn.gdn_decode_step_pooled(pools[i % 2], idx, *d, y=y, dev_status=status)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, alg_bytes=decode_bytes(B, Hk, Hv, Dk, Dv))
+
+
+# The Comba spec's measure shapes (B, H, K, V).
+COMBA_SWEEP = [(896, 16, 128, 128), (448, 32, 128, 128), (1792, 8, 128, 128), (1280, 16, 64, 128),
+               (640, 24, 128, 128)]
+
+
+def bench_comba_sweep(torch, gdn, dist, steps, warmup, seed):
+    dev = torch.device("cuda")
+    b16, f32 = torch.bfloat16, torch.float32
+    out = []
+    for (B, H, K, V) in COMBA_SWEEP:
+        g = gi.rng(seed + B + K)
+        t = gi.comba_decode_token(g, B, H, K, V)
+        d = [torch.from_numpy(t[n]).to(dt).to(dev) for n, dt in
+             (("q", b16), ("k", b16), ("v", b16), ("p", b16), ("beta", b16), ("g_log", f32))]
+        states = [torch.randn((B, H, K, V), device=dev) * 0.1 for _ in range(2)]
+        o = torch.empty((B, H, V), dtype=b16, device=dev)
+
+        def step(i):
+            gdn.comba_decode_step(states[i % 2], *d, state_new=states[1 - i % 2], o=o)
+
+        for i in range(warmup):
+            step(i)
+        secs = _timed(torch, dist, steps, step)
+        out.append(dict(shape=[B, H, K, V], secs=secs, alg_bytes=comba_bytes(B, H, K, V)))
+        del states
+    return out
+
+
 def bench_comba(torch, gdn, dist, steps, warmup, seed):
     c = gi.COMBA_DECODE
     B, H, K, V = c["B"], c["H"], c["K"], c["V"]
@@ -453,7 +531,14 @@ def main():
                          ("window_verify", lambda: bench_window(torch, gdn, dist, args.steps,
                                                                 args.warmup, seed, False)),
                          ("window_commit", lambda: bench_window(torch, gdn, dist, args.steps,
-                                                                args.warmup, seed, True))):
+                                                                args.warmup, seed, True)),
+                         ("decode_multi", lambda: bench_decode_multi(torch, gdn, dist, args.steps,
+                                                                     args.warmup, seed)),
+                         ("decode_pooled", lambda: bench_decode_pooled(torch, gdn, dist, args.steps,
+                                                                       args.warmup, seed)),
+                         ("comba_sweep", lambda: bench_comba_sweep(torch, gdn, dist,
+                                                                   max(3, args.steps // 5),
+                                                                   args.warmup, seed))):
             try:
                 extra[name] = fn()
             except gdn.GdnError as e:
@@ -518,6 +603,35 @@ def main():
                                      if key == "window_verify" else None}}
         elif key in extra:
             ops[key] = w
+
+    dm = extra.get("decode_multi", {})
+    if "secs" in dm:
+        t1 = dm["secs"] / K
+        gbs = dm["alg_bytes"] / t1 / 1e9
+        ops["decode_multi"] = {
+            "workload": f"gdn decode, {dm['T']} tokens per call, B64 Hk16 Hv32 D128",
+            "value": N * dm["B"] * dm["T"] / t1, "unit": "token-steps/s", "us_per_call": t1 * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+    dp = extra.get("decode_pooled", {})
+    if "secs" in dp:
+        t1 = dp["secs"] / K
+        gbs = dp["alg_bytes"] / t1 / 1e9
+        ops["decode_pooled"] = {
+            "workload": "gdn decode on a 128-slot pool, B64 Hk16 Hv32 D128", "value": N * gbs,
+            "unit": "GB/s", "us_per_step": t1 * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+    if isinstance(extra.get("comba_sweep"), list):
+        ksw = max(3, args.steps // 5)
+        rows = []
+        for r in extra["comba_sweep"]:
+            t1 = r["secs"] / ksw
+            gbs = r["alg_bytes"] / t1 / 1e9
+            rows.append({"shape_BHKV": r["shape"], "GB/s": gbs, "frac": gbs / hbm_peak,
+                         "us_per_step": t1 * 1e6})
+        ops["comba_sweep"] = {"workload": "Comba spec measure shapes", "rows": rows,
+                              "note": peak_note}
 
     cpu = None
     if dist.rank == 0 and N == 1:

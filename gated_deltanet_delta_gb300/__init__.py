@@ -23,7 +23,7 @@ STATUS_BAD_CACHE_INDEX = 1
 STATUS_BAD_SEQLENS = 2
 
 # Every symbol that include/gdn.h declares.
-ABI_SYMBOLS = ("gdn_decode_step", "comba_decode_step", "gdn_prefill_workspace_size",
+ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "gdn_prefill_workspace_size",
                "gdn_prefill_chunked", "gdn_window_fused", "gdn_status_string", "gdn_last_error")
 
 
@@ -53,6 +53,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         I64, SZ = ctypes.c_int64, ctypes.c_size_t
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.gdn_decode_step.restype = I
+        lib.gdn_decode_multi.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.gdn_decode_multi.restype = I
+        lib.gdn_decode_step_pooled.argtypes = [P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+        lib.gdn_decode_step_pooled.restype = I
         lib.comba_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.comba_decode_step.restype = I
         lib.gdn_prefill_workspace_size.argtypes = [I, I64, I, I, I, I, I]
@@ -152,6 +156,61 @@ def gdn_decode_step(state_in, q, k, v, g, beta, scale=None, state_out=None, y=No
                                   _ptr(g), _ptr(beta), _ptr(y), _out_code(y.dtype), B, Hk, Hv, Dk,
                                   Dv, scale, _stream(state_in.device)), "gdn_decode_step")
     return state_out, y
+
+
+def gdn_decode_multi(state_in, q, k, v, g, beta, scale=None, state_out=None, y=None, y_dtype=None):
+    """T consecutive GDN decode steps.  state_in f32 [B,Hv,Dv,Dk]; q,k bf16 [B,T,Hk,Dk];
+    v bf16 [B,T,Hv,Dv]; g f32 [B,T,Hv]; beta bf16 [B,T,Hv].  Returns (state_out, y [B,T,Hv,Dv])."""
+    torch = _torch()
+    B, Hv, Dv, Dk = state_in.shape
+    T, Hk = q.shape[1], q.shape[2]
+    _want(state_in, "state_in", torch.float32)
+    _want(q, "q", torch.bfloat16, (B, T, Hk, Dk))
+    _want(k, "k", torch.bfloat16, (B, T, Hk, Dk))
+    _want(v, "v", torch.bfloat16, (B, T, Hv, Dv))
+    _want(g, "g", torch.float32, (B, T, Hv))
+    _want(beta, "beta", torch.bfloat16, (B, T, Hv))
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    _want(state_out, "state_out", torch.float32, state_in.shape)
+    if y is None:
+        y = torch.empty((B, T, Hv, Dv), dtype=y_dtype or torch.bfloat16, device=state_in.device)
+    _want(y, "y", y.dtype, (B, T, Hv, Dv))
+    scale = Dk ** -0.5 if scale is None else float(scale)
+    _check(load().gdn_decode_multi(_ptr(state_in), _ptr(state_out), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(g), _ptr(beta), _ptr(y), _out_code(y.dtype), B, T, Hk, Hv,
+                                   Dk, Dv, scale, _stream(state_in.device)), "gdn_decode_multi")
+    return state_out, y
+
+
+def gdn_decode_step_pooled(state_pool, cache_indices, q, k, v, g, beta, scale=None, y=None,
+                           y_dtype=None, dev_status=None):
+    """One GDN decode step on a pooled state, in place: batch row b uses slot cache_indices[b] of
+    state_pool f32 [pool,Hv,Dv,Dk].  q,k bf16 [B,Hk,Dk]; v bf16 [B,Hv,Dv]; g f32 [B,Hv];
+    beta bf16 [B,Hv].  Returns y.  dev_status (int32 [1], zeroed) receives STATUS_BAD_CACHE_INDEX."""
+    torch = _torch()
+    _want(state_pool, "state_pool", torch.float32)
+    pool, Hv, Dv, Dk = state_pool.shape
+    B, Hk = q.shape[0], q.shape[1]
+    _want(cache_indices, "cache_indices", torch.int64, (B,))
+    _want(q, "q", torch.bfloat16, (B, Hk, Dk))
+    _want(k, "k", torch.bfloat16, (B, Hk, Dk))
+    _want(v, "v", torch.bfloat16, (B, Hv, Dv))
+    _want(g, "g", torch.float32, (B, Hv))
+    _want(beta, "beta", torch.bfloat16, (B, Hv))
+    if y is None:
+        y = torch.empty((B, Hv, Dv), dtype=y_dtype or torch.bfloat16, device=state_pool.device)
+    _want(y, "y", y.dtype, (B, Hv, Dv))
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=state_pool.device)
+    _want(dev_status, "dev_status", torch.int32, (1,))
+    scale = Dk ** -0.5 if scale is None else float(scale)
+    _check(load().gdn_decode_step_pooled(_ptr(state_pool), pool, _ptr(cache_indices), _ptr(q),
+                                         _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(y),
+                                         _out_code(y.dtype), B, Hk, Hv, Dk, Dv, scale,
+                                         _ptr(dev_status), _stream(state_pool.device)),
+           "gdn_decode_step_pooled")
+    return y
 
 
 def comba_decode_step(state, q, k, v, p, beta, g, scale=None, state_new=None, o=None,

@@ -76,8 +76,8 @@ gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* 
             Hv, Hk);
     REQUIRE(y_dtype == GDN_BF16 || y_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
             "gdn_decode_step: y_dtype must be GDN_BF16 or GDN_F32");
-    REQUIRE(Dk == 64 || Dk == 128, GDN_ERR_UNSUPPORTED, "gdn_decode_step: Dk must be 64 or 128 (got %d)",
-            Dk);
+    REQUIRE(Dk == 64 || Dk == 128 || Dk == 256, GDN_ERR_UNSUPPORTED,
+            "gdn_decode_step: Dk must be 64, 128 or 256 (got %d)", Dk);
     if (B == 0) return GDN_OK;
     REQUIRE(state_in && state_out && q && k && v && g && beta && y, GDN_ERR_INVALID_ARG,
             "gdn_decode_step: null pointer");
@@ -111,8 +111,108 @@ gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* 
     a.Dv = Dv;
     a.scale = scale;
     a.tiles = 0;
+    a.slots = nullptr;
+    a.pool_size = 0;
+    a.status = nullptr;
     gdn::launch_decode(a, B, Dk, static_cast<cudaStream_t>(stream));
     return launched("gdn_decode_step");
+}
+
+// ------------------------------------------------------------------------------------------------
+gdn_status gdn_decode_multi(const float* state_in, float* state_out, const void* q, const void* k,
+                            const void* v, const float* g, const void* beta, void* y,
+                            gdn_dtype y_dtype, int B, int T, int Hk, int Hv, int Dk, int Dv,
+                            float scale, gdn_stream_t stream) {
+    REQUIRE(B >= 0 && T >= 0 && Hk >= 1 && Hv >= 1 && Dk >= 1 && Dv >= 1, GDN_ERR_INVALID_ARG,
+            "gdn_decode_multi: sizes must be B, T >= 0 and Hk, Hv, Dk, Dv >= 1");
+    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG, "gdn_decode_multi: Hv (%d) must be a multiple of Hk (%d)",
+            Hv, Hk);
+    REQUIRE(y_dtype == GDN_BF16 || y_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
+            "gdn_decode_multi: y_dtype must be GDN_BF16 or GDN_F32");
+    REQUIRE(Dk == 64 || Dk == 128 || Dk == 256, GDN_ERR_UNSUPPORTED,
+            "gdn_decode_multi: Dk must be 64, 128 or 256 (got %d)", Dk);
+    if (B == 0 || T == 0) return GDN_OK;
+    REQUIRE(state_in && state_out && q && k && v && g && beta && y, GDN_ERR_INVALID_ARG,
+            "gdn_decode_multi: null pointer");
+    const size_t sbytes = size_t(B) * Hv * Dv * Dk * sizeof(float);
+    REQUIRE(!partial_overlap(state_in, sbytes, state_out, sbytes), GDN_ERR_INVALID_ARG,
+            "gdn_decode_multi: state_out partially overlaps state_in");
+    REQUIRE(aligned(state_in, 16) && aligned(state_out, 16) && aligned(q, 8) && aligned(k, 8),
+            GDN_ERR_INVALID_ARG, "gdn_decode_multi: state must be 16-byte, q and k 8-byte aligned");
+    REQUIRE(aligned(y, y_dtype == GDN_F32 ? 4 : 2) && aligned(v, 2) && aligned(beta, 2) && aligned(g, 4),
+            GDN_ERR_INVALID_ARG, "gdn_decode_multi: misaligned v, beta, g or y");
+    const size_t yb = size_t(B) * T * Hv * Dv * (y_dtype == GDN_F32 ? 4 : 2);
+    REQUIRE(!any_overlap(y, yb, state_out, sbytes), GDN_ERR_INVALID_ARG, "gdn_decode_multi: y overlaps state_out");
+    REQUIRE((long long)B * Hv * ((Dv + 31) / 32) < (1LL << 31), GDN_ERR_UNSUPPORTED,
+            "gdn_decode_multi: grid too large");
+    gdn::DecodeMultiArgs a;
+    a.state_in = state_in;
+    a.state_out = state_out;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.g = g;
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.y = y;
+    a.y_f32 = y_dtype == GDN_F32;
+    a.T = T;
+    a.Hk = Hk;
+    a.Hv = Hv;
+    a.Dv = Dv;
+    a.tiles = 0;
+    a.scale = scale;
+    gdn::launch_decode_multi(a, B, Dk, static_cast<cudaStream_t>(stream));
+    return launched("gdn_decode_multi");
+}
+
+// ------------------------------------------------------------------------------------------------
+gdn_status gdn_decode_step_pooled(float* state_pool, int pool_size, const int64_t* cache_indices,
+                                  const void* q, const void* k, const void* v, const float* g,
+                                  const void* beta, void* y, gdn_dtype y_dtype, int B, int Hk, int Hv,
+                                  int Dk, int Dv, float scale, int32_t* dev_status,
+                                  gdn_stream_t stream) {
+    REQUIRE(B >= 0 && pool_size >= 0 && Hk >= 1 && Hv >= 1 && Dk >= 1 && Dv >= 1, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step_pooled: sizes must be B, pool_size >= 0 and Hk, Hv, Dk, Dv >= 1");
+    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step_pooled: Hv (%d) must be a multiple of Hk (%d)", Hv, Hk);
+    REQUIRE(y_dtype == GDN_BF16 || y_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
+            "gdn_decode_step_pooled: y_dtype must be GDN_BF16 or GDN_F32");
+    REQUIRE(Dk == 64 || Dk == 128 || Dk == 256, GDN_ERR_UNSUPPORTED,
+            "gdn_decode_step_pooled: Dk must be 64, 128 or 256 (got %d)", Dk);
+    if (B == 0) return GDN_OK;
+    REQUIRE(state_pool && cache_indices && q && k && v && g && beta && y && dev_status,
+            GDN_ERR_INVALID_ARG, "gdn_decode_step_pooled: null pointer");
+    REQUIRE(aligned(state_pool, 16) && aligned(q, 8) && aligned(k, 8) && aligned(cache_indices, 8) &&
+                aligned(dev_status, 4),
+            GDN_ERR_INVALID_ARG, "gdn_decode_step_pooled: misaligned argument");
+    REQUIRE(aligned(y, y_dtype == GDN_F32 ? 4 : 2) && aligned(v, 2) && aligned(beta, 2) && aligned(g, 4),
+            GDN_ERR_INVALID_ARG, "gdn_decode_step_pooled: misaligned v, beta, g or y");
+    const size_t pbytes = size_t(pool_size) * Hv * Dv * Dk * sizeof(float);
+    const size_t yb = size_t(B) * Hv * Dv * (y_dtype == GDN_F32 ? 4 : 2);
+    REQUIRE(!any_overlap(y, yb, state_pool, pbytes), GDN_ERR_INVALID_ARG,
+            "gdn_decode_step_pooled: y overlaps state_pool");
+    REQUIRE((long long)B * Hv * ((Dv + 31) / 32) < (1LL << 31), GDN_ERR_UNSUPPORTED,
+            "gdn_decode_step_pooled: grid too large");
+    gdn::DecodeArgs a;
+    a.state_in = state_pool;
+    a.state_out = state_pool;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.g = g;
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.y = y;
+    a.y_f32 = y_dtype == GDN_F32;
+    a.Hk = Hk;
+    a.Hv = Hv;
+    a.Dv = Dv;
+    a.scale = scale;
+    a.tiles = 0;
+    a.slots = cache_indices;
+    a.pool_size = pool_size;
+    a.status = dev_status;
+    gdn::launch_decode(a, B, Dk, static_cast<cudaStream_t>(stream));
+    return launched("gdn_decode_step_pooled");
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -4,7 +4,8 @@
 // (b, hv) head and state row r (Dv rows of Dk columns, Dk contiguous):
 //     S'[r,:] = g S[r,:];  kv_r = S'[r,:] . k;  delta_r = (v_r - kv_r) beta;
 //     S_new[r,:] = S'[r,:] + delta_r k;  y_r = scale * S_new[r,:] . q
-// with key head hk = hv / (Hv / Hk) (the page's DISPATCH INVARIANTS).
+// with key head hk = hv / (Hv / Hk) (the page's DISPATCH INVARIANTS).  In the pooled form the state
+// of batch row b is slot slots[b] of a [pool, Hv, Dv, Dk] pool, updated in place.
 //
 // GB300 mapping.  The step is a stream of the fp32 state: 4 bytes in and 4 bytes out per element
 // against ~6 flops, so HBM bandwidth is the only bound.  Each state row is split over TPR adjacent
@@ -40,7 +41,15 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeArgs a) {
     const int lr = threadIdx.x % TPR;
     const int rw = threadIdx.x / TPR;
 
-    const size_t head_off = size_t(head) * a.Dv * DK;
+    long long srow = b;  // the state row (pool slot) of batch row b
+    if (a.slots) {
+        srow = a.slots[b];
+        if (srow < 0 || srow >= a.pool_size) {
+            if (threadIdx.x == 0 && tile == 0 && hv == 0) atomicOr(a.status, 1);
+            return;
+        }
+    }
+    const size_t head_off = (size_t(srow) * a.Hv + hv) * a.Dv * DK;
     const float4* src = reinterpret_cast<const float4*>(a.state_in + head_off);
     float4* dst = reinterpret_cast<float4*>(a.state_out + head_off);
 
@@ -117,6 +126,114 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeArgs a) {
                 static_cast<uint16_t*>(a.y)[yi] = f32_to_bf16_rne(yv);
         }
     }
+}
+
+// T consecutive decode steps ([gated_delta.rs] mt_gated_delta_chunk).  The same row split as the
+// single step; the state rows stay in registers for all T tokens.  Tokens are staged in blocks of
+// TB: q and k of the key head (fp32), v of this CTA's rows, g and beta go to shared memory, then the
+// block's tokens run with warp shuffles only, so a block costs two barriers.
+template <int DK, int TPR, int RPT, int NT, int TB>
+__global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiArgs a) {
+    constexpr int NV = DK / (4 * TPR);
+    constexpr int RPP = NT / TPR;
+    constexpr int ROWS = RPP * RPT;
+    __shared__ float4 ks[TB][DK / 4];
+    __shared__ float4 qs[TB][DK / 4];
+    __shared__ float vs[TB][ROWS];
+    __shared__ float gs[TB], bs[TB];
+
+    const int head = blockIdx.x / a.tiles;
+    const int tile = blockIdx.x - head * a.tiles;
+    const int hv = head % a.Hv;
+    const int b = head / a.Hv;
+    const int hk = hv / (a.Hv / a.Hk);
+    const int lr = threadIdx.x % TPR;
+    const int rw = threadIdx.x / TPR;
+    const size_t head_off = size_t(head) * a.Dv * DK;
+    const float4* src = reinterpret_cast<const float4*>(a.state_in + head_off);
+    float4* dst = reinterpret_cast<float4*>(a.state_out + head_off);
+
+    float4 s[RPT][NV];
+    int row[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        row[r] = tile * ROWS + r * RPP + rw;
+        const bool ok = row[r] < a.Dv;
+#pragma unroll
+        for (int m = 0; m < NV; ++m)
+            s[r][m] = ok ? ld_stream(src + size_t(row[r]) * (DK / 4) + lr + TPR * m)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    for (int t0 = 0; t0 < a.T; t0 += TB) {
+        const int nb = a.T - t0 < TB ? a.T - t0 : TB;
+        __syncthreads();  // the previous block's shared inputs are no longer read
+        for (int i = threadIdx.x; i < nb * (DK / 4); i += NT) {
+            const int tt = i / (DK / 4), c = i - tt * (DK / 4);
+            const size_t off = ((size_t(b) * a.T + t0 + tt) * a.Hk + hk) * DK + 4 * c;
+            ks[tt][c] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.k + off));
+            qs[tt][c] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.q + off));
+        }
+        for (int i = threadIdx.x; i < nb * ROWS; i += NT) {
+            const int tt = i / ROWS, r = i - tt * ROWS;
+            const int rr = tile * ROWS + r;
+            vs[tt][r] = rr < a.Dv ? bf16_to_f32(a.v[((size_t(b) * a.T + t0 + tt) * a.Hv + hv) * a.Dv + rr]) : 0.f;
+        }
+        if (threadIdx.x < nb) {
+            const size_t gi = (size_t(b) * a.T + t0 + threadIdx.x) * a.Hv + hv;
+            gs[threadIdx.x] = a.g[gi];
+            bs[threadIdx.x] = bf16_to_f32(a.beta[gi]);
+        }
+        __syncthreads();
+        for (int tt = 0; tt < nb; ++tt) {
+            const float gate = gs[tt], beta = bs[tt];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                float kv = 0.f;
+#pragma unroll
+                for (int m = 0; m < NV; ++m) {
+                    const float4 kk = ks[tt][lr + TPR * m];
+                    float4& x = s[r][m];
+                    x.x *= gate; x.y *= gate; x.z *= gate; x.w *= gate;
+                    kv = fmaf(x.x, kk.x, kv);
+                    kv = fmaf(x.y, kk.y, kv);
+                    kv = fmaf(x.z, kk.z, kv);
+                    kv = fmaf(x.w, kk.w, kv);
+                }
+                kv = group_sum<TPR>(kv);
+                const float delta = (vs[tt][r * RPP + rw] - kv) * beta;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < NV; ++m) {
+                    const float4 kk = ks[tt][lr + TPR * m];
+                    const float4 qq = qs[tt][lr + TPR * m];
+                    float4& x = s[r][m];
+                    x.x = fmaf(delta, kk.x, x.x);
+                    x.y = fmaf(delta, kk.y, x.y);
+                    x.z = fmaf(delta, kk.z, x.z);
+                    x.w = fmaf(delta, kk.w, x.w);
+                    acc = fmaf(x.x, qq.x, acc);
+                    acc = fmaf(x.y, qq.y, acc);
+                    acc = fmaf(x.z, qq.z, acc);
+                    acc = fmaf(x.w, qq.w, acc);
+                }
+                acc = group_sum<TPR>(acc);
+                if (row[r] < a.Dv && lr == 0) {
+                    const float yv = a.scale * acc;
+                    const size_t yi = ((size_t(b) * a.T + t0 + tt) * a.Hv + hv) * a.Dv + row[r];
+                    if (a.y_f32)
+                        static_cast<float*>(a.y)[yi] = yv;
+                    else
+                        static_cast<uint16_t*>(a.y)[yi] = f32_to_bf16_rne(yv);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+        if (row[r] < a.Dv)
+#pragma unroll
+            for (int m = 0; m < NV; ++m) st_stream(dst + size_t(row[r]) * (DK / 4) + lr + TPR * m, s[r][m]);
 }
 
 // Rows covered by one CTA of a configuration.

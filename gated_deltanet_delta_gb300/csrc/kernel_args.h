@@ -20,6 +20,26 @@ struct DecodeArgs {
     int Hk, Hv, Dv;
     int tiles;  // row tiles per head
     float scale;
+    // pooled form: state_in == state_out is the pool [pool_size, Hv, Dv, Dk] and batch row b reads
+    // and writes slot slots[b]; a slot outside [0, pool_size) sets bit 1 of *status and is skipped
+    const int64_t* slots;  // null: state row b is batch row b
+    int pool_size;
+    int32_t* status;
+};
+
+struct DecodeMultiArgs {
+    const float* state_in;
+    float* state_out;
+    const uint16_t* q;  // [B, T, Hk, Dk]
+    const uint16_t* k;
+    const uint16_t* v;  // [B, T, Hv, Dv]
+    const float* g;     // [B, T, Hv]
+    const uint16_t* beta;
+    void* y;            // [B, T, Hv, Dv]
+    int y_f32;
+    int T, Hk, Hv, Dv;
+    int tiles;
+    float scale;
 };
 
 struct CombaArgs {

@@ -4,6 +4,8 @@
  * Four operations of the gated delta-rule recurrence, each a set of hand-written CUDA kernels for
  * sm_103a:
  *   gdn_decode_step      one-token GDN step with key sharing (Hv value heads over Hk key heads)
+ *   gdn_decode_step_pooled  the same on a pooled state indexed by cache_indices
+ *   gdn_decode_multi     T consecutive decode steps with the state held on chip
  *   comba_decode_step    one-token Comba step (state read with key p, written with key k)
  *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
  *   gdn_window_fused     fused decode window: conv + SiLU, L2 norm, gates, recurrence over ntok
@@ -54,9 +56,10 @@ typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
 /* A cudaStream_t, passed opaquely so that this header needs no CUDA header. */
 typedef void* gdn_stream_t;
 
-/* Bits of the device status word of gdn_prefill_chunked. */
+/* Bits of the device status word of gdn_prefill_chunked and gdn_decode_step_pooled. */
 #define GDN_STATUS_BAD_CACHE_INDEX 1 /* a cache_indices entry outside [0, pool_size) */
 #define GDN_STATUS_BAD_SEQLENS 2     /* cu_seqlens[n] < 0, decreasing, or beyond T */
+#define GDN_STATUS_TIMEOUT 4         /* a bounded wait for the tensor core or a copy gave up */
 
 /*
  * gdn_decode_step -- one GDN decode step for B sequences.  [gated_delta.rs] "Recurrence per step":
@@ -73,13 +76,49 @@ typedef void* gdn_stream_t;
  *   beta       bf16 [B, Hv]
  *   y          [B, Hv, Dv] of y_dtype (GDN_BF16: round to nearest even; GDN_F32)
  *   scale      readout scale (Dk^-0.5 is the usual choice; 1 reproduces the page exactly)
- * Supported: Dk in {64, 128}, Dv a positive multiple of 8, Hk >= 1, Hv % Hk == 0.
+ * Supported: Dk in {64, 128, 256}, any Dv >= 1, Hk >= 1, Hv % Hk == 0.
  * All state arithmetic is f32; bf16 inputs are widened exactly.
  */
 gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* q, const void* k,
                            const void* v, const float* g, const void* beta, void* y,
                            gdn_dtype y_dtype, int B, int Hk, int Hv, int Dk, int Dv, float scale,
                            gdn_stream_t stream);
+
+/*
+ * gdn_decode_multi -- T consecutive GDN decode steps for B sequences in one call: the state stays
+ * in registers across the tokens and crosses HBM once ([gated_delta.rs] mt_gated_delta_chunk:
+ * the same recurrence as gdn_decode_step, wrapped in a loop over t).
+ *
+ *   state_in, state_out  f32 [B, Hv, Dv, Dk]   as gdn_decode_step (state_out after the T tokens)
+ *   q, k       bf16 [B, T, Hk, Dk]
+ *   v          bf16 [B, T, Hv, Dv]
+ *   g          f32  [B, T, Hv]   linear gates
+ *   beta       bf16 [B, T, Hv]
+ *   y          [B, T, Hv, Dv] of y_dtype
+ * Supported: as gdn_decode_step, any T >= 0 (T = 0 copies nothing and writes nothing).
+ */
+gdn_status gdn_decode_multi(const float* state_in, float* state_out, const void* q, const void* k,
+                            const void* v, const float* g, const void* beta, void* y,
+                            gdn_dtype y_dtype, int B, int T, int Hk, int Hv, int Dk, int Dv,
+                            float scale, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step_pooled -- the same decode step on a pooled state: batch row b reads and writes,
+ * in place, slot cache_indices[b] of state_pool (the cache_indices / state_pool convention of
+ * [gdn_chunkwise] gdn_extend_chunkwise, applied to one decode token).
+ *
+ *   state_pool     f32 [pool_size, Hv, Dv, Dk]   updated in place at the referenced slots only
+ *   cache_indices  int64 [B]    distinct slots; duplicates give an undefined result
+ *   q, k, v, g, beta, y, y_dtype, scale: as gdn_decode_step
+ *   dev_status     device int32, zeroed by the caller; bit GDN_STATUS_BAD_CACHE_INDEX is set for a
+ *                  slot outside [0, pool_size), whose batch row is then skipped (y not written)
+ * Supported: as gdn_decode_step.
+ */
+gdn_status gdn_decode_step_pooled(float* state_pool, int pool_size, const int64_t* cache_indices,
+                                  const void* q, const void* k, const void* v, const float* g,
+                                  const void* beta, void* y, gdn_dtype y_dtype, int B, int Hk, int Hv,
+                                  int Dk, int Dv, float scale, int32_t* dev_status,
+                                  gdn_stream_t stream);
 
 /*
  * comba_decode_step -- one Comba decode step for B sequences.  [comba spec] spec_md:
@@ -95,8 +134,7 @@ gdn_status gdn_decode_step(const float* state_in, float* state_out, const void* 
  *   g          f32  [B, H]   log-decay (<= 0 in use; any finite value is accepted)
  *   o          [B, H, V] of o_dtype (GDN_BF16 or GDN_F32)
  *   scale      query scale ([comba spec]: K^-0.5 when the caller has no other value)
- * Supported: K in {32, 64, 128}, V a positive multiple of 32 up to 128 ... see gdn_last_error for
- * the exact reason of an GDN_ERR_UNSUPPORTED.
+ * Supported: K in {64, 128} and V in {64, 128} (the shapes of the Comba spec's regime).
  */
 gdn_status comba_decode_step(const float* state, float* state_new, const void* q, const void* k,
                              const void* v, const void* p, const void* beta, const float* g,

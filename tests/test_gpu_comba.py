@@ -102,3 +102,22 @@ def test_empty_batch_is_a_no_op():
     b = torch.zeros((0, 2), dtype=torch.bfloat16, device="cuda")
     S1, o = gdn.comba_decode_step(S, q, q, q, q, b, torch.zeros((0, 2), device="cuda"))
     assert S1.shape == S.shape and o.shape == (0, 2, 128)
+
+
+# The Comba spec's quick measure shapes (B, H, K, V), including K = 64: the GPU runs the whole step,
+# the oracle a sample of heads.
+@pytest.mark.parametrize("B,H,K,V", [(256, 16, 128, 128), (128, 32, 128, 128), (512, 16, 64, 128)])
+def test_spec_measure_shapes_sampled(B, H, K, V):
+    scale = K ** -0.5
+    g = gi.rng(B + H + K)
+    S = (g.standard_normal((B, H, K, V)) * 0.1).astype(np.float32)
+    t = gi.comba_decode_token(g, B, H, K, V)
+    S1, o = gdn.comba_decode_step(dev(S, torch.float32), *_dev_token(t), scale=scale,
+                                  o_dtype=torch.float32)
+    S_h, o_h = host(S1), host(o)
+    for (b, h) in sample_heads(np.random.default_rng(3), B, H, 16):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        Sn, on = oracle.comba_decode(S[sl], t["q"][sl], t["k"][sl], t["v"][sl], t["p"][sl],
+                                     t["beta"][sl], t["g_log"][sl], scale)
+        assert max_rel_err(S_h[b, h], Sn[0, 0]) <= TOL
+        assert max_rel_err(o_h[b, h], on[0, 0]) <= TOL

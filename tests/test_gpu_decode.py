@@ -154,3 +154,67 @@ def test_rejects_indivisible_heads_without_writing():
                             torch.zeros((1, 3), dtype=torch.bfloat16, device="cuda"), state_out=out)
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
     assert bool(torch.all(out == 5.0))
+
+
+@pytest.mark.parametrize("B,Hk,Hv,Dv", [(3, 2, 4, 256), (2, 1, 2, 100)])
+def test_head_dim_256(B, Hk, Hv, Dv):
+    g = gi.rng(B + Dv)
+    S = (g.standard_normal((B, Hv, Dv, 256)) * 0.2).astype(np.float32)
+    t = gi.gdn_decode_token(g, B, Hk, Hv, 256, Dv)
+    ref_S, ref_y = oracle.gdn_decode(S, t["q"], t["k"], t["v"], t["g"], t["beta"], 256 ** -0.5)
+    S1, y = _gpu_step(dev(S, torch.float32), t, 256 ** -0.5)
+    assert max_rel_err(host(S1), ref_S) <= TOL
+    assert max_rel_err(host(y), ref_y) <= TOL
+
+
+@pytest.mark.parametrize("Dk", [64, 128, 256])
+def test_pooled_decode_gathers_and_scatters_its_slots(Dk):
+    # batch row b updates pool slot cache_indices[b] in place; other slots stay bitwise untouched;
+    # an out-of-range slot is flagged and its row skipped
+    B, Hk, Hv, Dv, pool = 4, 2, 4, 64, 7
+    g = gi.rng(40 + Dk)
+    P = (g.standard_normal((pool, Hv, Dv, Dk)) * 0.2).astype(np.float32)
+    t = gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv)
+    idx = np.array([5, 0, 3, 9], dtype=np.int64)   # 9 is outside the pool
+    scale = Dk ** -0.5
+    Pd = dev(P, torch.float32)
+    y = torch.full((B, Hv, Dv), -7.0, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, k, v, gg, beta = _dev_token(t)
+    gdn.gdn_decode_step_pooled(Pd, dev(idx, torch.int64), q, k, v, gg, beta, scale=scale, y=y,
+                               dev_status=status)
+    assert int(status.item()) & gdn.STATUS_BAD_CACHE_INDEX
+    Ph, yh = host(Pd), host(y)
+    for b, slot in enumerate(idx[:3]):
+        ref_S, ref_y = oracle.gdn_decode(P[slot][None], t["q"][b:b + 1], t["k"][b:b + 1],
+                                         t["v"][b:b + 1], t["g"][b:b + 1], t["beta"][b:b + 1], scale)
+        assert max_rel_err(Ph[slot], ref_S[0]) <= TOL
+        assert max_rel_err(yh[b], ref_y[0]) <= TOL
+    assert np.all(yh[3] == -7.0)
+    for s in (1, 2, 4, 6):
+        assert np.array_equal(Ph[s], P[s].astype(np.float64))
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv", [(2, 1, 2, 4, 128, 128), (3, 37, 1, 2, 128, 100),
+                                             (1, 16, 2, 2, 64, 64), (2, 9, 1, 1, 256, 40)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_multi_token_steps_equal_a_chain_of_steps(B, T, Hk, Hv, Dk, Dv, in_place):
+    # [gated_delta.rs] mt_gated_delta_chunk: the decode recurrence wrapped in a loop over t
+    g = gi.rng(B * 100 + T + Dk)
+    S = (g.standard_normal((B, Hv, Dv, Dk)) * 0.2).astype(np.float32)
+    toks = [gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv) for _ in range(T)]
+    stack = {n: np.stack([t[n] for t in toks], axis=1) for n in ("q", "k", "v", "g", "beta")}
+    scale = Dk ** -0.5
+    ref = S.astype(np.float64)
+    ys = []
+    for t in toks:
+        ref, y = oracle.gdn_decode(ref, t["q"], t["k"], t["v"], t["g"], t["beta"], scale)
+        ys.append(y)
+    ref_y = np.stack(ys, axis=1)
+    Sd = dev(S, torch.float32)
+    S1, y = gdn.gdn_decode_multi(Sd, dev(stack["q"], torch.bfloat16), dev(stack["k"], torch.bfloat16),
+                                 dev(stack["v"], torch.bfloat16), dev(stack["g"], torch.float32),
+                                 dev(stack["beta"], torch.bfloat16), scale=scale,
+                                 state_out=Sd if in_place else None, y_dtype=torch.float32)
+    assert max_rel_err(host(S1), ref) <= TOL
+    assert max_rel_err(host(y), ref_y) <= TOL
