@@ -12,21 +12,20 @@
 // 0x100|k: token k; 0: never).
 //
 // GB300 mapping.  A CTA of 128 threads owns one (n, h) head's 128 x 64 half of the state (columns
-// 64*half ..): thread (c, rg) holds column group c (4 columns) of the 16 consecutive rows
-// 16rg .. 16rg+15 in registers for the whole window, so the 64 KB head state is read from HBM once
-// and written at most once; a warp's load covers two 256-byte row pieces.  The kernel is bound by
-// instruction issue, not by memory, so the per-element work is cut to three packed f32x2 FMAs per
-// two elements and token: the state is held as c * R with a per-head scalar c (the gate multiplies
-// c, and R += k (rk delta / c) is the rank-1 update; c is folded back into R when it drops below
-// 2^-40), and the L2 norms of q and k are applied to the reduced sums instead of every row.  The
-// reductions over the rows (kv, o) run serially in registers, then over the two row groups of a
-// warp with one shuffle, then over the four warps through shared memory.  The two halves of a head
-// form a thread-block cluster of 2: the output RMSNorm needs sum_j o_j^2 over all 128 columns, so
-// each half keeps its o_t and partial sums for every token in shared memory and the pair exchanges
-// the partial sums once, through distributed shared memory, after the last token.  Each CTA
-// convolves the 256 q/k channels of key head hk and its own 64 v channels (thread t: q channel t,
-// k channel t, v channel t < 64), with histories and taps in registers, and prefetches the next
-// token's inputs a token ahead.
+// 64*half ..); each warp owns 16 whole columns: lane (column group cl, row block rb) holds 4 columns
+// of the 16 rows 16rb .. 16rb+15 in registers for the whole window, so the 64 KB head state is read
+// from HBM once and written at most once.  Both reductions over the 128 rows (kv and o) are a
+// register sum plus three xor-shuffles inside the warp, so a token needs one barrier (after the conv
+// outputs are written; the per-token buffers are double-buffered by token parity).  The kernel is
+// bound by instruction issue and latency, not memory, so the per-element work is three packed
+// f32x2 FMAs per two elements and token: the state is held as c * R with a per-head scalar c (the
+// gate multiplies c; R += k (rk delta / c) is the rank-1 update; c is folded back into R when it
+// drops below 2^-40), and the q/k norms are applied to reduced sums.  The two halves of a head form
+// a thread-block cluster of 2: the output RMSNorm needs sum_j o_j^2 over all 128 columns, so each
+// half keeps its o_t and partial sums for every token in shared memory and the pair exchanges the
+// partial sums once, through distributed shared memory, after the last token.  Each CTA convolves
+// the 256 q/k channels of key head hk and its own 64 v channels (thread t: q channel t, k channel
+// t, v channel t < 64), with histories and taps in registers, a token ahead of their use.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -45,21 +44,32 @@ __device__ __forceinline__ float softplus_f32(float x) { return x > 20.0f ? x : 
 // below kWinRenorm it is folded back into R.
 constexpr float kWinRenorm = 9.094947e-13f;  // 2^-40
 
+// Asynchronous 4-byte global -> shared copy (completes at cp_async_wait_all of the same thread).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     gdn_window_kernel(const WindowArgs a) {
     namespace cg = cooperative_groups;
-    constexpr int D = kWinD, CG = kWinHalf / 4, RG = kWinThreads / CG, NR = D / RG;
-    static_assert(CG == 16 && RG == 8 && NR == 16, "window tile");
+    constexpr int D = kWinD, NR = 16;  // rows per lane
+    static_assert(kWinThreads == 128 && kWinHalf == 64, "window tile");
 
-    // per-token buffers are double-buffered by token parity, so that a token needs two barriers:
-    // one after the conv outputs are written, one after the kv partial sums are written
+    // per-token buffers, double-buffered by token parity: one barrier per token
     __shared__ __align__(16) float qraw[2][D];
     __shared__ __align__(16) float kraw[2][D];
     __shared__ __align__(16) float vraw[2][kWinHalf];
-    __shared__ float part_q[2][4], part_k[2][4], gb[2][2];
-    __shared__ float4 red_kv[4][CG], red_o[2][4][CG];
-    __shared__ float osm[kWinMaxTok][kWinHalf];
+    __shared__ float part_q[2][4], part_k[2][4];
+    __shared__ float gates[kWinMaxTok][2];  // gate and beta of every token, computed up front
+    __shared__ __align__(16) float osm[kWinMaxTok][kWinHalf];
+    __shared__ float ssw[kWinMaxTok][4];  // per-warp sums of o^2
     __shared__ float ss[kWinMaxTok];
+    __shared__ float zs[kWinMaxTok * kWinHalf];  // the epilogue's z and gamma, fetched up front
+    __shared__ float gs[kWinThreads];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int half = int(cluster.block_rank());
@@ -68,22 +78,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     const int n = unit / a.h_v;
     const int hk = h % a.h_k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = tid % CG, rg = tid / CG;
+    const int cl = lane & 3;           // column group inside the warp
+    const int rb = lane >> 2;          // block of 16 rows
+    const int col = 16 * warp + 4 * cl;  // first of this lane's 4 columns inside the half
     const int C = (2 * a.h_k + a.h_v) * D;
     const int ntok = a.ntok;
 
-    // ---- the state half in registers: rows rg*16 .. rg*16+15, columns half*64 + 4c .. +3
-    const size_t row_stride = size_t(a.h_v) * D;  // floats between consecutive rows i
-    float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + half * kWinHalf + 4 * c;
-    float2 R[NR][2];
+    // ---- the state: rows 16rb .. 16rb+15, columns half*64 + col .. +3, held as cs * R
+    const size_t row_stride = size_t(a.h_v) * D;
+    float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + half * kWinHalf + col;
+    // packed along rows: R[p][j] = (S[2p][j], S[2p+1][j]) of this lane's rows and 4 columns, so that
+    // the per-row k and q pairs come straight from float4 loads
+    float2 R[NR / 2][4];
 #pragma unroll
-    for (int m = 0; m < NR; ++m) {
-        const float4 x = ld_stream(reinterpret_cast<const float4*>(sbase + size_t(rg * NR + m) * row_stride));
-        R[m][0] = make_float2(x.x, x.y);
-        R[m][1] = make_float2(x.z, x.w);
+    for (int p = 0; p < NR / 2; ++p) {
+        const float4 x = ld_stream(reinterpret_cast<const float4*>(sbase + size_t(rb * NR + 2 * p) * row_stride));
+        const float4 y = ld_stream(reinterpret_cast<const float4*>(sbase + size_t(rb * NR + 2 * p + 1) * row_stride));
+        R[p][0] = make_float2(x.x, y.x);
+        R[p][1] = make_float2(x.y, y.y);
+        R[p][2] = make_float2(x.z, y.z);
+        R[p][3] = make_float2(x.w, y.w);
     }
-    float cs = 1.0f;  // S = cs * R
-    float rq_last = 0.f, cs_last = 0.f;  // the previous token's q norm and state scale
+    float cs = 1.0f;
 
     // ---- this thread's conv channels: q and k of key head hk, and (tid < 64) one v channel
     const int ch_q = hk * D + tid;
@@ -102,36 +118,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     const float4 wk = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_k) * 4);
     const float4 wv = has_v ? *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_v) * 4)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    // q/k history is owned by the head h == hk (half 0 writes q, half 1 writes k); v by every head
-    const bool own_qk = h < a.h_k;
+    const bool own_qk = h < a.h_k;  // q/k history: head h == hk owns it (half 0: q, half 1: k)
     const float dth = a.dt[h], ssm = a.ssm_a[h];
-
     const float* x_n = a.qkv + size_t(n) * ntok * C;
     float xq = x_n[ch_q], xk = x_n[ch_k], xv = has_v ? x_n[ch_v] : 0.f;
-
-    // warp 0 finishes token u's readout (after the barrier that follows its partial sums): lanes
-    // 0..15 sum the four warps' partials of 4 columns each, the warp sums o^2 for the RMSNorm
-    auto finish_readout = [&](int u, float rq_u, float cs_u) {
-        if (warp != 0) return;
-        const int bu = u & 1;
-        float e = 0.f;
-        if (lane < CG) {
-            const float4 r0 = red_o[bu][0][lane], r1 = red_o[bu][1][lane], r2 = red_o[bu][2][lane],
-                         r3 = red_o[bu][3][lane];
-            const float sc = cs_u * rq_u * 0.08838834764831845f;  // cs rq / sqrt(128)
-            const float4 ot = make_float4(((r0.x + r1.x) + (r2.x + r3.x)) * sc,
-                                          ((r0.y + r1.y) + (r2.y + r3.y)) * sc,
-                                          ((r0.z + r1.z) + (r2.z + r3.z)) * sc,
-                                          ((r0.w + r1.w) + (r2.w + r3.w)) * sc);
-            reinterpret_cast<float4*>(osm[u])[lane] = ot;
-            e = ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w;
-        }
-        e = group_sum<32>(e);
-        if (lane == 0) ss[u] = e;
-    };
+    // every token's gate and beta (thread t), read after the first token's barrier
+    if (tid < ntok) {
+        const size_t gi = (size_t(n) * ntok + tid) * a.h_v + h;
+        gates[tid][0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
+        gates[tid][1] = sigmoid_f32(a.beta[gi]);
+    }
+    // the epilogue's z (this thread's items tid + 128 i) and gamma, copied asynchronously now
+#pragma unroll
+    for (int i = 0; i < kWinMaxTok / 2; ++i) {
+        const int idx = tid + kWinThreads * i;
+        const int t = idx / kWinHalf, j = idx % kWinHalf;
+        if (t < ntok)
+            cp_async4(&zs[idx], a.z + ((size_t(n) * ntok + t) * a.h_v + h) * D + half * kWinHalf + j);
+    }
+    cp_async4(&gs[tid], a.gamma + half * kWinHalf + (tid & (kWinHalf - 1)));
 
     for (int t = 0; t < ntok; ++t) {
-        // next token's conv inputs, ahead of this token's barriers
+        const int b = t & 1;
         float nq = 0.f, nk = 0.f, nv = 0.f;
         if (t + 1 < ntok) {
             const float* xn = x_n + size_t(t + 1) * C;
@@ -139,7 +147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             nk = xn[ch_k];
             nv = has_v ? xn[ch_v] : 0.f;
         }
-        // conv + SiLU, history shift
+        // conv + SiLU, history shift, committed history
         const float cq = silu_f32(fmaf(xq, wq.w, fmaf(hq[2], wq.z, fmaf(hq[1], wq.y, hq[0] * wq.x))));
         const float ck = silu_f32(fmaf(xk, wk.w, fmaf(hk3[2], wk.z, fmaf(hk3[1], wk.y, hk3[0] * wk.x))));
         const float cv = silu_f32(fmaf(xv, wv.w, fmaf(hv[2], wv.z, fmaf(hv[1], wv.y, hv[0] * wv.x))));
@@ -162,9 +170,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             }
         }
         xq = nq; xk = nk; xv = nv;
-
-        // raw q, k, v to shared memory; sums of squares per warp; gate and beta on thread 0
-        const int b = t & 1;
         qraw[b][tid] = cq;
         kraw[b][tid] = ck;
         if (has_v) vraw[b][tid] = cv;
@@ -174,112 +179,114 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             part_q[b][warp] = sq;
             part_k[b][warp] = sk;
         }
-        if (tid == 0) {
-            const size_t gi = (size_t(n) * ntok + t) * a.h_v + h;
-            gb[b][0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
-            gb[b][1] = sigmoid_f32(a.beta[gi]);
-        }
         __syncthreads();
-        if (t > 0) finish_readout(t - 1, rq_last, cs_last);
 
+        // everything below is warp-local: the warp owns 16 whole columns
         const float rk = rsqrtf(((part_k[b][0] + part_k[b][1]) + (part_k[b][2] + part_k[b][3])) + a.eps);
         const float rq = rsqrtf(((part_q[b][0] + part_q[b][1]) + (part_q[b][2] + part_q[b][3])) + a.eps);
-        const float gate = gb[b][0], beta = gb[b][1];
-        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rg * NR);
-        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rg * NR);
+        const float gate = gates[t][0], beta = gates[t][1];
+        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * NR);
+        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * NR);
 
-        // kv = cs rk sum_i R_ij k_i: this thread's 16 rows, the warp's two row groups, four warps
-        float2 kva = make_float2(0.f, 0.f), kvb = make_float2(0.f, 0.f);
+        // kv = cs rk sum_i R_ij k_i: 16 rows in registers (as 8 row pairs), then the 8 row blocks
+        // by shuffles
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int m4 = 0; m4 < NR / 4; ++m4) {
             const float4 kk = k4[m4];
-            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+            const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 k2 = make_float2(kr[u], kr[u]);
-                kva = __ffma2_rn(R[m4 * 4 + u][0], k2, kva);
-                kvb = __ffma2_rn(R[m4 * 4 + u][1], k2, kvb);
+            for (int j = 0; j < 4; ++j) {
+                acc[j] = __ffma2_rn(R[2 * m4][j], k01, acc[j]);
+                acc[j] = __ffma2_rn(R[2 * m4 + 1][j], k23, acc[j]);
             }
         }
-        float4 kv = make_float4(kva.x, kva.y, kvb.x, kvb.y);
-        kv.x += __shfl_xor_sync(kFullMask, kv.x, 16);
-        kv.y += __shfl_xor_sync(kFullMask, kv.y, 16);
-        kv.z += __shfl_xor_sync(kFullMask, kv.z, 16);
-        kv.w += __shfl_xor_sync(kFullMask, kv.w, 16);
-        if (lane < 16) red_kv[warp][c] = kv;
-        __syncthreads();
-        {
-            const float4 r0 = red_kv[0][c], r1 = red_kv[1][c], r2 = red_kv[2][c], r3 = red_kv[3][c];
-            kv.x = (r0.x + r1.x) + (r2.x + r3.x);
-            kv.y = (r0.y + r1.y) + (r2.y + r3.y);
-            kv.z = (r0.z + r1.z) + (r2.z + r3.z);
-            kv.w = (r0.w + r1.w) + (r2.w + r3.w);
-        }
-        const float4 vv = reinterpret_cast<const float4*>(vraw[b])[c];
-        const float gk = gate * cs * rk;  // gate * kv_j = gk * (reduced sum)
-        // delta_j = (v_j - gate kv_j) beta;  the update R += k (rk delta / cs'), cs' = gate cs
+        float kvs[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kvs[j] = acc[j].x + acc[j].y;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) kvs[j] += __shfl_xor_sync(kFullMask, kvs[j], o);
+        const float4 vv = *reinterpret_cast<const float4*>(vraw[b] + col);
+        const float gk = gate * cs * rk;
         float cn = gate * cs;
         if (cn < kWinRenorm) {  // uniform over the CTA: fold cs' into R
 #pragma unroll
-            for (int m = 0; m < NR; ++m) {
-                const float2 c2 = make_float2(cn, cn);
-                R[m][0] = __fmul2_rn(R[m][0], c2);
-                R[m][1] = __fmul2_rn(R[m][1], c2);
-            }
+            for (int p = 0; p < NR / 2; ++p)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) R[p][j] = __fmul2_rn(R[p][j], make_float2(cn, cn));
             cn = 1.0f;
         }
         const float ek = beta * rk / cn;
-        const float2 ea = make_float2((vv.x - gk * kv.x) * ek, (vv.y - gk * kv.y) * ek);
-        const float2 eb = make_float2((vv.z - gk * kv.z) * ek, (vv.w - gk * kv.w) * ek);
+        const float vj[4] = {vv.x, vv.y, vv.z, vv.w};
+        float2 e2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float e = (vj[j] - gk * kvs[j]) * ek;
+            e2[j] = make_float2(e, e);
+        }
         cs = cn;
-        rq_last = rq;
-        cs_last = cs;
 
-        // rank-1 update and the readout partial sum_i R_ij q_i
-        float2 oa = make_float2(0.f, 0.f), ob = make_float2(0.f, 0.f);
+        // rank-1 update and readout
+        float2 oacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
         for (int m4 = 0; m4 < NR / 4; ++m4) {
             const float4 kk = k4[m4];
             const float4 qq = q4[m4];
-            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
-            const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
+            const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+            const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int m = m4 * 4 + u;
-                const float2 k2 = make_float2(kr[u], kr[u]);
-                const float2 q2 = make_float2(qr[u], qr[u]);
-                R[m][0] = __ffma2_rn(k2, ea, R[m][0]);
-                R[m][1] = __ffma2_rn(k2, eb, R[m][1]);
-                oa = __ffma2_rn(R[m][0], q2, oa);
-                ob = __ffma2_rn(R[m][1], q2, ob);
+            for (int j = 0; j < 4; ++j) {
+                R[2 * m4][j] = __ffma2_rn(k01, e2[j], R[2 * m4][j]);
+                R[2 * m4 + 1][j] = __ffma2_rn(k23, e2[j], R[2 * m4 + 1][j]);
+                oacc[j] = __ffma2_rn(R[2 * m4][j], q01, oacc[j]);
+                oacc[j] = __ffma2_rn(R[2 * m4 + 1][j], q23, oacc[j]);
             }
         }
         if (t + 1 == a.commit_at) {
 #pragma unroll
-            for (int m = 0; m < NR; ++m)
-                st_stream(reinterpret_cast<float4*>(sbase + size_t(rg * NR + m) * row_stride),
-                          make_float4(cs * R[m][0].x, cs * R[m][0].y, cs * R[m][1].x, cs * R[m][1].y));
+            for (int p = 0; p < NR / 2; ++p) {
+                st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p) * row_stride),
+                          make_float4(cs * R[p][0].x, cs * R[p][1].x, cs * R[p][2].x, cs * R[p][3].x));
+                st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p + 1) * row_stride),
+                          make_float4(cs * R[p][0].y, cs * R[p][1].y, cs * R[p][2].y, cs * R[p][3].y));
+            }
         }
-        float4 o = make_float4(oa.x, oa.y, ob.x, ob.y);
-        o.x += __shfl_xor_sync(kFullMask, o.x, 16);
-        o.y += __shfl_xor_sync(kFullMask, o.y, 16);
-        o.z += __shfl_xor_sync(kFullMask, o.z, 16);
-        o.w += __shfl_xor_sync(kFullMask, o.w, 16);
-        if (lane < 16) red_o[b][warp][c] = o;
+        float os[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) os[j] = oacc[j].x + oacc[j].y;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) os[j] += __shfl_xor_sync(kFullMask, os[j], o);
+        const float sc = cs * rq * 0.08838834764831845f;  // cs rq / sqrt(128)
+        const float4 ot = make_float4(os[0] * sc, os[1] * sc, os[2] * sc, os[3] * sc);
+        float e = rb == 0 ? ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w : 0.f;
+        if (rb == 0) *reinterpret_cast<float4*>(&osm[t][col]) = ot;
+        e += __shfl_xor_sync(kFullMask, e, 1);
+        e += __shfl_xor_sync(kFullMask, e, 2);
+        if (lane == 0) ssw[t][warp] = e;
     }
+    cp_async_wait_all();  // this thread's z and gamma (read only by this thread)
     __syncthreads();
-    finish_readout(ntok - 1, rq_last, cs_last);
+    if (tid < ntok) ss[tid] = (ssw[tid][0] + ssw[tid][1]) + (ssw[tid][2] + ssw[tid][3]);
 
     // the gated RMSNorm needs both halves' sums of o^2: exchange them once through the cluster
     cluster.sync();
     const float* peer_ss = cluster.map_shared_rank(ss, half ^ 1);
-    for (int idx = tid; idx < ntok * kWinHalf; idx += kWinThreads) {
+#pragma unroll
+    for (int i = 0; i < kWinMaxTok / 2; ++i) {
+        const int idx = tid + kWinThreads * i;
         const int t = idx / kWinHalf, j = idx % kWinHalf;
-        const float tot = ss[t] + peer_ss[t];
-        const float rs = rsqrtf(tot / float(D) + a.eps);
-        const size_t yi = ((size_t(n) * ntok + t) * a.h_v + h) * D + half * kWinHalf + j;
-        const int jj = half * kWinHalf + j;
-        a.y[yi] = osm[t][j] * rs * a.gamma[jj] * sigmoid_f32(a.z[yi]);
+        if (t < ntok) {
+            const float tot = ss[t] + peer_ss[t];
+            const float rs = rsqrtf(tot / float(D) + a.eps);
+            const size_t yi = ((size_t(n) * ntok + t) * a.h_v + h) * D + half * kWinHalf + j;
+            a.y[yi] = osm[t][j] * rs * gs[tid] * sigmoid_f32(zs[idx]);
+        }
     }
     cluster.sync();  // the peer has read this CTA's sums before it exits
 }
