@@ -265,8 +265,10 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 // ------------------------------------------------------------------------------------------------
 extern "C" size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
                                              int chunk_size) {
-    (void)num_seqs; (void)T; (void)Hk; (void)Hv; (void)K; (void)V; (void)chunk_size;
-    return 0;  // the chunk state lives in shared memory and TMEM
+    if (num_seqs <= 0 || T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || K != 128 || V != 128 ||
+        chunk_size != 64 || T >= (1LL << 31) - 64)
+        return 0;
+    return gdn::prefill_workspace_bytes(T, num_seqs, Hv);
 }
 
 extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
@@ -277,7 +279,6 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
                                           int chunk_size, float scale, void* out, void* workspace,
                                           size_t workspace_bytes, int32_t* dev_status,
                                           gdn_stream_t stream) {
-    (void)workspace; (void)workspace_bytes;
     REQUIRE(num_seqs >= 0 && T >= 0 && pool_size >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1,
             GDN_ERR_INVALID_ARG,
             "gdn_prefill_chunked: sizes must be num_seqs, T, pool_size >= 0 and Hk, Hv, K, V >= 1");
@@ -301,8 +302,17 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
     const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
     REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG,
             "gdn_prefill_chunked: out overlaps state_pool");
-    REQUIRE((long long)num_seqs * Hv < (1LL << 31) && T < (1LL << 31) - 64, GDN_ERR_UNSUPPORTED,
-            "gdn_prefill_chunked: grid or token count too large");
+    REQUIRE((long long)num_seqs * Hv < (1LL << 31) && T < (1LL << 31) - 64 &&
+                gdn::prefill_chunk_cap(T, num_seqs) * Hv < (1LL << 31),
+            GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: grid or token count too large");
+    const size_t ws_need = gdn::prefill_workspace_bytes(T, num_seqs, Hv);
+    REQUIRE(workspace && workspace_bytes >= ws_need, GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: workspace of %zu bytes given, %zu needed", workspace ? workspace_bytes : 0,
+            ws_need);
+    REQUIRE(aligned(workspace, 256), GDN_ERR_INVALID_ARG,
+            "gdn_prefill_chunked: workspace must be 256-byte aligned");
+    REQUIRE(!any_overlap(workspace, ws_need, out, obytes) && !any_overlap(workspace, ws_need, state_pool, pbytes),
+            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: workspace overlaps out or state_pool");
 
     gdn::PrefillArgs p;
     p.q = static_cast<const uint16_t*>(q);
@@ -324,7 +334,7 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
     p.Hv = Hv;
     p.scale = scale;
     p.eps = 1e-6f;
-    const cudaError_t e = gdn::launch_prefill(p, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = gdn::launch_prefill(p, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(GDN_ERR_CUDA, "gdn_prefill_chunked: launch failed (TMA descriptors or kernel): %s",
                     cudaGetErrorString(e));

@@ -14,6 +14,13 @@ void launch_decode_multi(DecodeMultiArgs a, int B, int Dk, cudaStream_t stream);
 void launch_comba(const CombaArgs& a, int heads, int K, int V, cudaStream_t stream);
 void launch_window(const WindowArgs& a, int N, cudaStream_t stream);
 // Raises the kernel's shared-memory limit once per device, then launches; returns the launch error.
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// The prefill workspace: the chunk offsets (8 bytes per sequence + 1, padded to 1 KB), then one
+// kPfRecordBytes record per (chunk, value head) for up to ceil(T / 64) + num_seqs chunks.
+inline size_t prefill_header_bytes(int num_seqs) {
+    return (static_cast<size_t>(num_seqs + 1) * 8 + 1023) / 1024 * 1024;
+}
+long long prefill_chunk_cap(long long T, int num_seqs);
+size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv);
+cudaError_t launch_prefill(const PrefillArgs& a, void* workspace, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,5 +1,5 @@
-// prefill.cu -- launch of the chunkwise-WY prefill kernel (kernel in prefill.cuh): TMA descriptors of
-// q, k, v and the per-device shared-memory limit.
+// prefill.cu -- launch of the chunkwise-WY prefill (kernels in prefill.cuh): the workspace layout, the
+// TMA descriptors of q, k, v and the per-device shared-memory limits.
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -13,7 +13,7 @@ namespace gdn {
 
 namespace {
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_smem_set[kMaxDevices];  // per device: dynamic shared memory limit raised
+std::atomic<int> g_smem_set[kMaxDevices];  // per device: dynamic shared memory limits raised
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -44,7 +44,15 @@ bool encode_rows(CUtensorMap* map, const void* base, long long T, int H) {
 }
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+long long prefill_chunk_cap(long long T, int num_seqs) { return (T + pf::C - 1) / pf::C + num_seqs; }
+
+size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) {
+    if (num_seqs <= 0) return 0;
+    return prefill_header_bytes(num_seqs) +
+           static_cast<size_t>(prefill_chunk_cap(T, num_seqs)) * Hv * static_cast<size_t>(kPfRecordBytes);
+}
+
+cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -53,17 +61,30 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(pf::SMEM_BYTES));
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gdn_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(pf::P_SMEM));
+        if (e != cudaSuccess) return e;
         g_smem_set[dev].store(1, std::memory_order_release);
     }
+    PrefillArgs a = args;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.chunk_off = reinterpret_cast<long long*>(ws);
+    a.records = ws + prefill_header_bytes(a.num_seqs);
+    a.cap = prefill_chunk_cap(a.T, a.num_seqs);
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (a.T > 0) {  // with T = 0 every sequence is empty and the kernel never reads the maps
+    if (a.T > 0) {  // with T = 0 every sequence is empty and no kernel reads the maps
         if (!encode_rows(&maps.q, a.q, a.T, a.Hk) || !encode_rows(&maps.k, a.k, a.T, a.Hk) ||
             !encode_rows(&maps.v, a.v, a.T, a.Hv))
             return cudaErrorInvalidValue;
     }
+    gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.chunk_off);
+    if (a.T > 0) {
+        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hv);
+        gdn_prefill_prep_kernel<<<pgrid, pf::NT, pf::P_SMEM, stream>>>(a, maps);
+    }
     const unsigned grid = static_cast<unsigned>(a.num_seqs) * static_cast<unsigned>(a.Hv);
-    gdn_prefill_kernel<<<grid, pf::NT, pf::SMEM_BYTES, stream>>>(a, maps);
+    gdn_prefill_kernel<<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
     return cudaGetLastError();
 }
 

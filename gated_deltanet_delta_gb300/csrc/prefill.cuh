@@ -15,14 +15,23 @@
 // with D_ts = e^{G_t-G_s} for s <= t (0 above the diagonal), gamma_t = e^{G_t}, D_L = D_{L-1,.}.
 // The page's w recursion is read untransposed and its "U^T K" as U K^T (the [V, K] state layout).
 //
-// GB300 mapping.  One CTA of 512 threads per (sequence, value head); threads i, i + 128, i + 256
-// and i + 384 share TMEM lane i (each takes a quarter of the columns).  q, k and v rows arrive by
-// TMA (cp.async.bulk.tensor, 64 tokens x 64 features per box) straight into the swizzled operand
-// tiles; the next chunk's v and q are fetched as soon as their last MMA has read them, its k after
-// the state update.  The fp32 state S (V x K = 128 x 128) lives in TMEM
-// for the whole sequence and reaches HBM only at the start (gather from the pool slot) and at the
-// end (scatter back).  Every contraction is a
-// tcgen05.mma with M = 128 (the transposed forms keep V or the feature index on M):
+// GB300 mapping: three kernels on one stream.
+//   gdn_prefill_offsets_kernel (one CTA): the first chunk of every sequence (a scan of the chunk
+//     counts), so that every chunk of every sequence has a flat index f.
+//   gdn_prefill_prep_kernel (one CTA of 512 threads per (chunk, value head), two per SM): all the
+//     work that does not depend on the carried state -- row norms, gates, G = [K; Q] K^T on the
+//     tensor core, Lm and M, the triangular inverse, Tw = T diag(beta gamma rk) and Tu = T diag(beta)
+//     split into bf16 high and low parts -- written as one chunk record (kPfRecordBytes, the
+//     shared-memory image the sequential kernel uses) by one bulk store.  This is the bulk of the
+//     CUDA-core work; here every chunk of every sequence runs in parallel.
+//   gdn_prefill_kernel (one CTA of 512 threads per (sequence, value head)): the chunk recurrence.
+//     The fp32 state S (V x K = 128 x 128) lives in TMEM for the whole sequence and reaches HBM only
+//     at the start (gather from the pool slot) and at the end (scatter back).  Per chunk it takes
+//     q, k, v rows by TMA (cp.async.bulk.tensor, 64 tokens x 64 features per box) and the chunk
+//     record by two bulk copies, all fetched a chunk ahead as their buffers free up; threads i,
+//     i + 128, i + 256 and i + 384 share TMEM lane i (each takes a quarter of the columns).
+// Every contraction is a tcgen05.mma with M = 128 (the transposed forms keep V or the feature index
+// on M):
 //     G   = [K; Q] K^T              M=128 (64 k rows + 64 q rows), N=64,  K=128   bf16 (exact inputs)
 //     W^T = K^T Tw^T,  U^T = V^T Tu^T   M=128, N=64, K=64   (Tw = T diag(beta gamma rk), Tu = T diag(beta))
 //     Delta^T = U^T - S0 W^T,  P^T = S0 Q^T                M=128, N=64, K=128
@@ -50,23 +59,65 @@ constexpr int D = 128;    // K = V = 128
 constexpr int NT = 512;   // threads per CTA: four per TMEM lane, each with a quarter of the columns
 constexpr int LST = 68;   // row stride (floats) of the fp32 Lm and T matrices: rows are 16-byte aligned
 constexpr int ZST = 36;   // row stride (floats) of the 32 x 32 scratch of the inverse
-// dynamic shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;       // [K;Q] tile: two 64-feature halves of 16 KB, each 64 k rows + 64 q rows
-constexpr uint32_t OFF_V = 32768;    // V tile: two halves of 8 KB (64 token rows)
-constexpr uint32_t OFF_S = 49152;    // S0 bf16, K-major, 128 v rows, two halves of 16 KB
-constexpr uint32_t OFF_W = 81920;    // W as MN-major B operand: 128 feature rows x 64 t
-constexpr uint32_t OFF_T4 = 98304;   // Tw hi, Tw lo, Tu hi, Tu lo (8 KB each); later Delta~ hi, lo (16 KB each)
-constexpr uint32_t OFF_DL = 131072;  // Delta^T hi, lo (16 KB each): 128 v rows x 64 s
-constexpr uint32_t OFF_M = 163840;   // M hi, lo (8 KB each): 64 t rows x 64 s
-constexpr uint32_t OFF_L = 180224;   // fp32 [64][LST] strictly lower Lm
-constexpr uint32_t OFF_T = OFF_L + 64 * LST * 4;  // fp32 [64][LST] T = (I + Lm)^-1
-constexpr uint32_t OFF_X = OFF_T + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
-constexpr uint32_t SMEM_USED = OFF_X + 32 * ZST * 4;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-// TMEM columns (fp32, 128 lanes)
-constexpr uint32_t TM_S = 0, TM_G = 128, TM_W = 192, TM_U = 256, TM_P = 320, TM_MD = 384;
-constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t kWaitLimit = 1u << 26;  // mbarrier polls before giving up (seconds of waiting)
+
+// chunk record (bytes): Tw hi, Tw lo, Tu hi, Tu lo | M hi, M lo | vectors
+constexpr uint32_t REC_T4 = 0, REC_M = 32768, REC_VEC = 49152, REC_BYTES = 51200;
+constexpr uint32_t REC_PART1 = REC_M;                // Tw/Tu: used first, refetched first
+constexpr uint32_t REC_PART2 = REC_BYTES - REC_M;    // M and the vectors
+// vector offsets (floats) inside the record's vector block
+constexpr int V_GQ = 0, V_RQ = 64, V_DL = 128, V_RK = 192, V_GL = 256;
+
+// the chunk-preparation kernel's dynamic shared memory (bytes from a 1024-aligned base); the first
+// REC_BYTES are the record being built, stored by one bulk copy at the end
+constexpr uint32_t P_KQ = 0;         // [K;Q] tile (two 16 KB feature halves: 64 k rows + 64 q rows);
+                                     // once G is computed, Tw / Tu hi / lo (record bytes 0 .. 32 KB)
+constexpr uint32_t P_M = REC_M;      // M hi / lo (record bytes 32 .. 48 KB)
+constexpr uint32_t P_VEC = REC_VEC;  // record vectors
+constexpr uint32_t P_L = REC_BYTES;  // fp32 [64][LST] strictly lower Lm
+constexpr uint32_t P_T = P_L + 64 * LST * 4;  // fp32 [64][LST] T = (I + Lm)^-1
+constexpr uint32_t P_X = P_T + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
+constexpr uint32_t P_USED = P_X + 32 * ZST * 4;
+constexpr uint32_t P_SMEM = P_USED + 1024;
+constexpr uint32_t P_TM_G = 0, P_TM_COLS = 64;
+
+// the sequential kernel's dynamic shared memory
+constexpr uint32_t OFF_K = 0;         // two K tiles (chunks of even / odd index), 16 KB each: two
+                                      // 64-feature halves of 8 KB, 64 token rows each
+constexpr uint32_t OFF_Q = 32768;     // Q tile (two halves of 8 KB)
+constexpr uint32_t OFF_V = 49152;     // V tile (two halves of 8 KB)
+constexpr uint32_t OFF_S = 65536;     // S0 bf16, K-major, 128 v rows, two halves of 16 KB
+constexpr uint32_t OFF_T4 = 98304;    // record part: Tw hi, Tw lo, Tu hi, Tu lo
+constexpr uint32_t OFF_M = OFF_T4 + REC_M;      // record part: M hi, M lo
+constexpr uint32_t OFF_VEC = OFF_T4 + REC_VEC;  // record part: the vectors, two buffers of 2 KB
+constexpr uint32_t OFF_DL = OFF_VEC + 2 * (REC_BYTES - REC_VEC);  // Delta^T hi, lo (16 KB each)
+constexpr uint32_t OFF_DT = OFF_DL + 32768;     // Delta~^T hi, lo (16 KB each); before them, W as
+                                                // the MN-major B operand (128 feature rows x 64 t)
+constexpr uint32_t SMEM_USED = OFF_DT + 32768;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+// TMEM columns (fp32, 128 lanes); P and (M Delta) alternate between two buffers by chunk parity
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_P = 256, TM_MD = 384;
+constexpr uint32_t TM_COLS = 512;
+// the sequential kernel's threads: 16 worker warps (conversions, outputs) and one control warp
+// (lane 0 issues every MMA and every copy)
+constexpr int NW = 16, NTS = 32 * (NW + 1);
+// its mbarriers: MMA completions (tcgen05.commit), worker hand-offs (one arrival per worker warp)
+// and copies
+enum : int {
+    B_A = 0,   // P and Delta of a chunk computed
+    B_C,       // (M Delta) and the state update computed
+    B_WU,      // W and U of a chunk computed
+    R_B,       // workers: Delta converted, state scaled
+    R_D,       // workers: S0 and W of the next chunk in place
+    R_Z,       // workers: the tail of a short chunk zeroed
+    B_K0, B_K1, B_Q, B_V, B_R1, B_RM, B_RV0, B_RV1,
+    NBAR
+};
+
+static_assert(REC_BYTES == kPfRecordBytes && REC_VEC == kPfRecordVec, "chunk record layout");
+static_assert(OFF_DL % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_M % 1024 == 0, "operand tiles 1024-aligned");
+static_assert(2 * (P_SMEM + 1024) <= 228 * 1024, "two preparation CTAs per SM");
+static_assert(SMEM_BYTES <= 227 * 1024, "sequential kernel shared memory");
 }  // namespace pf
 
 // Pack 8 floats to 8 bf16 (round to nearest even) in a uint4.
@@ -107,196 +158,175 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
         v[16 + i] = b[i];
     }
 }
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return p + ((1024u - (tc::smem_u32(p) & 1023u)) & 1023u);
+}
 
-__global__ void __launch_bounds__(pf::NT, 1)
-    gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
+// ------------------------------------------------------------------------------------------------
+// The first chunk of every sequence: chunk_off[n] = sum over n' < n of ceil(len_n' / 64), with 0
+// chunks for a sequence whose bounds are invalid (flagged by the sequential kernel).  One CTA.
+constexpr int kPfOffThreads = 1024;
+__global__ void __launch_bounds__(kPfOffThreads)
+    gdn_prefill_offsets_kernel(const int64_t* cu_seqlens, int num_seqs, long long T, long long* chunk_off) {
+    __shared__ long long warp_tot[kPfOffThreads / 32];
+    __shared__ long long carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < num_seqs; base += kPfOffThreads) {
+        const int i = base + tid;
+        long long cnt = 0;
+        if (i < num_seqs) {
+            const long long bos = cu_seqlens[i], eos = cu_seqlens[i + 1];
+            if (bos >= 0 && eos >= bos && eos <= T) cnt = (eos - bos + pf::C - 1) / pf::C;
+        }
+        long long x = cnt;  // inclusive scan inside the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long w = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(kFullMask, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_tot[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const long long before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - cnt;
+        if (i < num_seqs) chunk_off[i] = before;
+        __syncthreads();
+        if (tid == 0) carry += warp_tot[kPfOffThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0) chunk_off[num_seqs] = carry;
+}
+
+// ------------------------------------------------------------------------------------------------
+// The state-independent part of one chunk f (flat index) of one value head h -> its chunk record.
+__global__ void __launch_bounds__(pf::NT, 2)
+    gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float Gf[C], betas[C], rks[C], rqs[C], gams[C], dls[C];
+    __shared__ float Gf[C], betas[C], rks[C], rqs[C], gams[C];
     __shared__ float scan_total;
     __shared__ uint32_t tmem_slot;
-    __shared__ __align__(8) uint64_t mbar;     // MMA completion
-    __shared__ __align__(8) uint64_t bar_vq;   // TMA of the v and q rows of a chunk
-    __shared__ __align__(8) uint64_t bar_k;    // TMA of the k rows of a chunk
+    __shared__ __align__(8) uint64_t mbar;    // MMA completion
+    __shared__ __align__(8) uint64_t bar_kq;  // TMA of the chunk's k and q rows
 
-    const int n = blockIdx.x / a.Hv;
-    const int h = blockIdx.x - n * a.Hv;
+    const long long f = blockIdx.x / a.Hv;
+    const int h = static_cast<int>(blockIdx.x - f * a.Hv);
+    const long long total = a.chunk_off[a.num_seqs];
+    if (f >= total || f >= a.cap) return;
+    // the sequence holding chunk f: chunk_off[n] <= f < chunk_off[n + 1]
+    int lo = 0, hi = a.num_seqs;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a.chunk_off[mid] <= f) lo = mid; else hi = mid;
+    }
+    const int n = lo;
+    if (a.chunk_off[n + 1] > a.cap) return;  // past the workspace: the sequential kernel flags it
+    const long long bos = a.cu_seqlens[n], Tn = a.cu_seqlens[n + 1] - bos;
+    const long long c0 = (f - a.chunk_off[n]) * C;
+    const int L = static_cast<int>(Tn - c0 < C ? Tn - c0 : C);
+
     const int hk = h / (a.Hv / a.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row = tid & 127;   // the TMEM lane this thread reads and writes
+    const int row = tid & 127;   // the TMEM lane this thread reads
     const int qt = tid >> 7;     // which quarter of the columns
-
-    // ---- sequence bounds and pool slot (uniform over the CTA; bad ones are flagged and skipped)
-    const long long bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
-    if (bos < 0 || eos < bos || eos > a.T) {
-        if (tid == 0) atomicOr(a.status, 2);
-        return;
-    }
-    const long long slot = a.cache_indices[n];
-    if (slot < 0 || slot >= a.pool_size) {
-        if (tid == 0) atomicOr(a.status, 1);
-        return;
-    }
-    const long long Tn = eos - bos;
-    if (Tn == 0) return;
-
-    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = tc::smem_u32(sm);
-    float* Ls = reinterpret_cast<float*>(sm + OFF_L);
-    float* Ts = reinterpret_cast<float*>(sm + OFF_T);
-    float* Xs = reinterpret_cast<float*>(sm + OFF_X);
+    float* Ls = reinterpret_cast<float*>(sm + P_L);
+    float* Ts = reinterpret_cast<float*>(sm + P_T);
+    float* Xs = reinterpret_cast<float*>(sm + P_X);
+    float* vec = reinterpret_cast<float*>(sm + P_VEC);
 
-    if (warp == 0) tc::tmem_alloc(&tmem_slot, TM_COLS);
+    if (warp == 0) tc::tmem_alloc(&tmem_slot, P_TM_COLS);
     if (tid == 0) {
         tc::mbar_init(&mbar, 1);
-        tc::mbar_init(&bar_vq, 1);
-        tc::mbar_init(&bar_k, 1);
+        tc::mbar_init(&bar_kq, 1);
+        const int z = static_cast<int>(bos + c0);
+        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
+        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_kq);
     }
-    // T's blocks above the diagonal stay zero for the whole kernel
+    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < L)
+    if (tid < L) {
+        const size_t gi = static_cast<size_t>(bos + c0 + tid) * a.Hv + h;
+        a_raw = a.a[gi];
+        b_raw = a.b[gi];
+    }
+    const float a_mul = expf(a.A_log[h]);
+    const float dtb = a.dt_bias[h];
+    // T's blocks above the diagonal stay zero
     for (int i = tid; i < C * LST; i += NT) Ts[i] = 0.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = tmem_slot;
     const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
-    uint32_t phase = 0, ph_vq = 0, ph_k = 0;
     bool timed_out = false;
-    // operand descriptors at their tile bases (K-major: LBO unused; MN-major: LBO = half stride)
-    const uint64_t dKQ = tc::sdesc(sb + OFF_KQ, 16, 1024);         // [K; Q] rows, K-major
-    const uint64_t dKmn = tc::sdesc(sb + OFF_KQ, 16384, 1024);     // k rows read MN-major
-    const uint64_t dVmn = tc::sdesc(sb + OFF_V, 8192, 1024);       // v rows read MN-major
-    const uint64_t dS0 = tc::sdesc(sb + OFF_S, 16, 1024);          // S0, K-major
-    const uint64_t dWmn = tc::sdesc(sb + OFF_W, 8192, 1024);       // W, MN-major
-    const uint64_t dT4 = tc::sdesc(sb + OFF_T4, 16, 1024);         // Tw/Tu hi/lo, then Delta~ hi/lo
-    const uint64_t dDL = tc::sdesc(sb + OFF_DL, 16, 1024);         // Delta hi/lo
-    const uint64_t dM = tc::sdesc(sb + OFF_M, 16, 1024);           // M hi/lo
 
-    // one thread polls the mbarrier for the MMAs committed so far; the barrier releases the rest
-    // (a timeout on that thread stops every thread)
-    auto mma_wait = [&]() -> bool {
-        const bool ok = tid != 0 || tc::mbar_wait(&mbar, phase, kWaitLimit);
-        phase ^= 1u;
-        const bool all = __syncthreads_and(ok ? 1 : 0) != 0;
-        tc::fence_after();
-        return all;
-    };
-    auto publish = [&]() {
-        tc::wait_st();
-        tc::fence_proxy_async();
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-    };
-
-    // ---- gather the state from its pool slot: row v, columns 32*qt .. -> TMEM and S0 (bf16)
-    float* Sg = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * D * D;
-    {
-        const float4* src = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
-#pragma unroll
-        for (int c16 = 0; c16 < 2; ++c16) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 f = src[c16 * 4 + j];
-                v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-            }
-            tc::st16(trow + TM_S + 32 * qt + c16 * 16, v);
-            const int c8 = 4 * qt + 2 * c16;
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8, 128)) = pack_bf16x8(v);
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + 1, 128)) = pack_bf16x8(v + 8);
-        }
-    }
-
-    const float a_mul = expf(a.A_log[h]);
-    const float dtb = a.dt_bias[h];
-    const size_t vo_stride = static_cast<size_t>(a.Hv) * D;  // elements between tokens of v, out
-
-    // TMA of one chunk's rows (thread 0): v and q (both halves of each) on bar_vq, k on bar_k.  The
-    // boxes land in the 128-byte swizzled operand layout; rows past T arrive as zeros.
-    auto issue_vq = [&](long long c0n) {
-        const int z = static_cast<int>(bos + c0n);
-        tc::mbar_expect_tx(&bar_vq, 4 * 8192);
-        tc::tma_load_3d(sb + OFF_KQ + 8192, &maps.q, 0, hk, z, &bar_vq);
-        tc::tma_load_3d(sb + OFF_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_vq);
-        tc::tma_load_3d(sb + OFF_V, &maps.v, 0, h, z, &bar_vq);
-        tc::tma_load_3d(sb + OFF_V + 8192, &maps.v, 64, h, z, &bar_vq);
-    };
-    auto issue_k = [&](long long c0n) {
-        const int z = static_cast<int>(bos + c0n);
-        tc::mbar_expect_tx(&bar_k, 2 * 8192);
-        tc::tma_load_3d(sb + OFF_KQ, &maps.k, 0, hk, z, &bar_k);
-        tc::tma_load_3d(sb + OFF_KQ + 16384, &maps.k, 64, hk, z, &bar_k);
-    };
-    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < 64)
-    auto load_gates = [&](long long c0n) {
-        if (tid < Tn - c0n && tid < C) {
-            const size_t gi = static_cast<size_t>(bos + c0n + tid) * a.Hv + h;
-            a_raw = a.a[gi];
-            b_raw = a.b[gi];
-        }
-    };
-    if (tid == 0) {
-        issue_vq(0);
-        issue_k(0);
-    }
-    load_gates(0);
-    const int rp = tid >> 4, ch = tid & 15;  // norms: 16 threads per row, rows rp and rp + 32
-    publish();
-
-    for (long long c0 = 0; c0 < Tn && !timed_out; c0 += C) {
-        const int L = static_cast<int>(Tn - c0 < C ? Tn - c0 : C);
-        const long long tok0 = bos + c0;
-
-        // ---- 1. wait for this chunk's rows, zero the rows past the sequence end, row norms
+    do {
+        // ---- 1. wait for the rows, zero the rows past the sequence end, row norms
         {
-            const bool ok = tc::mbar_wait(&bar_vq, ph_vq, kWaitLimit) && tc::mbar_wait(&bar_k, ph_k, kWaitLimit);
-            ph_vq ^= 1u;
-            ph_k ^= 1u;
-            if (!__syncthreads_and(ok ? 1 : 0)) { timed_out = true; break; }
+            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, 0, kWaitLimit);
+            if (!__syncthreads_and(ok ? 1 : 0)) {  // give the copies one more bounded wait
+                if (tid == 0) tc::mbar_wait(&bar_kq, 0, kWaitLimit);
+                timed_out = true;
+                break;
+            }
         }
         if (L < C) {
             for (int e = tid; e < (C - L) * 16; e += NT) {
                 const int s = L + (e >> 4), c = e & 15;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(s, c, 128)) = z;
-                *reinterpret_cast<uint4*>(sm + OFF_KQ + tc::sw_chunk(64 + s, c, 128)) = z;
-                *reinterpret_cast<uint4*>(sm + OFF_V + tc::sw_chunk(s, c, 64)) = z;
+                *reinterpret_cast<uint4*>(sm + P_KQ + tc::sw_chunk(s, c, 128)) = z;
+                *reinterpret_cast<uint4*>(sm + P_KQ + tc::sw_chunk(64 + s, c, 128)) = z;
             }
             __syncthreads();
         }
+        {
+            const int rp = tid >> 4, ch = tid & 15;  // 16 threads per row, rows rp and rp + 32
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const int s = p * 32 + rp;
-            const uint4 kv4 = *reinterpret_cast<const uint4*>(sm + OFF_KQ + tc::sw_chunk(s, ch, 128));
-            const uint4 qv4 = *reinterpret_cast<const uint4*>(sm + OFF_KQ + tc::sw_chunk(64 + s, ch, 128));
-            float sk = bf16_sumsq8(kv4), sq = bf16_sumsq8(qv4);
+            for (int p = 0; p < 2; ++p) {
+                const int s = p * 32 + rp;
+                const uint4 kv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(s, ch, 128));
+                const uint4 qv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + s, ch, 128));
+                float sk = bf16_sumsq8(kv4), sq = bf16_sumsq8(qv4);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                sk += __shfl_xor_sync(kFullMask, sk, o);
-                sq += __shfl_xor_sync(kFullMask, sq, o);
-            }
-            if (ch == 0) {
-                rks[s] = rsqrtf(sk + a.eps);
-                rqs[s] = rsqrtf(sq + a.eps);
+                for (int o = 8; o > 0; o >>= 1) {
+                    sk += __shfl_xor_sync(kFullMask, sk, o);
+                    sq += __shfl_xor_sync(kFullMask, sq, o);
+                }
+                if (ch == 0) {
+                    rks[s] = rsqrtf(sk + a.eps);
+                    rqs[s] = rsqrtf(sq + a.eps);
+                }
             }
         }
-        publish();
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
 
-        // ---- 2. G = [K; Q] K^T, committed alone; P^T = S0 Q^T is issued behind it and completes
-        //         with the next commit group (it needs only this chunk's q rows and S0)
+        // ---- 2. G = [K; Q] K^T
         if (tid == 0) {
+            const uint64_t dKQ = tc::sdesc(sb + P_KQ, 16, 1024);
             const uint32_t id = tc::idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t d = dadd(dKQ, (ks >> 2) * 16384 + (ks & 3) * 32);
-                tc::mma_bf16(tm + TM_G, d, d, id, ks > 0);
+                tc::mma_bf16(tm + P_TM_G, d, d, id, ks > 0);
             }
             tc::commit(&mbar);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                tc::mma_bf16(tm + TM_P, dadd(dS0, off), dadd(dKQ, 8192 + off), id, ks > 0);
-            }
         }
         // ---- 3. gates and their in-chunk cumulative sum (while G is computed)
         if (tid < C) {
@@ -322,15 +352,29 @@ __global__ void __launch_bounds__(pf::NT, 1)
         }
         __syncthreads();
         if (tid < C) {
-            gams[tid] = __expf(Gf[tid]);
-            dls[tid] = tid < L ? __expf(Gf[L - 1] - Gf[tid]) : 0.f;
+            const int t = tid;
+            gams[t] = __expf(Gf[t]);
+            const float rq = rqs[t] * a.scale;
+            vec[V_GQ + t] = gams[t] * rq;
+            vec[V_RQ + t] = rq;
+            vec[V_DL + t] = t < L ? __expf(Gf[L - 1] - Gf[t]) : 0.f;
+            vec[V_RK + t] = rks[t];
         }
-        if (!mma_wait()) { timed_out = true; break; }
+        {
+            const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, kWaitLimit);
+            if (!__syncthreads_and(ok ? 1 : 0)) {
+                if (tid == 0) tc::mbar_wait(&mbar, 0, kWaitLimit);
+                timed_out = true;
+                break;
+            }
+            tc::fence_after();
+        }
+        if (tid == 0) vec[V_GL] = gams[L - 1];
 
         // ---- 4. Lm (lanes t < 64, fp32) and M (lanes 64 + t, bf16 hi / lo) from G, 16 columns each
         {
             float g[16];
-            tc::ld16(trow + TM_G + 16 * qt, g);
+            tc::ld16(trow + P_TM_G + 16 * qt, g);
             tc::wait_ld();
             const int s0 = 16 * qt;
             if (row < C) {
@@ -358,10 +402,10 @@ __global__ void __launch_bounds__(pf::NT, 1)
                         const int s = s0 + c * 8 + i;
                         m8[i] = s <= t ? rks[s] * g[c * 8 + i] * __expf(Gt - Gf[s]) : 0.f;
                     }
-                    uint4 hi, lo;
-                    split_bf16x8(m8, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + OFF_M + tc::sw_chunk(t, 2 * qt + c, 64)) = hi;
-                    *reinterpret_cast<uint4*>(sm + OFF_M + 8192 + tc::sw_chunk(t, 2 * qt + c, 64)) = lo;
+                    uint4 mh, ml;
+                    split_bf16x8(m8, mh, ml);
+                    *reinterpret_cast<uint4*>(sm + P_M + tc::sw_chunk(t, 2 * qt + c, 64)) = mh;
+                    *reinterpret_cast<uint4*>(sm + P_M + 8192 + tc::sw_chunk(t, 2 * qt + c, 64)) = ml;
                 }
             }
         }
@@ -468,11 +512,12 @@ __global__ void __launch_bounds__(pf::NT, 1)
         }
         __syncthreads();
 
-        // ---- 6. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major)
+        // ---- 6. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major),
+        //         over the [K;Q] tile, which G no longer needs
         {
             const int t = tid & (C - 1);
             const bool w_side = ((tid >> 6) & 1) == 0;
-            const uint32_t base = OFF_T4 + (w_side ? 0u : 16384u);
+            const uint32_t base = P_KQ + (w_side ? 0u : 16384u);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int cc = 2 * qt + c;
@@ -486,147 +531,412 @@ __global__ void __launch_bounds__(pf::NT, 1)
                     const float w = w_side ? betas[s] * gams[s] * rks[s] : betas[s];
                     x8[i] = tv[i] * w;
                 }
-                uint4 hi, lo;
-                split_bf16x8(x8, hi, lo);
-                *reinterpret_cast<uint4*>(sm + base + tc::sw_chunk(t, cc, 64)) = hi;
-                *reinterpret_cast<uint4*>(sm + base + 8192 + tc::sw_chunk(t, cc, 64)) = lo;
+                uint4 th, tl;
+                split_bf16x8(x8, th, tl);
+                *reinterpret_cast<uint4*>(sm + base + tc::sw_chunk(t, cc, 64)) = th;
+                *reinterpret_cast<uint4*>(sm + base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
             }
         }
-        publish();
-
-        // ---- 7. W^T = K^T Tw^T and U^T = V^T Tu^T (A MN-major from the token tiles)
+        // ---- 7. the record to the workspace (one bulk store of the shared-memory image)
+        tc::fence_proxy_async();
+        __syncthreads();
         if (tid == 0) {
-            const uint32_t id = tc::idesc_bf16(128, 64, 1, 0, 0);
+            tc::bulk_store(a.records + (f * a.Hv + h) * static_cast<long long>(REC_BYTES), sb, REC_BYTES);
+            tc::bulk_commit();
+            tc::bulk_wait_all();
+        }
+    } while (false);
+
+    if (timed_out && tid == 0) atomicOr(a.status, 4);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, P_TM_COLS);
+}
+
+// ------------------------------------------------------------------------------------------------
+// The chunk recurrence of one (sequence, value head), from its chunk records, warp-specialized.
+// Per chunk c the state path is: P = S0 Q^T and Delta = U - S0 W^T (tensor core) -> Delta to bf16
+// hi / lo and the state scaled by gamma_L (workers) -> M Delta and S += Delta~^T K (tensor core) ->
+// S to bf16 (workers).  W and U of chunk c + 1 are multiplied right behind the state update, and W
+// is converted with S; chunk c's outputs are written while chunk c + 1's P and Delta are computed
+// (P and (M Delta) alternate between two TMEM buffers).  The control lane issues the MMAs as soon
+// as the workers' hand-off arrives and each copy as soon as its buffer's last reader is done.
+__global__ void __launch_bounds__(pf::NTS, 1)
+    gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
+    using namespace pf;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ __align__(8) uint64_t bars[NBAR];
+    __shared__ volatile int abort_flag;
+
+    const int n = blockIdx.x / a.Hv;
+    const int h = blockIdx.x - n * a.Hv;
+    const int hk = h / (a.Hv / a.Hk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool control = warp == NW;
+    const int row = tid & 127;   // workers: the TMEM lane this thread reads and writes
+    const int qt = tid >> 7;     // workers: which quarter of the columns
+
+    // ---- sequence bounds, pool slot and records (uniform over the CTA; bad ones are flagged and skipped)
+    const long long bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > a.T || a.chunk_off[n + 1] > a.cap) {
+        if (tid == 0) atomicOr(a.status, 2);
+        return;
+    }
+    const long long slot = a.cache_indices[n];
+    if (slot < 0 || slot >= a.pool_size) {
+        if (tid == 0) atomicOr(a.status, 1);
+        return;
+    }
+    const long long Tn = eos - bos;
+    if (Tn == 0) return;
+    const long long nch = (Tn + C - 1) / C;
+    const long long chunk0 = a.chunk_off[n];
+    auto chunk_len = [&](long long c) -> int { return static_cast<int>(Tn - c * C < C ? Tn - c * C : C); };
+    const bool short_last = chunk_len(nch - 1) < C;
+
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = tc::smem_u32(sm);
+
+    if (warp == 0) tc::tmem_alloc(&tmem_slot, TM_COLS);
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&bars[i], (i == R_B || i == R_D || i == R_Z) ? NW : 1);
+        abort_flag = 0;
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = tmem_slot;
+    const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
+
+    // A bounded wait on phase `parity` of barrier i; on a timeout it raises the abort flag, and it
+    // gives up once someone else has.
+    auto wait_bar = [&](int i, uint32_t parity) -> bool {
+        if (tc::mbar_wait_or_abort(&bars[i], parity, kWaitLimit, &abort_flag)) return true;
+        abort_flag = 1;
+        return false;
+    };
+    // workers: lane 0 of each warp waits, the warp follows
+    auto warp_wait = [&](int i, uint32_t parity) -> bool {
+        bool ok = true;
+        if (lane == 0) ok = wait_bar(i, parity);
+        ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+        tc::fence_after();
+        return ok;
+    };
+    // workers: hand this warp's shared-memory and TMEM writes to the tensor core
+    auto warp_arrive = [&](int i) {
+        tc::wait_st();
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars[i]);
+    };
+    // operand descriptors at their tile bases (K-major: LBO unused; MN-major: LBO = half stride)
+    const uint64_t dQ = tc::sdesc(sb + OFF_Q, 16, 1024);           // q rows, K-major
+    const uint64_t dK0 = tc::sdesc(sb + OFF_K, 8192, 1024);        // k rows read MN-major (even chunks)
+    const uint64_t dVmn = tc::sdesc(sb + OFF_V, 8192, 1024);       // v rows read MN-major
+    const uint64_t dS0 = tc::sdesc(sb + OFF_S, 16, 1024);          // S0, K-major
+    const uint64_t dWmn = tc::sdesc(sb + OFF_DT, 8192, 1024);      // W, MN-major
+    const uint64_t dT4 = tc::sdesc(sb + OFF_T4, 16, 1024);         // Tw/Tu hi/lo
+    const uint64_t dDL = tc::sdesc(sb + OFF_DL, 16, 1024);         // Delta hi/lo
+    const uint64_t dDT = tc::sdesc(sb + OFF_DT, 16, 1024);         // Delta~ hi/lo
+    const uint64_t dM = tc::sdesc(sb + OFF_M, 16, 1024);           // M hi/lo
+    const size_t vo_stride = static_cast<size_t>(a.Hv) * D;       // elements between tokens of v, out
+    float* Sg = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * D * D;
+
+    // ---- workers' pieces
+    // zero the k and v rows of chunk c past the sequence end (before its W and U)
+    auto zero_tail = [&](long long c) {
+        const int L = chunk_len(c);
+        uint8_t* kt = sm + OFF_K + (c & 1) * 16384;
+        for (int e = tid; e < (C - L) * 16; e += NW * 32) {
+            const int s = L + (e >> 4), cc = e & 15;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(kt + tc::sw_chunk(s, cc, 64)) = z;
+            *reinterpret_cast<uint4*>(sm + OFF_V + tc::sw_chunk(s, cc, 64)) = z;
+        }
+    };
+    // W (W^T in TMEM) -> bf16 MN-major B operand: lane f holds W[t][f], t = 16*qt ..
+    auto convert_w = [&]() {
+        float w16[16];
+        tc::ld16(trow + TM_W + 16 * qt, w16);
+        tc::wait_ld();
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
+        for (int c = 0; c < 2; ++c)
+            *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, 2 * qt + c, 128)) = pack_bf16x8(w16 + 8 * c);
+    };
+    // S (TMEM) -> S0 (bf16, K-major) for the next chunk's P and Delta
+    auto convert_s = [&]() {
+        float s32[32];
+        ld32(trow + TM_S + 32 * qt, s32);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    tc::mma_bf16(tm + TM_W, dadd(dKmn, ks * 2048), dadd(dT4, part * 8192 + ks * 32), id,
-                                 (part | ks) != 0);
-                    tc::mma_bf16(tm + TM_U, dadd(dVmn, ks * 2048),
-                                 dadd(dT4, 16384 + part * 8192 + ks * 32), id, (part | ks) != 0);
+        for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, 4 * qt + q4, 128)) = pack_bf16x8(s32 + 8 * q4);
+    };
+    // outputs o_t = gamma_t rq_t scale P_t + rq_t scale (M Delta)_t of chunk c, tokens 16*qt ..
+    // (lane v)
+    auto outputs = [&](long long c) {
+        const int L = chunk_len(c);
+        float p16[16], m16[16];
+        tc::ld16(trow + TM_P + (c & 1) * 64 + 16 * qt, p16);
+        tc::ld16(trow + TM_MD + (c & 1) * 64 + 16 * qt, m16);
+        tc::wait_ld();
+        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC));
+        uint16_t* o = a.out + static_cast<size_t>(bos + c * C) * vo_stride + h * D + row;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            if (t < L) {
+                const float v = fmaf(p16[i], vec[V_GQ + t], m16[i] * vec[V_RQ + t]);
+                o[static_cast<size_t>(t) * vo_stride] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
+            }
+        }
+    };
+    // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
+    // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates
+    auto convert_delta = [&](long long c) {
+        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC));
+        float d16[16], sa[16], sb16[16];
+        tc::ld16(trow + TM_U + 16 * qt, d16);
+        tc::ld16(trow + TM_S + 32 * qt, sa);
+        tc::ld16(trow + TM_S + 32 * qt + 16, sb16);
+        tc::wait_ld();
+#pragma unroll
+        for (int cc2 = 0; cc2 < 2; ++cc2) {
+            const int cc = 2 * qt + cc2;
+            uint4 hi, lo;
+            split_bf16x8(d16 + 8 * cc2, hi, lo);
+            *reinterpret_cast<uint4*>(sm + OFF_DL + tc::sw_chunk(row, cc, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + OFF_DL + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
+            float x8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] = d16[8 * cc2 + i] * vec[V_DL + 8 * cc + i] * vec[V_RK + 8 * cc + i];
+            split_bf16x8(x8, hi, lo);
+            *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, cc, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + OFF_DT + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
+        }
+        const float gL = vec[V_GL];
+        float lo16[16], hi16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            lo16[i] = sa[i] * gL;
+            hi16[i] = sb16[i] * gL;
+        }
+        tc::st16(trow + TM_S + 32 * qt, lo16);
+        tc::st16(trow + TM_S + 32 * qt + 16, hi16);
+    };
+
+    if (control) {
+        if (lane == 0) {
+            // barriers with an operation of this lane in flight, and the parity of its phase (for
+            // the bounded drain after an abort)
+            uint32_t inflight = 0, lastpar = 0;
+            auto mark = [&](int i, uint32_t parity) {
+                inflight |= 1u << i;
+                lastpar = (lastpar & ~(1u << i)) | (parity << i);
+            };
+            // q, k, v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
+            auto fetch_rows = [&](const CUtensorMap* map, int head, long long c, uint32_t dst, int bar,
+                                  uint32_t parity) {
+                const int z = static_cast<int>(bos + c * C);
+                tc::mbar_expect_tx(&bars[bar], 2 * 8192);
+                tc::tma_load_3d(sb + dst, map, 0, head, z, &bars[bar]);
+                tc::tma_load_3d(sb + dst + 8192, map, 64, head, z, &bars[bar]);
+                mark(bar, parity);
+            };
+            // a part of chunk c's record by a bulk copy
+            auto fetch_rec = [&](long long c, uint32_t from, uint32_t bytes, uint32_t dst, int bar, uint32_t parity) {
+                const uint8_t* rec = a.records + ((chunk0 + c) * a.Hv + h) * static_cast<long long>(REC_BYTES);
+                tc::mbar_expect_tx(&bars[bar], bytes);
+                tc::bulk_load(sb + dst, rec + from, bytes, &bars[bar]);
+                mark(bar, parity);
+            };
+            auto fetch_k = [&](long long c) {
+                fetch_rows(&maps.k, hk, c, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
+            };
+            auto fetch_q = [&](long long c) { fetch_rows(&maps.q, hk, c, OFF_Q, B_Q, c & 1); };
+            auto fetch_v = [&](long long c) { fetch_rows(&maps.v, h, c, OFF_V, B_V, c & 1); };
+            auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_M - REC_T4, OFF_T4, B_R1, c & 1); };
+            auto fetch_rm = [&](long long c) { fetch_rec(c, REC_M, REC_VEC - REC_M, OFF_M, B_RM, c & 1); };
+            auto fetch_rv = [&](long long c) {
+                fetch_rec(c, REC_VEC, REC_BYTES - REC_VEC, OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC),
+                          B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1);
+            };
+            // W^T = K^T Tw^T and U^T = V^T Tu^T of chunk c (A MN-major from the token tiles)
+            auto issue_wu = [&](long long c) {
+                const uint64_t dK = dadd(dK0, (c & 1) * 16384);
+                const uint32_t idw = tc::idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        tc::mma_bf16(tm + TM_W, dadd(dK, ks * 2048), dadd(dT4, part * 8192 + ks * 32), idw,
+                                     (part | ks) != 0);
+                        tc::mma_bf16(tm + TM_U, dadd(dVmn, ks * 2048), dadd(dT4, 16384 + part * 8192 + ks * 32),
+                                     idw, (part | ks) != 0);
+                    }
+                tc::commit(&bars[B_WU]);
+                mark(B_WU, c & 1);
+            };
+            // the tile of chunk c is ready for W and U (a short chunk: after the workers zeroed its tail)
+            auto wu_inputs = [&](long long c) -> bool {
+                if (c == nch - 1 && short_last) return wait_bar(R_Z, 0) && wait_bar(B_R1, c & 1);
+                return wait_bar(B_K0 + static_cast<int>(c & 1), (c >> 1) & 1) && wait_bar(B_V, c & 1) &&
+                       wait_bar(B_R1, c & 1);
+            };
+
+            fetch_k(0);
+            fetch_q(0);
+            fetch_v(0);
+            fetch_r1(0);
+            fetch_rm(0);
+            fetch_rv(0);
+            if (nch > 1) fetch_k(1);
+            do {
+                if (!wu_inputs(0)) break;
+                tc::fence_after();
+                issue_wu(0);
+                if (!wait_bar(B_WU, 0)) break;
+                if (nch > 1) {
+                    fetch_v(1);
+                    fetch_r1(1);
                 }
-            tc::commit(&mbar);
-        }
-        if (!mma_wait()) { timed_out = true; break; }
-        if (c0 + C < Tn) {  // the V and Q tiles are free: fetch the next chunk's
-            if (tid == 0) issue_vq(c0 + C);
-            load_gates(c0 + C);
-        }
-
-        // ---- 8. W (bf16) as the MN-major B operand: lane f holds W[t][f], t = 16*qt ..
-        {
-            float w16[16];
-            tc::ld16(trow + TM_W + 16 * qt, w16);
-            tc::wait_ld();
+                for (long long c = 0; c < nch; ++c) {
+                    const bool more = c + 1 < nch;
+                    const uint32_t par = c & 1;
+                    const uint64_t dK = dadd(dK0, (c & 1) * 16384);
+                    // ---- A. P^T = S0 Q^T and Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated)
+                    if (!wait_bar(R_D, par) || !wait_bar(B_Q, par)) break;
+                    tc::fence_after();
+                    {
+                        const uint32_t id = tc::idesc_bf16(128, 64, 0, 0, 0);
+                        const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
-                *reinterpret_cast<uint4*>(sm + OFF_W + tc::sw_chunk(row, 2 * qt + c, 128)) =
-                    pack_bf16x8(w16 + 8 * c);
-        }
-        publish();
-
-        // ---- 9. Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated)
-        if (tid == 0) {
-            const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_P + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                         dadd(dQ, (ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                tc::mma_bf16(tm + TM_U, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32), dadd(dWmn, ks * 2048),
-                             idd, 1u);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_U, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                         dadd(dWmn, ks * 2048), idd, 1u);
+                        tc::commit(&bars[B_A]);
+                        mark(B_A, par);
+                    }
+                    if (!wait_bar(B_A, par)) break;
+                    if (more) fetch_q(c + 1);  // P read the q tile
+                    // ---- C. (M Delta)^T = Delta^T M^T (three hi / lo products) and S += Delta~^T K,
+                    //         then W and U of the next chunk
+                    if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
+                    tc::fence_after();
+                    {
+                        const uint32_t idm = tc::idesc_bf16(128, 64, 0, 0, 0);
+                        const uint32_t ids = tc::idesc_bf16(128, 128, 0, 1, 0);
+#pragma unroll
+                        for (int pr = 0; pr < 3; ++pr) {
+                            const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo
+                            const uint32_t pb = pr == 1 ? 8192u : 0u;   // M hi, lo, hi
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                tc::mma_bf16(tm + TM_MD + (c & 1) * 64, dadd(dDL, pa + ks * 32),
+                                             dadd(dM, pb + ks * 32), idm, (pr | ks) != 0);
+                        }
+#pragma unroll
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                tc::mma_bf16(tm + TM_S, dadd(dDT, part * 16384 + ks * 32), dadd(dK, ks * 2048), ids, 1u);
+                        tc::commit(&bars[B_C]);
+                        mark(B_C, par);
+                    }
+                    if (more) {
+                        if (!wu_inputs(c + 1)) break;
+                        tc::fence_after();
+                        issue_wu(c + 1);
+                        fetch_rv(c + 1);  // its buffer's last reader, chunk c - 1's outputs, is done (R_B)
+                    }
+                    if (!wait_bar(B_C, par)) break;
+                    if (more) {
+                        fetch_rm(c + 1);                   // (M Delta) read M
+                        if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
+                        if (!wait_bar(B_WU, (c + 1) & 1)) break;
+                        if (c + 2 < nch) {                 // U read the v tile, W and U the record part
+                            fetch_v(c + 2);
+                            fetch_r1(c + 2);
+                        }
+                    }
+                }
+            } while (false);
+            if (abort_flag) {  // give what is still in flight one more bounded wait
+                for (int i = 0; i < NBAR; ++i)
+                    if (inflight & (1u << i)) tc::mbar_wait(&bars[i], (lastpar >> i) & 1u, 1u << 20);
             }
-            tc::commit(&mbar);
         }
-        if (!mma_wait()) { timed_out = true; break; }
-
-        // ---- 10. Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each;
-        //          the state is scaled by gamma_L in TMEM before the update accumulates onto it
-        {
-            float d16[16], sa[16], sb16[16];
-            tc::ld16(trow + TM_U + 16 * qt, d16);
-            tc::ld16(trow + TM_S + 32 * qt, sa);
-            tc::ld16(trow + TM_S + 32 * qt + 16, sb16);
-            tc::wait_ld();
+        __syncwarp();  // the control warp reconverges before the CTA barrier
+    } else {
+        // ---- workers
+        do {
+            // gather the state from its pool slot: row v, columns 32*qt .. -> TMEM and S0 (bf16)
+            {
+                const float4* src = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int cc = 2 * qt + c;
-                uint4 hi, lo;
-                split_bf16x8(d16 + 8 * c, hi, lo);
-                *reinterpret_cast<uint4*>(sm + OFF_DL + tc::sw_chunk(row, cc, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + OFF_DL + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
-                float x8[8];
+                for (int c16 = 0; c16 < 2; ++c16) {
+                    float v[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x8[i] = d16[8 * c + i] * dls[8 * cc + i] * rks[8 * cc + i];
-                split_bf16x8(x8, hi, lo);
-                *reinterpret_cast<uint4*>(sm + OFF_T4 + tc::sw_chunk(row, cc, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + OFF_T4 + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
-            }
-            const float gL = gams[L - 1];
-            float lo16[16], hi16[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                lo16[i] = sa[i] * gL;
-                hi16[i] = sb16[i] * gL;
-            }
-            tc::st16(trow + TM_S + 32 * qt, lo16);
-            tc::st16(trow + TM_S + 32 * qt + 16, hi16);
-        }
-        publish();
-
-        // ---- 11. (M Delta)^T = Delta^T M^T (three hi / lo products) and S += Delta~^T K
-        if (tid == 0) {
-            const uint32_t idm = tc::idesc_bf16(128, 64, 0, 0, 0);
-            const uint32_t ids = tc::idesc_bf16(128, 128, 0, 1, 0);
-#pragma unroll
-            for (int pr = 0; pr < 3; ++pr) {
-                const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo
-                const uint32_t pb = pr == 1 ? 8192u : 0u;   // M hi, lo, hi
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tm + TM_MD, dadd(dDL, pa + ks * 32), dadd(dM, pb + ks * 32), idm,
-                                 (pr | ks) != 0);
-            }
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tm + TM_S, dadd(dT4, part * 16384 + ks * 32), dadd(dKmn, ks * 2048), ids, 1u);
-            tc::commit(&mbar);
-        }
-        if (!mma_wait()) { timed_out = true; break; }
-        if (tid == 0 && c0 + C < Tn) issue_k(c0 + C);  // the K tile is free
-
-        // ---- 12. outputs o_t = gamma_t rq_t scale P_t + rq_t scale (M Delta)_t (lane v, 16 tokens);
-        //          the new state to bf16 for the next chunk
-        {
-            float p16[16], m16[16];
-            tc::ld16(trow + TM_P + 16 * qt, p16);
-            tc::ld16(trow + TM_MD + 16 * qt, m16);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 16 * qt + i;
-                if (t < L) {
-                    const float rq = rqs[t] * a.scale;
-                    const float o = fmaf(p16[i], gams[t] * rq, m16[i] * rq);
-                    a.out[static_cast<size_t>(tok0 + t) * vo_stride + h * D + row] =
-                        static_cast<uint16_t>(pack_bf16x2(o, 0.f) & 0xffffu);
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 f = src[c16 * 4 + j];
+                        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+                    }
+                    tc::st16(trow + TM_S + 32 * qt + c16 * 16, v);
+                    const int c8 = 4 * qt + 2 * c16;
+                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8, 128)) = pack_bf16x8(v);
+                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + 1, 128)) = pack_bf16x8(v + 8);
                 }
             }
-            if (c0 + C < Tn) {
-                float s32[32];
-                ld32(trow + TM_S + 32 * qt, s32);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, 4 * qt + c, 128)) =
-                        pack_bf16x8(s32 + 8 * c);
+            if (nch == 1 && short_last) {
+                if (!warp_wait(B_K0, 0) || !warp_wait(B_V, 0)) break;
+                zero_tail(0);
+                warp_arrive(R_Z);
             }
-        }
-        publish();
+            if (!warp_wait(B_WU, 0)) break;
+            convert_w();
+            warp_arrive(R_D);  // S0 and W of chunk 0 in place
+            bool ok = true;
+            for (long long c = 0; c < nch && ok; ++c) {
+                const bool more = c + 1 < nch;
+                const uint32_t par = c & 1;
+                if (c > 0) outputs(c - 1);
+                if (!warp_wait(B_A, par) || !warp_wait(B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1)) { ok = false; break; }
+                convert_delta(c);
+                warp_arrive(R_B);
+                if (!warp_wait(B_C, par)) { ok = false; break; }
+                if (more) {
+                    convert_s();
+                    const long long c1 = c + 1;
+                    if (c1 == nch - 1 && short_last) {
+                        if (!warp_wait(B_K0 + static_cast<int>(c1 & 1), (c1 >> 1) & 1) || !warp_wait(B_V, c1 & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        zero_tail(c1);
+                        warp_arrive(R_Z);
+                    }
+                    if (!warp_wait(B_WU, c1 & 1)) { ok = false; break; }
+                    convert_w();
+                    warp_arrive(R_D);
+                }
+            }
+            if (!ok) break;
+            outputs(nch - 1);
+        } while (false);
     }
 
-    if (timed_out) {
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (abort_flag) {
         if (tid == 0) atomicOr(a.status, 4);
-    } else {
+    } else if (!control) {
         // ---- scatter the final state back to its pool slot (row v, columns 32*qt ..)
         float4* dst = reinterpret_cast<float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
         float s32[32];

@@ -143,7 +143,11 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 
 /*
  * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_chunked needs for these
- * sizes (0 when it needs none).  Pure host function; returns 0 for invalid sizes.
+ * sizes: the first chunk of every sequence (8 bytes each, num_seqs + 1 of them, padded to 1 KB)
+ * and one 51,200-byte record per (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
+ * (what a chunk contributes independently of the carried state: Tw, Tu and M split into bf16
+ * high / low parts, and per-token scales).  Pure host function; returns 0 when num_seqs is 0 and
+ * for sizes gdn_prefill_chunked does not support.
  */
 size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
                                   int chunk_size);
@@ -169,8 +173,10 @@ size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K
  *   cache_indices  int64 [num_seqs]   distinct slots; duplicates give an undefined result
  *   cu_seqlens     int64 [num_seqs + 1]
  *   out            bf16 [T, Hv, V]    tokens of skipped sequences are not written
- *   workspace      device buffer of at least gdn_prefill_workspace_size(...) bytes (or NULL
- *                  when that size is 0); contents need not be initialised
+ *   workspace      device buffer of at least gdn_prefill_workspace_size(...) bytes, 256-byte
+ *                  aligned, overlapping neither out nor state_pool (NULL only when num_seqs is 0);
+ *                  contents need not be initialised and are scratch after the call; calls that
+ *                  share a workspace must not overlap on the GPU
  *   dev_status     device int32, zeroed by the caller; the kernels OR in GDN_STATUS_* bits for a
  *                  sequence they skip (slot out of range, malformed bounds)
  *   scale          query scale (K^-0.5 when the caller has no other value)

@@ -84,3 +84,31 @@ def test_window_validation(lib):
     h = ctypes.c_void_p(1 << 24)
     a = [P, h, h] + [P] * 9
     assert f(*a, 1, 2, 4, 3, 1, 1e-6, N) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_prefill_workspace_size(lib):
+    # chunk offsets (8 bytes per sequence + 1, padded to 1 KB) + one 51,200-byte record per
+    # (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 1024 + (240 + 4) * 32 * 51200
+    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 2048 + (2 + 200) * 2 * 51200
+    assert gdn.gdn_prefill_workspace_size(0, 100, 1, 1, 128, 128, 64) == 0
+    assert gdn.gdn_prefill_workspace_size(1, 100, 1, 1, 64, 128, 64) == 0    # unsupported K
+    assert gdn.gdn_prefill_workspace_size(1, 100, 2, 3, 128, 128, 64) == 0   # Hv % Hk != 0
+
+
+def test_prefill_validation(lib):
+    f = lib.gdn_prefill_chunked
+    pool, out = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 40)
+    need = gdn.gdn_prefill_workspace_size(2, 100, 1, 2, 128, 128, 64)
+
+    def call(ws, ws_bytes, chunk=64, num_seqs=2, K=128):
+        return f(P, P, P, P, P, P, P, pool, 4, P, P, num_seqs, 100, 1, 2, K, 128, chunk, 1.0, out,
+                 ws, ws_bytes, P, N)
+    ws = ctypes.c_void_p(1 << 44)
+    assert call(N, 0) == gdn.GDN_ERR_INVALID_ARG and "workspace" in gdn.last_error()
+    assert call(ws, need - 1) == gdn.GDN_ERR_INVALID_ARG and "needed" in gdn.last_error()
+    assert call(ctypes.c_void_p((1 << 44) + 16), need) == gdn.GDN_ERR_INVALID_ARG   # misaligned
+    assert call(ctypes.c_void_p((1 << 40) - 256), need) == gdn.GDN_ERR_INVALID_ARG  # overlaps out
+    assert call(ws, need, chunk=32) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(ws, need, K=64) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(N, 0, num_seqs=0) == gdn.GDN_OK
