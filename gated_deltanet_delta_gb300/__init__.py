@@ -24,7 +24,8 @@ STATUS_BAD_SEQLENS = 2
 
 # Every symbol that include/gdn.h declares.
 ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "gdn_prefill_workspace_size",
-               "gdn_prefill_chunked", "gdn_window_fused", "gdn_status_string", "gdn_last_error")
+               "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "gdn_window_fused",
+               "gdn_status_string", "gdn_last_error")
 
 
 class GdnError(RuntimeError):
@@ -64,6 +65,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_chunked.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I, I, I,
                                             F, P, P, SZ, P, P]
         lib.gdn_prefill_chunked.restype = I
+        lib.gdn_prefill_chunked_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I,
+                                                    I, I, F, P, P, P]
+        lib.gdn_prefill_chunked_noalloc.restype = I
         lib.gdn_window_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, U, F, P]
         lib.gdn_window_fused.restype = I
         lib.gdn_status_string.argtypes = [I]
@@ -283,6 +287,44 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices
                                       _ptr(cache_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
                                       int(chunk_size), scale, _ptr(out), _ptr(workspace), wsz,
                                       _ptr(dev_status), _stream(q.device)), "gdn_prefill_chunked")
+    return out
+
+
+def gdn_prefill_chunked_noalloc(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, cu_seqlens,
+                                chunk_size: int = 64, scale=None, out=None, dev_status=None):
+    """gdn_prefill_chunked for callers that cannot allocate device memory: the same arguments and
+    results without a workspace; the library's own fixed 64 MiB device scratch serves instead.
+    Workloads needing more than that raise GdnError (GDN_ERR_UNSUPPORTED).  Calls on one device
+    share the scratch, so calls that run concurrently on the GPU race: order them on one stream.
+    This wrapper allocates out and dev_status only when they are not given."""
+    torch = _torch()
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cache_indices.shape[0]
+    _want(q, "q", torch.bfloat16)
+    _want(k, "k", torch.bfloat16, (T, Hk, K))
+    _want(v, "v", torch.bfloat16, (T, Hv, V))
+    _want(a, "a", torch.bfloat16, (T, Hv))
+    _want(b, "b", torch.bfloat16, (T, Hv))
+    _want(A_log, "A_log", torch.float32, (Hv,))
+    _want(dt_bias, "dt_bias", torch.float32, (Hv,))
+    _want(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (Hv, V, K):
+        raise ValueError(f"state_pool must be [pool,{Hv},{V},{K}], got {tuple(state_pool.shape)}")
+    _want(cache_indices, "cache_indices", torch.int64, (N,))
+    _want(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,))
+    if out is None:
+        out = torch.empty((T, Hv, V), dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, (T, Hv, V))
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    _want(dev_status, "dev_status", torch.int32, (1,))
+    scale = K ** -0.5 if scale is None else float(scale)
+    _check(load().gdn_prefill_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                                              _ptr(dt_bias), _ptr(state_pool), state_pool.shape[0],
+                                              _ptr(cache_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
+                                              int(chunk_size), scale, _ptr(out), _ptr(dev_status),
+                                              _stream(q.device)), "gdn_prefill_chunked_noalloc")
     return out
 
 

@@ -1,8 +1,10 @@
 // api.cu -- the C ABI of libgdn (declared in include/gdn.h): host-side validation, choice of kernel
 // configuration, launch, and error reporting.  No device memory is allocated here.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "gdn.h"
 #include "launch.h"
@@ -404,4 +406,62 @@ extern "C" gdn_status gdn_window_fused(float* state, const float* hist, float* h
     a.eps = eps;
     gdn::launch_window(a, N, static_cast<cudaStream_t>(stream));
     return launched("gdn_window_fused");
+}
+
+// ------------------------------------------------------------------------------------------------
+// gdn_prefill_chunked_noalloc: the prefill for callers that cannot allocate device memory
+// themselves (a host framework whose allocator owns all device memory, or code running where a
+// cudaMalloc is not allowed).  Its workspace is a file-scope device array of fixed size, which
+// every GPU that loads this library holds until the process exits.  Host code sees only a
+// host-side stand-in for the array, so its device address is looked up once per device, with that
+// device current, and handed to the kernels.
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) uint8_t g_prefill_scratch[kNoallocScratchBytes];
+
+constexpr int kNoallocMaxDevices = 64;
+void* g_scratch_ptr[kNoallocMaxDevices];    // the array's device address on each device
+std::atomic<int> g_scratch_ready[kNoallocMaxDevices];
+std::mutex g_scratch_mutex;
+
+}  // namespace
+
+extern "C" gdn_status gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, const void* a,
+                                                  const void* b, const float* A_log, const float* dt_bias,
+                                                  float* state_pool, int pool_size,
+                                                  const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                                  int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                                  int chunk_size, float scale, void* out,
+                                                  int32_t* dev_status, gdn_stream_t stream) {
+    const size_t need = gdn_prefill_workspace_size(num_seqs, T, Hk, Hv, K, V, chunk_size);
+    REQUIRE(need <= kNoallocScratchBytes, GDN_ERR_UNSUPPORTED,
+            "gdn_prefill_chunked_noalloc: these sizes need %zu bytes of workspace; the library's static "
+            "scratch holds %zu (use gdn_prefill_chunked with a caller-owned workspace)",
+            need, kNoallocScratchBytes);
+    if (num_seqs == 0)  // nothing runs; the scratch is not needed
+        return gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, pool_size, cache_indices,
+                                   cu_seqlens, num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out, nullptr, 0,
+                                   dev_status, stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "gdn_prefill_chunked_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    REQUIRE(dev >= 0 && dev < kNoallocMaxDevices, GDN_ERR_UNSUPPORTED,
+            "gdn_prefill_chunked_noalloc: device %d beyond the %d supported", dev, kNoallocMaxDevices);
+    if (!g_scratch_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        if (!g_scratch_ready[dev].load(std::memory_order_relaxed)) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+            if (e != cudaSuccess || p == nullptr)
+                return fail(GDN_ERR_CUDA, "gdn_prefill_chunked_noalloc: cudaGetSymbolAddress of the scratch: %s",
+                            cudaGetErrorString(e));
+            g_scratch_ptr[dev] = p;
+            g_scratch_ready[dev].store(1, std::memory_order_release);
+        }
+    }
+    return gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, pool_size, cache_indices, cu_seqlens,
+                               num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out, g_scratch_ptr[dev],
+                               kNoallocScratchBytes, dev_status, stream);
 }

@@ -8,6 +8,7 @@
  *   gdn_decode_multi     T consecutive decode steps with the state held on chip
  *   comba_decode_step    one-token Comba step (state read with key p, written with key k)
  *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
+ *   gdn_prefill_chunked_noalloc  the same with the library's own fixed-size workspace
  *   gdn_window_fused     fused decode window: conv + SiLU, L2 norm, gates, recurrence over ntok
  *                        tokens, gated RMSNorm, with verify / commit / partial commit
  *
@@ -15,7 +16,8 @@
  *   - Every tensor argument is a DEVICE pointer to dense, contiguous, row-major memory in the layout
  *     given beside it.  "bf16" is IEEE bfloat16 (the upper half of a float32); "f32" is IEEE float.
  *   - The caller owns every buffer, including the prefill workspace.  The library allocates no
- *     device memory and keeps no global state besides a per-device table of kernel attributes.
+ *     device memory and keeps no global state besides a per-device table of kernel attributes and
+ *     the fixed 64 MiB device scratch array of gdn_prefill_chunked_noalloc.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
  *     Results are valid once the stream has been synchronised.
  *   - Arguments are validated on the host before anything is launched.  A rejected call returns
@@ -189,6 +191,34 @@ gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, cons
                                int K, int V, int chunk_size, float scale, void* out,
                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                gdn_stream_t stream);
+
+/*
+ * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot allocate device memory
+ * themselves, for instance code running under a host framework whose allocator owns all device
+ * memory, or in a place where calling cudaMalloc is not allowed.  The paper has no counterpart: this
+ * is a deployment variant, not a different computation.  Same arguments, layouts and results as
+ * gdn_prefill_chunked, without the workspace arguments.
+ *
+ * The workspace is a 64 MiB array of the library's own device memory (a static device variable,
+ * which every GPU that loads the library holds until the process exits).  The call allocates and
+ * frees nothing:
+ *   - Sizes whose gdn_prefill_workspace_size(...) exceeds 64 MiB are rejected with
+ *     GDN_ERR_UNSUPPORTED before anything runs (use gdn_prefill_chunked then).  About 1,300
+ *     (chunk, value head) records fit: for instance T = 4,096 tokens over a few sequences with
+ *     Hv = 16.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *     that device current) and keeps it; make that first call before any stream capture.
+ *   - Every call on a device shares the one array.  Nothing in it has to start at zero: each call
+ *     writes everything it reads.  Calls whose kernels overlap on the GPU (different streams, no
+ *     ordering between them) race on the array and give undefined results; order them on one stream.
+ */
+gdn_status gdn_prefill_chunked_noalloc(const void* q, const void* k, const void* v, const void* a,
+                                       const void* b, const float* A_log, const float* dt_bias,
+                                       float* state_pool, int pool_size,
+                                       const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                       int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                       int chunk_size, float scale, void* out, int32_t* dev_status,
+                                       gdn_stream_t stream);
 
 /*
  * gdn_window_fused -- fused decode window over ntok tokens for N independent sequences.
