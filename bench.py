@@ -502,6 +502,26 @@ class OracleDecodeSample:
 
 
 # ------------------------------------------------------------------------------------------------
+def main_single_op(args, torch, gdn, dist, seed):
+    """One operation alone, args.steps timed calls after args.warmup: a small, repeatable command to
+    run under a profiler."""
+    fns = {
+        "decode": lambda: bench_decode(torch, gdn, dist, args.steps, args.warmup, seed),
+        "comba": lambda: bench_comba(torch, gdn, dist, args.steps, args.warmup, seed),
+        "prefill": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed),
+        "window_verify": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, False),
+        "window_commit": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, True),
+        "decode_multi": lambda: bench_decode_multi(torch, gdn, dist, args.steps, args.warmup, seed),
+        "decode_pooled": lambda: bench_decode_pooled(torch, gdn, dist, args.steps, args.warmup, seed),
+    }
+    r = fns[args.op]()
+    if dist.rank == 0:
+        print(json.dumps({"op": args.op, "steps": args.steps, "warmup": args.warmup,
+                          "us_per_call": r["secs"] / args.steps * 1e6}))
+    dist.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,6 +530,10 @@ def main():
     ap.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline (rank 0, N=1)")
+    ap.add_argument("--op", choices=("decode", "comba", "prefill", "window_verify", "window_commit",
+                                     "decode_multi", "decode_pooled"),
+                    help="time only this operation on its workload and print its time per call "
+                         "(for profiling; not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -527,6 +551,9 @@ def main():
     torch.cuda.set_device(dist.local_rank)
     hbm_peak, tf_peak, peak_src = load_peaks()
     seed = dist.rank
+
+    if args.op:
+        return main_single_op(args, torch, gdn, dist, seed)
 
     sampler = ClockSampler(dist.local_rank)
     with sampler:

@@ -97,10 +97,11 @@ struct PrefillArgs {
 // A prefill chunk record: everything a chunk contributes that does not depend on the state, laid
 // out as the shared-memory image the sequential kernel uses (swizzled bf16 operand tiles):
 //   [0, 32768)      Tw hi, Tw lo, Tu hi, Tu lo (64 x 64 each, rows t, K-major)
-//   [32768, 49152)  M hi, M lo (64 x 64 each, rows t, K-major)
-//   [49152, 51200)  fp32 vectors: gamma_t rq_t scale [64], rq_t scale [64], D_L [64], rk [64], gamma_L
-constexpr long long kPfRecordBytes = 51200;
-constexpr long long kPfRecordVec = 49152;
+//   [32768, 49152)  Q~ = diag(gamma_t rq_t scale) Q (64 x 128, rows t, K-major)
+//   [49152, 65536)  M~ = diag(rq_t scale) M, hi and lo (64 x 64 each, rows t, K-major)
+//   [65536, 66560)  fp32 vectors: D_L [64], rk [64], gamma_L
+constexpr long long kPfRecordBytes = 66560;
+constexpr long long kPfRecordVec = 65536;
 
 // TMA descriptors of the prefill's q [T, Hk, 128], k [T, Hk, 128] and v [T, Hv, 128] (bf16): boxes of
 // 64 features x 1 head x 64 tokens with the 128-byte swizzle.

@@ -60,21 +60,22 @@ constexpr int NT = 512;   // threads per CTA: four per TMEM lane, each with a qu
 constexpr int LST = 68;   // row stride (floats) of the fp32 Lm and T matrices: rows are 16-byte aligned
 constexpr int ZST = 36;   // row stride (floats) of the 32 x 32 scratch of the inverse
 constexpr uint32_t kWaitLimit = 1u << 26;  // mbarrier polls before giving up (seconds of waiting)
+constexpr uint32_t kSleepWaitLimit = 1u << 22;  // the same for polls with a 1 us suspend hint
 
-// chunk record (bytes): Tw hi, Tw lo, Tu hi, Tu lo | M hi, M lo | vectors
-constexpr uint32_t REC_T4 = 0, REC_M = 32768, REC_VEC = 49152, REC_BYTES = 51200;
-constexpr uint32_t REC_PART1 = REC_M;                // Tw/Tu: used first, refetched first
-constexpr uint32_t REC_PART2 = REC_BYTES - REC_M;    // M and the vectors
+// chunk record (bytes): Tw hi, Tw lo, Tu hi, Tu lo | Q~ | M~ hi, M~ lo | vectors
+constexpr uint32_t REC_T4 = 0, REC_QT = 32768, REC_M = 49152, REC_VEC = 65536, REC_BYTES = 66560;
+constexpr uint32_t REC_VEC_BYTES = REC_BYTES - REC_VEC;
 // vector offsets (floats) inside the record's vector block
-constexpr int V_GQ = 0, V_RQ = 64, V_DL = 128, V_RK = 192, V_GL = 256;
+constexpr int V_DL = 0, V_RK = 64, V_GL = 128;
 
 // the chunk-preparation kernel's dynamic shared memory (bytes from a 1024-aligned base); the first
 // REC_BYTES are the record being built, stored by one bulk copy at the end
-constexpr uint32_t P_KQ = 0;         // [K;Q] tile (two 16 KB feature halves: 64 k rows + 64 q rows);
-                                     // once G is computed, Tw / Tu hi / lo (record bytes 0 .. 32 KB)
-constexpr uint32_t P_M = REC_M;      // M hi / lo (record bytes 32 .. 48 KB)
-constexpr uint32_t P_VEC = REC_VEC;  // record vectors
-constexpr uint32_t P_L = REC_BYTES;  // fp32 [64][LST] strictly lower Lm
+constexpr uint32_t P_KQ = 0;          // [K;Q] tile (two 16 KB feature halves: 64 k rows + 64 q rows);
+                                      // once G is computed, Tw / Tu hi / lo (record bytes 0 .. 32 KB)
+constexpr uint32_t P_QT = REC_QT;     // Q~
+constexpr uint32_t P_M = REC_M;       // M~ hi / lo
+constexpr uint32_t P_VEC = REC_VEC;   // record vectors
+constexpr uint32_t P_L = REC_BYTES;   // fp32 [64][LST] strictly lower Lm
 constexpr uint32_t P_T = P_L + 64 * LST * 4;  // fp32 [64][LST] T = (I + Lm)^-1
 constexpr uint32_t P_X = P_T + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
 constexpr uint32_t P_USED = P_X + 32 * ZST * 4;
@@ -82,21 +83,22 @@ constexpr uint32_t P_SMEM = P_USED + 1024;
 constexpr uint32_t P_TM_G = 0, P_TM_COLS = 64;
 
 // the sequential kernel's dynamic shared memory
-constexpr uint32_t OFF_K = 0;         // two K tiles (chunks of even / odd index), 16 KB each: two
-                                      // 64-feature halves of 8 KB, 64 token rows each
-constexpr uint32_t OFF_Q = 32768;     // Q tile (two halves of 8 KB)
-constexpr uint32_t OFF_V = 49152;     // V tile (two halves of 8 KB)
-constexpr uint32_t OFF_S = 65536;     // S0 bf16, K-major, 128 v rows, two halves of 16 KB
-constexpr uint32_t OFF_T4 = 98304;    // record part: Tw hi, Tw lo, Tu hi, Tu lo
-constexpr uint32_t OFF_M = OFF_T4 + REC_M;      // record part: M hi, M lo
-constexpr uint32_t OFF_VEC = OFF_T4 + REC_VEC;  // record part: the vectors, two buffers of 2 KB
-constexpr uint32_t OFF_DL = OFF_VEC + 2 * (REC_BYTES - REC_VEC);  // Delta^T hi, lo (16 KB each)
-constexpr uint32_t OFF_DT = OFF_DL + 32768;     // Delta~^T hi, lo (16 KB each); before them, W as
-                                                // the MN-major B operand (128 feature rows x 64 t)
+constexpr uint32_t OFF_K = 0;          // two K tiles (chunks of even / odd index), 16 KB each: two
+                                       // 64-feature halves of 8 KB, 64 token rows each
+constexpr uint32_t OFF_V = 32768;      // V tile (two halves of 8 KB)
+constexpr uint32_t OFF_S = 49152;      // S0 bf16, K-major, 128 v rows, two halves of 16 KB
+constexpr uint32_t OFF_T4 = 81920;     // record part: Tw hi, Tw lo, Tu hi, Tu lo
+constexpr uint32_t OFF_QT = 114688;    // record part: Q~
+constexpr uint32_t OFF_M = 131072;     // record part: M~ hi, M~ lo
+constexpr uint32_t OFF_VEC = 147456;   // record part: the vectors, two buffers of 1 KB
+constexpr uint32_t OFF_DL = OFF_VEC + 2 * REC_VEC_BYTES;  // Delta^T hi, lo (16 KB each)
+constexpr uint32_t OFF_DT = OFF_DL + 32768;      // Delta~^T hi, lo (16 KB each); before them, W as
+                                                 // the MN-major B operand (128 feature rows x 64 t)
 constexpr uint32_t SMEM_USED = OFF_DT + 32768;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-// TMEM columns (fp32, 128 lanes); P and (M Delta) alternate between two buffers by chunk parity
-constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_P = 256, TM_MD = 384;
+// TMEM columns (fp32, 128 lanes): the state, W, U and the outputs O = P~ + M~ Delta, the last two
+// in a buffer per chunk parity
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 320;
 constexpr uint32_t TM_COLS = 512;
 // the sequential kernel's threads: 16 worker warps (conversions, outputs) and one control warp
 // (lane 0 issues every MMA and every copy)
@@ -104,18 +106,21 @@ constexpr int NW = 16, NTS = 32 * (NW + 1);
 // its mbarriers: MMA completions (tcgen05.commit), worker hand-offs (one arrival per worker warp)
 // and copies
 enum : int {
-    B_A = 0,   // P and Delta of a chunk computed
-    B_C,       // (M Delta) and the state update computed
+    B_A = 0,   // P~ and Delta of a chunk computed
+    B_C,       // M~ Delta and the state update computed
     B_WU,      // W and U of a chunk computed
     R_B,       // workers: Delta converted, state scaled
     R_D,       // workers: S0 and W of the next chunk in place
     R_Z,       // workers: the tail of a short chunk zeroed
-    B_K0, B_K1, B_Q, B_V, B_R1, B_RM, B_RV0, B_RV1,
+    B_K0, B_K1, B_V, B_R1, B_QT, B_RM, B_RV0, B_RV1,
     NBAR
 };
 
 static_assert(REC_BYTES == kPfRecordBytes && REC_VEC == kPfRecordVec, "chunk record layout");
-static_assert(OFF_DL % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_M % 1024 == 0, "operand tiles 1024-aligned");
+static_assert(OFF_DL % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_M % 1024 == 0 && OFF_QT % 1024 == 0 &&
+                  OFF_T4 % 1024 == 0, "operand tiles 1024-aligned");
+static_assert(OFF_T4 + REC_QT == OFF_QT && OFF_T4 + REC_M == OFF_M && OFF_T4 + REC_VEC == OFF_VEC,
+              "record parts land at their tiles");
 static_assert(2 * (P_SMEM + 1024) <= 228 * 1024, "two preparation CTAs per SM");
 static_assert(SMEM_BYTES <= 227 * 1024, "sequential kernel shared memory");
 }  // namespace pf
@@ -354,9 +359,6 @@ __global__ void __launch_bounds__(pf::NT, 2)
         if (tid < C) {
             const int t = tid;
             gams[t] = __expf(Gf[t]);
-            const float rq = rqs[t] * a.scale;
-            vec[V_GQ + t] = gams[t] * rq;
-            vec[V_RQ + t] = rq;
             vec[V_DL + t] = t < L ? __expf(Gf[L - 1] - Gf[t]) : 0.f;
             vec[V_RK + t] = rks[t];
         }
@@ -371,7 +373,18 @@ __global__ void __launch_bounds__(pf::NT, 2)
         }
         if (tid == 0) vec[V_GL] = gams[L - 1];
 
-        // ---- 4. Lm (lanes t < 64, fp32) and M (lanes 64 + t, bf16 hi / lo) from G, 16 columns each
+        // ---- 4. Q~ = diag(gamma_t rq_t scale) Q (bf16, rows t, K-major) from the q rows; Lm (lanes
+        //         t < 64, fp32) and M~ = diag(rq_t scale) M (lanes 64 + t, bf16 hi / lo) from G, 16
+        //         columns each
+        for (int e = tid; e < C * 16; e += NT) {
+            const int t = e >> 4, cc = e & 15;
+            const uint4 q8 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + t, cc, 128));
+            const float f = gams[t] * (rqs[t] * a.scale);
+            const float4 x0 = bf16x4_to_f32x4(make_uint2(q8.x, q8.y));
+            const float4 x1 = bf16x4_to_f32x4(make_uint2(q8.z, q8.w));
+            const float y[8] = {x0.x * f, x0.y * f, x0.z * f, x0.w * f, x1.x * f, x1.y * f, x1.z * f, x1.w * f};
+            *reinterpret_cast<uint4*>(sm + P_QT + tc::sw_chunk(t, cc, 64)) = pack_bf16x8(y);
+        }
         {
             float g[16];
             tc::ld16(trow + P_TM_G + 16 * qt, g);
@@ -394,13 +407,14 @@ __global__ void __launch_bounds__(pf::NT, 2)
             } else {
                 const int t = row - C;
                 const float Gt = Gf[t];
+                const float rt = rqs[t] * a.scale;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     float m8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int s = s0 + c * 8 + i;
-                        m8[i] = s <= t ? rks[s] * g[c * 8 + i] * __expf(Gt - Gf[s]) : 0.f;
+                        m8[i] = s <= t ? rt * (rks[s] * g[c * 8 + i] * __expf(Gt - Gf[s])) : 0.f;
                     }
                     uint4 mh, ml;
                     split_bf16x8(m8, mh, ml);
@@ -555,12 +569,14 @@ __global__ void __launch_bounds__(pf::NT, 2)
 
 // ------------------------------------------------------------------------------------------------
 // The chunk recurrence of one (sequence, value head), from its chunk records, warp-specialized.
-// Per chunk c the state path is: P = S0 Q^T and Delta = U - S0 W^T (tensor core) -> Delta to bf16
-// hi / lo and the state scaled by gamma_L (workers) -> M Delta and S += Delta~^T K (tensor core) ->
-// S to bf16 (workers).  W and U of chunk c + 1 are multiplied right behind the state update, and W
-// is converted with S; chunk c's outputs are written while chunk c + 1's P and Delta are computed
-// (P and (M Delta) alternate between two TMEM buffers).  The control lane issues the MMAs as soon
-// as the workers' hand-off arrives and each copy as soon as its buffer's last reader is done.
+// Per chunk c the state path is: P~ = S0 Q~^T and Delta = U - S0 W^T (tensor core) -> Delta to
+// bf16 hi / lo and the state scaled by gamma_L (workers) -> O = P~ + M~ Delta and S += Delta~^T K
+// (tensor core) -> S and the next chunk's W to bf16 (workers).  W and U of chunk c + 1 are
+// multiplied while the workers convert Delta (U alternates between two TMEM buffers), and chunk
+// c's outputs are converted and stored while chunk c + 1's O and state update are computed (O
+// alternates too).  The output scales are folded into Q~ and M~ by the preparation kernel, so an
+// output is one TMEM read and one store.  The control lane issues the MMAs as soon as the
+// workers' hand-off arrives and each copy as soon as its buffer's last reader is done.
 __global__ void __launch_bounds__(pf::NTS, 1)
     gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
@@ -609,18 +625,18 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     const uint32_t tm = tmem_slot;
     const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
 
-    // A bounded wait on phase `parity` of barrier i; on a timeout it raises the abort flag, and it
-    // gives up once someone else has.
+    // control: a bounded wait on phase `parity` of barrier i; on a timeout it raises the abort flag,
+    // and it gives up once someone else has
     auto wait_bar = [&](int i, uint32_t parity) -> bool {
         if (tc::mbar_wait_or_abort(&bars[i], parity, kWaitLimit, &abort_flag)) return true;
         abort_flag = 1;
         return false;
     };
-    // workers: lane 0 of each warp waits, the warp follows
+    // workers: the whole warp waits, converged, parked between polls
     auto warp_wait = [&](int i, uint32_t parity) -> bool {
-        bool ok = true;
-        if (lane == 0) ok = wait_bar(i, parity);
-        ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+        bool ok = tc::mbar_sleep_wait(&bars[i], parity, kSleepWaitLimit, 1000u, &abort_flag);
+        ok = __all_sync(kFullMask, ok ? 1 : 0) != 0;
+        if (!ok && lane == 0) abort_flag = 1;
         tc::fence_after();
         return ok;
     };
@@ -633,7 +649,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         if (lane == 0) tc::mbar_arrive(&bars[i]);
     };
     // operand descriptors at their tile bases (K-major: LBO unused; MN-major: LBO = half stride)
-    const uint64_t dQ = tc::sdesc(sb + OFF_Q, 16, 1024);           // q rows, K-major
+    const uint64_t dQT = tc::sdesc(sb + OFF_QT, 16, 1024);         // Q~ rows, K-major
     const uint64_t dK0 = tc::sdesc(sb + OFF_K, 8192, 1024);        // k rows read MN-major (even chunks)
     const uint64_t dVmn = tc::sdesc(sb + OFF_V, 8192, 1024);       // v rows read MN-major
     const uint64_t dS0 = tc::sdesc(sb + OFF_S, 16, 1024);          // S0, K-major
@@ -641,7 +657,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     const uint64_t dT4 = tc::sdesc(sb + OFF_T4, 16, 1024);         // Tw/Tu hi/lo
     const uint64_t dDL = tc::sdesc(sb + OFF_DL, 16, 1024);         // Delta hi/lo
     const uint64_t dDT = tc::sdesc(sb + OFF_DT, 16, 1024);         // Delta~ hi/lo
-    const uint64_t dM = tc::sdesc(sb + OFF_M, 16, 1024);           // M hi/lo
+    const uint64_t dM = tc::sdesc(sb + OFF_M, 16, 1024);           // M~ hi/lo
     const size_t vo_stride = static_cast<size_t>(a.Hv) * D;       // elements between tokens of v, out
     float* Sg = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * D * D;
 
@@ -666,7 +682,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         for (int c = 0; c < 2; ++c)
             *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, 2 * qt + c, 128)) = pack_bf16x8(w16 + 8 * c);
     };
-    // S (TMEM) -> S0 (bf16, K-major) for the next chunk's P and Delta
+    // S (TMEM) -> S0 (bf16, K-major) for the next chunk's P~ and Delta
     auto convert_s = [&]() {
         float s32[32];
         ld32(trow + TM_S + 32 * qt, s32);
@@ -674,31 +690,24 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         for (int q4 = 0; q4 < 4; ++q4)
             *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, 4 * qt + q4, 128)) = pack_bf16x8(s32 + 8 * q4);
     };
-    // outputs o_t = gamma_t rq_t scale P_t + rq_t scale (M Delta)_t of chunk c, tokens 16*qt ..
-    // (lane v)
+    // outputs of chunk c from O (TMEM), tokens 16*qt .. (lane v)
     auto outputs = [&](long long c) {
         const int L = chunk_len(c);
-        float p16[16], m16[16];
-        tc::ld16(trow + TM_P + (c & 1) * 64 + 16 * qt, p16);
-        tc::ld16(trow + TM_MD + (c & 1) * 64 + 16 * qt, m16);
+        float o16[16];
+        tc::ld16(trow + TM_O + (c & 1) * 64 + 16 * qt, o16);
         tc::wait_ld();
-        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC));
-        uint16_t* o = a.out + static_cast<size_t>(bos + c * C) * vo_stride + h * D + row;
+        uint16_t* o = a.out + static_cast<size_t>(bos + c * C + 16 * qt) * vo_stride + h * D + row;
+        const int n_here = L - 16 * qt;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int t = 16 * qt + i;
-            if (t < L) {
-                const float v = fmaf(p16[i], vec[V_GQ + t], m16[i] * vec[V_RQ + t]);
-                o[static_cast<size_t>(t) * vo_stride] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
-            }
-        }
+        for (int i = 0; i < 16; ++i)
+            if (i < n_here) o[i * vo_stride] = static_cast<uint16_t>(pack_bf16x2(o16[i], 0.f) & 0xffffu);
     };
     // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
     // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates
     auto convert_delta = [&](long long c) {
-        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC));
+        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * REC_VEC_BYTES);
         float d16[16], sa[16], sb16[16];
-        tc::ld16(trow + TM_U + 16 * qt, d16);
+        tc::ld16(trow + TM_U + (c & 1) * 64 + 16 * qt, d16);
         tc::ld16(trow + TM_S + 32 * qt, sa);
         tc::ld16(trow + TM_S + 32 * qt + 16, sb16);
         tc::wait_ld();
@@ -709,9 +718,15 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             split_bf16x8(d16 + 8 * cc2, hi, lo);
             *reinterpret_cast<uint4*>(sm + OFF_DL + tc::sw_chunk(row, cc, 128)) = hi;
             *reinterpret_cast<uint4*>(sm + OFF_DL + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
+            const float4 dl0 = *reinterpret_cast<const float4*>(vec + V_DL + 8 * cc);
+            const float4 dl1 = *reinterpret_cast<const float4*>(vec + V_DL + 8 * cc + 4);
+            const float4 rk0 = *reinterpret_cast<const float4*>(vec + V_RK + 8 * cc);
+            const float4 rk1 = *reinterpret_cast<const float4*>(vec + V_RK + 8 * cc + 4);
+            const float dl[8] = {dl0.x, dl0.y, dl0.z, dl0.w, dl1.x, dl1.y, dl1.z, dl1.w};
+            const float rk[8] = {rk0.x, rk0.y, rk0.z, rk0.w, rk1.x, rk1.y, rk1.z, rk1.w};
             float x8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x8[i] = d16[8 * cc2 + i] * vec[V_DL + 8 * cc + i] * vec[V_RK + 8 * cc + i];
+            for (int i = 0; i < 8; ++i) x8[i] = d16[8 * cc2 + i] * dl[i] * rk[i];
             split_bf16x8(x8, hi, lo);
             *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, cc, 128)) = hi;
             *reinterpret_cast<uint4*>(sm + OFF_DT + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
@@ -736,7 +751,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 inflight |= 1u << i;
                 lastpar = (lastpar & ~(1u << i)) | (parity << i);
             };
-            // q, k, v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
+            // k or v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
             auto fetch_rows = [&](const CUtensorMap* map, int head, long long c, uint32_t dst, int bar,
                                   uint32_t parity) {
                 const int z = static_cast<int>(bos + c * C);
@@ -755,17 +770,18 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             auto fetch_k = [&](long long c) {
                 fetch_rows(&maps.k, hk, c, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
             };
-            auto fetch_q = [&](long long c) { fetch_rows(&maps.q, hk, c, OFF_Q, B_Q, c & 1); };
             auto fetch_v = [&](long long c) { fetch_rows(&maps.v, h, c, OFF_V, B_V, c & 1); };
-            auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_M - REC_T4, OFF_T4, B_R1, c & 1); };
+            auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_QT - REC_T4, OFF_T4, B_R1, c & 1); };
+            auto fetch_qt = [&](long long c) { fetch_rec(c, REC_QT, REC_M - REC_QT, OFF_QT, B_QT, c & 1); };
             auto fetch_rm = [&](long long c) { fetch_rec(c, REC_M, REC_VEC - REC_M, OFF_M, B_RM, c & 1); };
             auto fetch_rv = [&](long long c) {
-                fetch_rec(c, REC_VEC, REC_BYTES - REC_VEC, OFF_VEC + (c & 1) * (REC_BYTES - REC_VEC),
-                          B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1);
+                fetch_rec(c, REC_VEC, REC_VEC_BYTES, OFF_VEC + (c & 1) * REC_VEC_BYTES, B_RV0 + static_cast<int>(c & 1),
+                          (c >> 1) & 1);
             };
             // W^T = K^T Tw^T and U^T = V^T Tu^T of chunk c (A MN-major from the token tiles)
             auto issue_wu = [&](long long c) {
                 const uint64_t dK = dadd(dK0, (c & 1) * 16384);
+                const uint32_t tu = tm + TM_U + (c & 1) * 64;
                 const uint32_t idw = tc::idesc_bf16(128, 64, 1, 0, 0);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -773,23 +789,28 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     for (int ks = 0; ks < 4; ++ks) {
                         tc::mma_bf16(tm + TM_W, dadd(dK, ks * 2048), dadd(dT4, part * 8192 + ks * 32), idw,
                                      (part | ks) != 0);
-                        tc::mma_bf16(tm + TM_U, dadd(dVmn, ks * 2048), dadd(dT4, 16384 + part * 8192 + ks * 32),
-                                     idw, (part | ks) != 0);
+                        tc::mma_bf16(tu, dadd(dVmn, ks * 2048), dadd(dT4, 16384 + part * 8192 + ks * 32), idw,
+                                     (part | ks) != 0);
                     }
                 tc::commit(&bars[B_WU]);
                 mark(B_WU, c & 1);
             };
-            // the tile of chunk c is ready for W and U (a short chunk: after the workers zeroed its tail)
+            // the tiles of chunk c are in place for W and U (a short chunk: after the workers zeroed
+            // its tail)
             auto wu_inputs = [&](long long c) -> bool {
                 if (c == nch - 1 && short_last) return wait_bar(R_Z, 0) && wait_bar(B_R1, c & 1);
                 return wait_bar(B_K0 + static_cast<int>(c & 1), (c >> 1) & 1) && wait_bar(B_V, c & 1) &&
                        wait_bar(B_R1, c & 1);
             };
+            auto wu_ready_now = [&](long long c) -> bool {
+                return !(c == nch - 1 && short_last) && tc::mbar_test(&bars[B_K0 + static_cast<int>(c & 1)], (c >> 1) & 1) &&
+                       tc::mbar_test(&bars[B_V], c & 1) && tc::mbar_test(&bars[B_R1], c & 1);
+            };
 
             fetch_k(0);
-            fetch_q(0);
             fetch_v(0);
             fetch_r1(0);
+            fetch_qt(0);
             fetch_rm(0);
             fetch_rv(0);
             if (nch > 1) fetch_k(1);
@@ -798,7 +819,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 tc::fence_after();
                 issue_wu(0);
                 if (!wait_bar(B_WU, 0)) break;
-                if (nch > 1) {
+                if (nch > 1) {  // U read the v tile, W and U the record part
                     fetch_v(1);
                     fetch_r1(1);
                 }
@@ -806,27 +827,33 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     const bool more = c + 1 < nch;
                     const uint32_t par = c & 1;
                     const uint64_t dK = dadd(dK0, (c & 1) * 16384);
-                    // ---- A. P^T = S0 Q^T and Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated)
-                    if (!wait_bar(R_D, par) || !wait_bar(B_Q, par)) break;
+                    // ---- A. P~^T = S0 Q~^T and Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated)
+                    if (!wait_bar(R_D, par) || !wait_bar(B_QT, par)) break;
                     tc::fence_after();
                     {
                         const uint32_t id = tc::idesc_bf16(128, 64, 0, 0, 0);
                         const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_bf16(tm + TM_P + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
-                                         dadd(dQ, (ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
+                            tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                         dadd(dQT, (ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_bf16(tm + TM_U, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                            tc::mma_bf16(tm + TM_U + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
                                          dadd(dWmn, ks * 2048), idd, 1u);
                         tc::commit(&bars[B_A]);
                         mark(B_A, par);
                     }
                     if (!wait_bar(B_A, par)) break;
-                    if (more) fetch_q(c + 1);  // P read the q tile
-                    // ---- C. (M Delta)^T = Delta^T M^T (three hi / lo products) and S += Delta~^T K,
-                    //         then W and U of the next chunk
+                    if (more) fetch_qt(c + 1);  // P~ read Q~
+                    // W and U of the next chunk while the workers convert Delta, if its tiles are in
+                    bool wu_done = !more;
+                    if (more && wu_ready_now(c + 1)) {
+                        tc::fence_after();
+                        issue_wu(c + 1);
+                        wu_done = true;
+                    }
+                    // ---- C. O^T = P~^T + Delta^T M~^T (three hi / lo products) and S += Delta~^T K
                     if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
                     tc::fence_after();
                     {
@@ -835,11 +862,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
 #pragma unroll
                         for (int pr = 0; pr < 3; ++pr) {
                             const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo
-                            const uint32_t pb = pr == 1 ? 8192u : 0u;   // M hi, lo, hi
+                            const uint32_t pb = pr == 1 ? 8192u : 0u;   // M~ hi, lo, hi
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
-                                tc::mma_bf16(tm + TM_MD + (c & 1) * 64, dadd(dDL, pa + ks * 32),
-                                             dadd(dM, pb + ks * 32), idm, (pr | ks) != 0);
+                                tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dDL, pa + ks * 32), dadd(dM, pb + ks * 32),
+                                             idm, 1u);
                         }
 #pragma unroll
                         for (int part = 0; part < 2; ++part)
@@ -849,21 +876,23 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         tc::commit(&bars[B_C]);
                         mark(B_C, par);
                     }
-                    if (more) {
+                    if (!wu_done) {  // the tiles came late, or the next chunk is the short last one
                         if (!wu_inputs(c + 1)) break;
                         tc::fence_after();
                         issue_wu(c + 1);
-                        fetch_rv(c + 1);  // its buffer's last reader, chunk c - 1's outputs, is done (R_B)
                     }
-                    if (!wait_bar(B_C, par)) break;
                     if (more) {
-                        fetch_rm(c + 1);                   // (M Delta) read M
-                        if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
+                        fetch_rv(c + 1);  // its buffer's last reader, chunk c - 1's Delta conversion, is done
                         if (!wait_bar(B_WU, (c + 1) & 1)) break;
-                        if (c + 2 < nch) {                 // U read the v tile, W and U the record part
+                        if (c + 2 < nch) {  // U read the v tile, W and U the record part
                             fetch_v(c + 2);
                             fetch_r1(c + 2);
                         }
+                    }
+                    if (!wait_bar(B_C, par)) break;
+                    if (more) {
+                        fetch_rm(c + 1);                   // M~ Delta read M~
+                        if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
                     }
                 }
             } while (false);
@@ -905,10 +934,10 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             for (long long c = 0; c < nch && ok; ++c) {
                 const bool more = c + 1 < nch;
                 const uint32_t par = c & 1;
-                if (c > 0) outputs(c - 1);
                 if (!warp_wait(B_A, par) || !warp_wait(B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1)) { ok = false; break; }
                 convert_delta(c);
                 warp_arrive(R_B);
+                if (c > 0) outputs(c - 1);  // while O and the update of chunk c are computed
                 if (!warp_wait(B_C, par)) { ok = false; break; }
                 if (more) {
                     convert_s();

@@ -93,6 +93,37 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* mbar, uint32_t pari
     return false;
 }
 
+// Poll with a suspend-time hint: each try_wait may park the thread for up to `hint_ns` until the
+// phase completes, so waiting warps leave the issue slots to the working ones.  At most `limit`
+// polls (with a 1 us hint, 2^22 polls bound the wait to a few seconds); gives up early once *abort
+// is nonzero.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t* mbar, uint32_t parity, uint32_t limit, uint32_t hint_ns,
+                                                const volatile int* abort) {
+    const uint32_t a = smem_u32(mbar);
+    for (uint32_t i = 0; i < limit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p;}"
+            : "=r"(done)
+            : "r"(a), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (done) return true;
+        if ((i & 15u) == 15u && *abort) return false;
+    }
+    return false;
+}
+
+// Non-blocking: has the phase with parity `parity` completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+        : "=r"(done)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // One arrival on the mbarrier (release semantics at CTA scope).
 __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");

@@ -146,9 +146,9 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 /*
  * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_chunked needs for these
  * sizes: the first chunk of every sequence (8 bytes each, num_seqs + 1 of them, padded to 1 KB)
- * and one 51,200-byte record per (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
- * (what a chunk contributes independently of the carried state: Tw, Tu and M split into bf16
- * high / low parts, and per-token scales).  Pure host function; returns 0 when num_seqs is 0 and
+ * and one 66,560-byte record per (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
+ * (what a chunk contributes independently of the carried state: Tw, Tu and the output-scaled M
+ * split into bf16 high / low parts, the output-scaled q rows, and per-token scales).  Pure host function; returns 0 when num_seqs is 0 and
  * for sizes gdn_prefill_chunked does not support.
  */
 size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
@@ -203,8 +203,8 @@ gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, cons
  * which every GPU that loads the library holds until the process exits).  The call allocates and
  * frees nothing:
  *   - Sizes whose gdn_prefill_workspace_size(...) exceeds 64 MiB are rejected with
- *     GDN_ERR_UNSUPPORTED before anything runs (use gdn_prefill_chunked then).  About 1,300
- *     (chunk, value head) records fit: for instance T = 4,096 tokens over a few sequences with
+ *     GDN_ERR_UNSUPPORTED before anything runs (use gdn_prefill_chunked then).  About 1,000
+ *     (chunk, value head) records fit: for instance T = 3,000 tokens over a few sequences with
  *     Hv = 16.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *     that device current) and keeps it; make that first call before any stream capture.

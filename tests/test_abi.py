@@ -87,10 +87,10 @@ def test_window_validation(lib):
 
 
 def test_prefill_workspace_size(lib):
-    # chunk offsets (8 bytes per sequence + 1, padded to 1 KB) + one 51,200-byte record per
+    # chunk offsets (8 bytes per sequence + 1, padded to 1 KB) + one 66,560-byte record per
     # (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
-    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 1024 + (240 + 4) * 32 * 51200
-    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 2048 + (2 + 200) * 2 * 51200
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 1024 + (240 + 4) * 32 * 66560
+    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 2048 + (2 + 200) * 2 * 66560
     assert gdn.gdn_prefill_workspace_size(0, 100, 1, 1, 128, 128, 64) == 0
     assert gdn.gdn_prefill_workspace_size(1, 100, 1, 1, 64, 128, 64) == 0    # unsupported K
     assert gdn.gdn_prefill_workspace_size(1, 100, 2, 3, 128, 128, 64) == 0   # Hv % Hk != 0
