@@ -87,6 +87,7 @@ struct PrefillArgs {
     uint16_t* out;
     int32_t* status;
     long long* chunk_off;  // workspace: first chunk of every sequence, [num_seqs + 1]
+    longlong2* chunk_tab;  // workspace: per chunk (first token, sequence << 32 | length), [cap]
     uint8_t* records;      // workspace: one record per (chunk, value head), kPfRecordBytes each
     long long T;
     long long cap;         // chunk capacity of the workspace

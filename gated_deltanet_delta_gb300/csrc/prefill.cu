@@ -48,8 +48,8 @@ long long prefill_chunk_cap(long long T, int num_seqs) { return (T + pf::C - 1) 
 
 size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) {
     if (num_seqs <= 0) return 0;
-    return prefill_header_bytes(num_seqs) +
-           static_cast<size_t>(prefill_chunk_cap(T, num_seqs)) * Hv * static_cast<size_t>(kPfRecordBytes);
+    const long long cap = prefill_chunk_cap(T, num_seqs);
+    return prefill_header_bytes(num_seqs, cap) + static_cast<size_t>(cap) * Hv * static_cast<size_t>(kPfRecordBytes);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_t stream) {
@@ -68,9 +68,10 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
     }
     PrefillArgs a = args;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    a.chunk_off = reinterpret_cast<long long*>(ws);
-    a.records = ws + prefill_header_bytes(a.num_seqs);
     a.cap = prefill_chunk_cap(a.T, a.num_seqs);
+    a.chunk_off = reinterpret_cast<long long*>(ws);
+    a.chunk_tab = reinterpret_cast<longlong2*>(ws + prefill_tab_offset(a.num_seqs));
+    a.records = ws + prefill_header_bytes(a.num_seqs, a.cap);
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (a.T > 0) {  // with T = 0 every sequence is empty and no kernel reads the maps
@@ -78,9 +79,14 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
             !encode_rows(&maps.v, a.v, a.T, a.Hv))
             return cudaErrorInvalidValue;
     }
-    gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.chunk_off);
-    if (a.T > 0) {
-        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hv);
+    gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.cap, a.chunk_off,
+                                                                a.chunk_tab);
+    if (a.T > 0) {  // persistent: two CTAs per SM, each over every (grid)-th (chunk, head) unit
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const long long units = a.cap * a.Hv;
+        const unsigned pgrid = static_cast<unsigned>(units < 2LL * sms ? units : 2LL * sms);
         gdn_prefill_prep_kernel<<<pgrid, pf::NT, pf::P_SMEM, stream>>>(a, maps);
     }
     const unsigned grid = static_cast<unsigned>(a.num_seqs) * static_cast<unsigned>(a.Hv);

@@ -168,11 +168,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// The first chunk of every sequence: chunk_off[n] = sum over n' < n of ceil(len_n' / 64), with 0
-// chunks for a sequence whose bounds are invalid (flagged by the sequential kernel).  One CTA.
+// The first chunk of every sequence, chunk_off[n] = sum over n' < n of ceil(len_n' / 64) (0 chunks
+// for a sequence whose bounds are invalid: the sequential kernel flags it), and the chunk table:
+// for chunk f of sequence n, (first token, n << 32 | length), for f < cap.  One CTA.
 constexpr int kPfOffThreads = 1024;
 __global__ void __launch_bounds__(kPfOffThreads)
-    gdn_prefill_offsets_kernel(const int64_t* cu_seqlens, int num_seqs, long long T, long long* chunk_off) {
+    gdn_prefill_offsets_kernel(const int64_t* cu_seqlens, int num_seqs, long long T, long long cap,
+                               long long* chunk_off, longlong2* chunk_tab) {
     __shared__ long long warp_tot[kPfOffThreads / 32];
     __shared__ long long carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -180,10 +182,14 @@ __global__ void __launch_bounds__(kPfOffThreads)
     __syncthreads();
     for (int base = 0; base < num_seqs; base += kPfOffThreads) {
         const int i = base + tid;
-        long long cnt = 0;
+        long long cnt = 0, bos = 0, len = 0;
         if (i < num_seqs) {
-            const long long bos = cu_seqlens[i], eos = cu_seqlens[i + 1];
-            if (bos >= 0 && eos >= bos && eos <= T) cnt = (eos - bos + pf::C - 1) / pf::C;
+            bos = cu_seqlens[i];
+            const long long eos = cu_seqlens[i + 1];
+            if (bos >= 0 && eos >= bos && eos <= T) {
+                len = eos - bos;
+                cnt = (len + pf::C - 1) / pf::C;
+            }
         }
         long long x = cnt;  // inclusive scan inside the warp
 #pragma unroll
@@ -204,7 +210,13 @@ __global__ void __launch_bounds__(kPfOffThreads)
         }
         __syncthreads();
         const long long before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - cnt;
-        if (i < num_seqs) chunk_off[i] = before;
+        if (i < num_seqs) {
+            chunk_off[i] = before;
+            for (long long j = 0; j < cnt && before + j < cap; ++j) {
+                const long long L = len - j * pf::C < pf::C ? len - j * pf::C : pf::C;
+                chunk_tab[before + j] = make_longlong2(bos + j * pf::C, (static_cast<long long>(i) << 32) | L);
+            }
+        }
         __syncthreads();
         if (tid == 0) carry += warp_tot[kPfOffThreads / 32 - 1];
         __syncthreads();
@@ -213,34 +225,26 @@ __global__ void __launch_bounds__(kPfOffThreads)
 }
 
 // ------------------------------------------------------------------------------------------------
-// The state-independent part of one chunk f (flat index) of one value head h -> its chunk record.
+// The state-independent part of every (chunk, value head) unit -> its chunk record.  Persistent:
+// CTA b takes units b, b + grid, ...; unit u is chunk f = u / Hv (the table gives its first token,
+// sequence and length) of value head h = u % Hv.  The next unit's k and q rows are fetched as soon
+// as the current unit's G and Q~ no longer need the tile; Tw and Tu go to the record with plain
+// stores, Q~, M~ and the vectors with one bulk store, waited for only when their buffer is reused.
 __global__ void __launch_bounds__(pf::NT, 2)
     gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float Gf[C], betas[C], rks[C], rqs[C], gams[C];
+    __shared__ __align__(16) float Gf[C], betas[C], rks[C], rqs[C], gams[C];
+    __shared__ __align__(16) float wws[C], wus[C];  // Tw and Tu column weights
     __shared__ float scan_total;
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(8) uint64_t mbar;    // MMA completion
-    __shared__ __align__(8) uint64_t bar_kq;  // TMA of the chunk's k and q rows
+    __shared__ __align__(8) uint64_t bar_kq;  // TMA of a unit's k and q rows
 
-    const long long f = blockIdx.x / a.Hv;
-    const int h = static_cast<int>(blockIdx.x - f * a.Hv);
-    const long long total = a.chunk_off[a.num_seqs];
-    if (f >= total || f >= a.cap) return;
-    // the sequence holding chunk f: chunk_off[n] <= f < chunk_off[n + 1]
-    int lo = 0, hi = a.num_seqs;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (a.chunk_off[mid] <= f) lo = mid; else hi = mid;
-    }
-    const int n = lo;
-    if (a.chunk_off[n + 1] > a.cap) return;  // past the workspace: the sequential kernel flags it
-    const long long bos = a.cu_seqlens[n], Tn = a.cu_seqlens[n + 1] - bos;
-    const long long c0 = (f - a.chunk_off[n]) * C;
-    const int L = static_cast<int>(Tn - c0 < C ? Tn - c0 : C);
+    const long long total = a.chunk_off[a.num_seqs] < a.cap ? a.chunk_off[a.num_seqs] : a.cap;
+    const long long units = total * a.Hv;
+    if (static_cast<long long>(blockIdx.x) >= units) return;
 
-    const int hk = h / (a.Hv / a.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = tid & 127;   // the TMEM lane this thread reads
     const int qt = tid >> 7;     // which quarter of the columns
@@ -251,40 +255,66 @@ __global__ void __launch_bounds__(pf::NT, 2)
     float* Xs = reinterpret_cast<float*>(sm + P_X);
     float* vec = reinterpret_cast<float*>(sm + P_VEC);
 
+    // a unit's chunk: first token, length, and the key / value head
+    struct Unit {
+        long long tok0;
+        int L, h, hk;
+    };
+    auto unit_of = [&](long long u) -> Unit {
+        const long long f = u / a.Hv;
+        const longlong2 e = a.chunk_tab[f];
+        Unit r;
+        r.tok0 = e.x;
+        r.L = static_cast<int>(e.y & 0xffffffffLL);
+        r.h = static_cast<int>(u - f * a.Hv);
+        r.hk = r.h / (a.Hv / a.Hk);
+        return r;
+    };
+    auto fetch_kq = [&](const Unit& w) {  // thread 0
+        const int z = static_cast<int>(w.tok0);
+        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
+        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, w.hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, w.hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, w.hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, w.hk, z, &bar_kq);
+    };
+
     if (warp == 0) tc::tmem_alloc(&tmem_slot, P_TM_COLS);
+    Unit cur = unit_of(blockIdx.x);
     if (tid == 0) {
         tc::mbar_init(&mbar, 1);
         tc::mbar_init(&bar_kq, 1);
-        const int z = static_cast<int>(bos + c0);
-        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
-        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_kq);
+        fetch_kq(cur);
     }
-    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < L)
-    if (tid < L) {
-        const size_t gi = static_cast<size_t>(bos + c0 + tid) * a.Hv + h;
+    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid of the current unit (threads < L)
+    if (tid < cur.L) {
+        const size_t gi = static_cast<size_t>(cur.tok0 + tid) * a.Hv + cur.h;
         a_raw = a.a[gi];
         b_raw = a.b[gi];
     }
-    const float a_mul = expf(a.A_log[h]);
-    const float dtb = a.dt_bias[h];
-    // T's blocks above the diagonal stay zero
+    // T's blocks above the diagonal stay zero for every unit
     for (int i = tid; i < C * LST; i += NT) Ts[i] = 0.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = tmem_slot;
     const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
-    bool timed_out = false;
+    bool timed_out = false, store_pending = false;
+    uint32_t ph = 0;
 
-    do {
+    for (long long u = blockIdx.x; u < units; u += gridDim.x, ph ^= 1u) {
+        const int L = cur.L;
+        const int h = cur.h;
+        const long long nxt = u + gridDim.x;
+        const float a_mul = expf(a.A_log[h]);
+        const float dtb = a.dt_bias[h];
+        uint8_t* rec = a.records + u * static_cast<long long>(REC_BYTES);
+
         // ---- 1. wait for the rows, zero the rows past the sequence end, row norms
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, 0, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, ph, kWaitLimit);
             if (!__syncthreads_and(ok ? 1 : 0)) {  // give the copies one more bounded wait
-                if (tid == 0) tc::mbar_wait(&bar_kq, 0, kWaitLimit);
+                if (tid == 0) tc::mbar_wait(&bar_kq, ph, kWaitLimit);
                 timed_out = true;
                 break;
             }
@@ -316,6 +346,11 @@ __global__ void __launch_bounds__(pf::NT, 2)
                     rqs[s] = rsqrtf(sq + a.eps);
                 }
             }
+        }
+        // the previous unit's bulk store must have read the staging area before it is rewritten
+        if (tid == 0 && store_pending) {
+            tc::bulk_wait_read();
+            store_pending = false;
         }
         tc::fence_proxy_async();
         tc::fence_before();
@@ -359,13 +394,15 @@ __global__ void __launch_bounds__(pf::NT, 2)
         if (tid < C) {
             const int t = tid;
             gams[t] = __expf(Gf[t]);
+            wws[t] = betas[t] * gams[t] * rks[t];
+            wus[t] = betas[t];
             vec[V_DL + t] = t < L ? __expf(Gf[L - 1] - Gf[t]) : 0.f;
             vec[V_RK + t] = rks[t];
         }
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&mbar, ph, kWaitLimit);
             if (!__syncthreads_and(ok ? 1 : 0)) {
-                if (tid == 0) tc::mbar_wait(&mbar, 0, kWaitLimit);
+                if (tid == 0) tc::mbar_wait(&mbar, ph, kWaitLimit);
                 timed_out = true;
                 break;
             }
@@ -396,11 +433,14 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 const float Gt = Gf[t];
 #pragma unroll
                 for (int i4 = 0; i4 < 4; ++i4) {
+                    const float4 r4 = *reinterpret_cast<const float4*>(rks + s0 + 4 * i4);
+                    const float4 G4 = *reinterpret_cast<const float4*>(Gf + s0 + 4 * i4);
+                    const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, GG[4] = {G4.x, G4.y, G4.z, G4.w};
                     float l4[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int s = s0 + 4 * i4 + u;
-                        l4[u] = s < t ? bt * rks[s] * g[4 * i4 + u] * __expf(Gt - Gf[s]) : 0.f;
+                        l4[u] = s < t ? bt * rr[u] * g[4 * i4 + u] * __expf(Gt - GG[u]) : 0.f;
                     }
                     *reinterpret_cast<float4*>(Ls + t * LST + s0 + 4 * i4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
                 }
@@ -410,11 +450,17 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 const float rt = rqs[t] * a.scale;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
+                    const float4 ra = *reinterpret_cast<const float4*>(rks + s0 + 8 * c);
+                    const float4 rb = *reinterpret_cast<const float4*>(rks + s0 + 8 * c + 4);
+                    const float4 Ga = *reinterpret_cast<const float4*>(Gf + s0 + 8 * c);
+                    const float4 Gb = *reinterpret_cast<const float4*>(Gf + s0 + 8 * c + 4);
+                    const float rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+                    const float GG[8] = {Ga.x, Ga.y, Ga.z, Ga.w, Gb.x, Gb.y, Gb.z, Gb.w};
                     float m8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int s = s0 + c * 8 + i;
-                        m8[i] = s <= t ? rt * (rks[s] * g[c * 8 + i] * __expf(Gt - Gf[s])) : 0.f;
+                        m8[i] = s <= t ? rt * (rr[i] * g[c * 8 + i] * __expf(Gt - GG[i])) : 0.f;
                     }
                     uint4 mh, ml;
                     split_bf16x8(m8, mh, ml);
@@ -424,6 +470,17 @@ __global__ void __launch_bounds__(pf::NT, 2)
             }
         }
         __syncthreads();
+        // the [K;Q] tile is free: fetch the next unit's rows and gate inputs
+        Unit nu = cur;
+        if (nxt < units) {
+            nu = unit_of(nxt);
+            if (tid == 0) fetch_kq(nu);
+            if (tid < nu.L) {
+                const size_t gi = static_cast<size_t>(nu.tok0 + tid) * a.Hv + nu.h;
+                a_raw = a.a[gi];
+                b_raw = a.b[gi];
+            }
+        }
 
         // ---- 5. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32):
         //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution;
@@ -527,41 +584,45 @@ __global__ void __launch_bounds__(pf::NT, 2)
         __syncthreads();
 
         // ---- 6. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major),
-        //         over the [K;Q] tile, which G no longer needs
+        //         stored straight into the record
         {
             const int t = tid & (C - 1);
             const bool w_side = ((tid >> 6) & 1) == 0;
-            const uint32_t base = P_KQ + (w_side ? 0u : 16384u);
+            uint8_t* base = rec + REC_T4 + (w_side ? 0u : 16384u);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int cc = 2 * qt + c;
                 const float4 ta = *reinterpret_cast<const float4*>(Ts + t * LST + cc * 8);
                 const float4 tb = *reinterpret_cast<const float4*>(Ts + t * LST + cc * 8 + 4);
                 const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+                const float* wsrc = (w_side ? wws : wus) + cc * 8;
+                const float4 wa = *reinterpret_cast<const float4*>(wsrc);
+                const float4 wb = *reinterpret_cast<const float4*>(wsrc + 4);
+                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                 float x8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int s = cc * 8 + i;
-                    const float w = w_side ? betas[s] * gams[s] * rks[s] : betas[s];
-                    x8[i] = tv[i] * w;
-                }
+                for (int i = 0; i < 8; ++i) x8[i] = tv[i] * wv[i];
                 uint4 th, tl;
                 split_bf16x8(x8, th, tl);
-                *reinterpret_cast<uint4*>(sm + base + tc::sw_chunk(t, cc, 64)) = th;
-                *reinterpret_cast<uint4*>(sm + base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
+                *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
+                *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
             }
         }
-        // ---- 7. the record to the workspace (one bulk store of the shared-memory image)
+        // ---- 7. Q~, M~ and the vectors to the record (one bulk store of the staging area)
         tc::fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
-            tc::bulk_store(a.records + (f * a.Hv + h) * static_cast<long long>(REC_BYTES), sb, REC_BYTES);
+            tc::bulk_store(rec + REC_QT, sb + P_QT, REC_BYTES - REC_QT);
             tc::bulk_commit();
-            tc::bulk_wait_all();
+            store_pending = true;
         }
-    } while (false);
+        cur = nu;
+    }
 
-    if (timed_out && tid == 0) atomicOr(a.status, 4);
+    if (tid == 0) {
+        if (timed_out) atomicOr(a.status, 4);
+        if (store_pending) tc::bulk_wait_all();
+    }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, P_TM_COLS);
@@ -844,11 +905,16 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         tc::commit(&bars[B_A]);
                         mark(B_A, par);
                     }
-                    if (!wait_bar(B_A, par)) break;
-                    if (more) fetch_qt(c + 1);  // P~ read Q~
-                    // W and U of the next chunk while the workers convert Delta, if its tiles are in
+                    // W and U of the next chunk right behind, so that they run while the workers
+                    // convert Delta (their TMEM buffers were last read before R_D), if the tiles are in
                     bool wu_done = !more;
                     if (more && wu_ready_now(c + 1)) {
+                        issue_wu(c + 1);
+                        wu_done = true;
+                    }
+                    if (!wait_bar(B_A, par)) break;
+                    if (more) fetch_qt(c + 1);  // P~ read Q~
+                    if (!wu_done && wu_ready_now(c + 1)) {
                         tc::fence_after();
                         issue_wu(c + 1);
                         wu_done = true;

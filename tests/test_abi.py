@@ -87,10 +87,14 @@ def test_window_validation(lib):
 
 
 def test_prefill_workspace_size(lib):
-    # chunk offsets (8 bytes per sequence + 1, padded to 1 KB) + one 66,560-byte record per
-    # (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
-    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 1024 + (240 + 4) * 32 * 66560
-    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 2048 + (2 + 200) * 2 * 66560
+    # chunk offsets (8 bytes per sequence + 1, padded to 16) and the chunk table (16 bytes per chunk),
+    # padded to 1 KB, + one 66,560-byte record per (chunk, value head), for up to
+    # cap = ceil(T / 64) + num_seqs chunks
+    def header(n, cap):
+        return ((8 * (n + 1) + 15) // 16 * 16 + 16 * cap + 1023) // 1024 * 1024
+    assert header(4, 244) == 4096 and header(200, 202) == 5120
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 4096 + (240 + 4) * 32 * 66560
+    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 5120 + (2 + 200) * 2 * 66560
     assert gdn.gdn_prefill_workspace_size(0, 100, 1, 1, 128, 128, 64) == 0
     assert gdn.gdn_prefill_workspace_size(1, 100, 1, 1, 64, 128, 64) == 0    # unsupported K
     assert gdn.gdn_prefill_workspace_size(1, 100, 2, 3, 128, 128, 64) == 0   # Hv % Hk != 0
