@@ -620,7 +620,7 @@ def main():
                          "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
                          "frac": roof / t1, "note": peak_note,
                          "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
-                         "traffic": profiled_traffic("gdn_prefill_kernel",
+                         "traffic": profiled_traffic("gdn_prefill_call",
                                                      "gated_deltanet_delta_gb300/csrc/prefill.cuh")}}
     elif "prefill" in extra:
         ops["prefill_chunked"] = extra["prefill"]

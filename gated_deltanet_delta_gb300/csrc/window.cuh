@@ -60,8 +60,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     static_assert(kWinThreads == 128 && kWinHalf == 64, "window tile");
 
     // per-token buffers, double-buffered by token parity: one barrier per token
-    __shared__ __align__(16) float qraw[2][D];
-    __shared__ __align__(16) float kraw[2][D];
+    // q and k of a token by row block of 16, padded to a stride of 20 floats so that the eight row
+    // blocks a warp reads at once fall in different banks
+    constexpr int RBS = 20;
+    __shared__ __align__(16) float qraw[2][8 * RBS];
+    __shared__ __align__(16) float kraw[2][8 * RBS];
     __shared__ __align__(16) float vraw[2][kWinHalf];
     __shared__ float part_q[2][4], part_k[2][4];
     __shared__ float gates[kWinMaxTok][2];  // gate and beta of every token, computed up front
@@ -170,8 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             }
         }
         xq = nq; xk = nk; xv = nv;
-        qraw[b][tid] = cq;
-        kraw[b][tid] = ck;
+        qraw[b][(tid >> 4) * RBS + (tid & 15)] = cq;
+        kraw[b][(tid >> 4) * RBS + (tid & 15)] = ck;
         if (has_v) vraw[b][tid] = cv;
         const float sq = group_sum<32>(cq * cq);
         const float sk = group_sum<32>(ck * ck);
@@ -185,8 +188,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         const float rk = rsqrtf(((part_k[b][0] + part_k[b][1]) + (part_k[b][2] + part_k[b][3])) + a.eps);
         const float rq = rsqrtf(((part_q[b][0] + part_q[b][1]) + (part_q[b][2] + part_q[b][3])) + a.eps);
         const float gate = gates[t][0], beta = gates[t][1];
-        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * NR);
-        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * NR);
+        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * RBS);
+        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * RBS);
 
         // kv = cs rk sum_i R_ij k_i: 16 rows in registers (as 8 row pairs), then the 8 row blocks
         // by shuffles
