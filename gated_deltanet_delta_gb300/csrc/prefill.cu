@@ -81,13 +81,9 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
     }
     gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.cap, a.chunk_off,
                                                                 a.chunk_tab);
-    if (a.T > 0) {  // persistent: two CTAs per SM, each over every (grid)-th (chunk, head) unit
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        const long long units = a.cap * a.Hv;
-        const unsigned pgrid = static_cast<unsigned>(units < 2LL * sms ? units : 2LL * sms);
-        gdn_prefill_prep_kernel<<<pgrid, pf::NT, pf::P_SMEM, stream>>>(a, maps);
+    if (a.T > 0) {  // one CTA per (chunk, value head) unit of the capacity; the ones past the last chunk exit
+        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hv);
+        gdn_prefill_prep_kernel<<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
     }
     const unsigned grid = static_cast<unsigned>(a.num_seqs) * static_cast<unsigned>(a.Hv);
     gdn_prefill_kernel<<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);

@@ -17,29 +17,31 @@
 //
 // GB300 mapping: three kernels on one stream.
 //   gdn_prefill_offsets_kernel (one CTA): the first chunk of every sequence (a scan of the chunk
-//     counts), so that every chunk of every sequence has a flat index f.
-//   gdn_prefill_prep_kernel (one CTA of 512 threads per (chunk, value head), two per SM): all the
+//     counts) and a table entry per chunk (first token, sequence, length).
+//   gdn_prefill_prep_kernel (one CTA of 256 threads per (chunk, value head), five per SM): all the
 //     work that does not depend on the carried state -- row norms, gates, G = [K; Q] K^T on the
-//     tensor core, Lm and M, the triangular inverse, Tw = T diag(beta gamma rk) and Tu = T diag(beta)
-//     split into bf16 high and low parts -- written as one chunk record (kPfRecordBytes, the
-//     shared-memory image the sequential kernel uses) by one bulk store.  This is the bulk of the
-//     CUDA-core work; here every chunk of every sequence runs in parallel.
-//   gdn_prefill_kernel (one CTA of 512 threads per (sequence, value head)): the chunk recurrence.
-//     The fp32 state S (V x K = 128 x 128) lives in TMEM for the whole sequence and reaches HBM only
-//     at the start (gather from the pool slot) and at the end (scatter back).  Per chunk it takes
-//     q, k, v rows by TMA (cp.async.bulk.tensor, 64 tokens x 64 features per box) and the chunk
-//     record by two bulk copies, all fetched a chunk ahead as their buffers free up; threads i,
-//     i + 128, i + 256 and i + 384 share TMEM lane i (each takes a quarter of the columns).
+//     tensor core, Lm, the triangular inverse, Tw = T diag(beta gamma rk) and Tu = T diag(beta),
+//     M~ = diag(rq scale) M (all split into bf16 high and low parts) and Q~ = diag(gamma rq scale) Q
+//     -- written as one chunk record (kPfRecordBytes, laid out as the sequential kernel's
+//     shared-memory image).  This is the bulk of the CUDA-core work; here every chunk of every
+//     sequence runs in parallel.
+//   gdn_prefill_kernel (one CTA of 16 worker warps and a control warp per (sequence, value head)):
+//     the chunk recurrence.  The fp32 state S (V x K = 128 x 128) lives in TMEM for the whole
+//     sequence and reaches HBM only at the start (gather from the pool slot) and at the end
+//     (scatter back).  Per chunk it takes k and v rows by TMA (cp.async.bulk.tensor, 64 tokens x 64
+//     features per box) and the parts of the chunk record by bulk copies, each fetched as soon as
+//     its buffer is free; worker threads i, i + 128, i + 256 and i + 384 share TMEM lane i (each
+//     takes a quarter of the columns).
 // Every contraction is a tcgen05.mma with M = 128 (the transposed forms keep V or the feature index
 // on M):
 //     G   = [K; Q] K^T              M=128 (64 k rows + 64 q rows), N=64,  K=128   bf16 (exact inputs)
-//     W^T = K^T Tw^T,  U^T = V^T Tu^T   M=128, N=64, K=64   (Tw = T diag(beta gamma rk), Tu = T diag(beta))
-//     Delta^T = U^T - S0 W^T,  P^T = S0 Q^T                M=128, N=64, K=128
-//     (M Delta)^T = Delta^T M^T   (M = Q K^T o D rk_s)    M=128, N=64, K=64
-//     S += Delta~^T K            (Delta~ = diag(D_L rk) Delta)   M=128, N=128, K=64
-// Raw bf16 q, k, v tiles are exact MMA operands; all row scales (norms, gates, decays) are folded
-// into the computed operand or applied in fp32 afterwards.  Computed operands are rounded to bf16,
-// except T, Delta~ and both factors of M Delta, which are split into a bf16 high part and a bf16
+//     W^T = K^T Tw^T,  U^T = V^T Tu^T   M=128, N=64, K=64 (x2: hi, lo)
+//     Delta^T = U^T - S0 W^T,  O^T = S0 Q~^T                M=128, N=64, K=128
+//     O^T += Delta^T M~^T                                   M=128, N=64, K=64 (x3: hi/lo products)
+//     S += Delta~^T K            (Delta~ = diag(D_L rk) Delta)   M=128, N=128, K=64 (x2)
+// Raw bf16 k and v tiles are exact MMA operands; the row scales (norms, gates, decays) are folded
+// into the computed operands or applied in fp32 afterwards.  Computed operands are rounded to bf16,
+// except T, Delta~ and both factors of M~ Delta, which are split into a bf16 high part and a bf16
 // low part (x = hi + lo, two or three MMAs): with plain bf16 there the output and the carried state
 // miss their tolerances.  The triangular inverse runs in fp32 on CUDA cores, blockwise (16 x 16
 // diagonal blocks by column-parallel forward substitution, then the off-diagonal blocks).
@@ -68,19 +70,17 @@ constexpr uint32_t REC_VEC_BYTES = REC_BYTES - REC_VEC;
 // vector offsets (floats) inside the record's vector block
 constexpr int V_DL = 0, V_RK = 64, V_GL = 128;
 
-// the chunk-preparation kernel's dynamic shared memory (bytes from a 1024-aligned base); the first
-// REC_BYTES are the record being built, stored by one bulk copy at the end
-constexpr uint32_t P_KQ = 0;          // [K;Q] tile (two 16 KB feature halves: 64 k rows + 64 q rows);
-                                      // once G is computed, Tw / Tu hi / lo (record bytes 0 .. 32 KB)
-constexpr uint32_t P_QT = REC_QT;     // Q~
-constexpr uint32_t P_M = REC_M;       // M~ hi / lo
-constexpr uint32_t P_VEC = REC_VEC;   // record vectors
-constexpr uint32_t P_L = REC_BYTES;   // fp32 [64][LST] strictly lower Lm
-constexpr uint32_t P_T = P_L + 64 * LST * 4;  // fp32 [64][LST] T = (I + Lm)^-1
-constexpr uint32_t P_X = P_T + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
-constexpr uint32_t P_USED = P_X + 32 * ZST * 4;
+// the chunk-preparation kernel: CTAs of 256 threads, five per SM; its dynamic shared memory (bytes
+// from a 1024-aligned base) is the [K;Q] tile, reused once G, the norms and Q~ are done for the fp32
+// Lm, which the blockwise inverse turns into T in place, and the inverse's scratch
+constexpr int PNT = 256;
+constexpr uint32_t P_KQ = 0;          // [K;Q] tile: two 16 KB feature halves, 64 k rows + 64 q rows
+constexpr uint32_t P_L = 0;           // fp32 [64][LST]: Lm, then T = (I + Lm)^-1
+constexpr uint32_t P_X = P_L + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
+constexpr uint32_t P_USED = 32768;
 constexpr uint32_t P_SMEM = P_USED + 1024;
 constexpr uint32_t P_TM_G = 0, P_TM_COLS = 64;
+static_assert(P_X + 32 * ZST * 4 <= P_USED, "Lm, T and the scratch fit in the [K;Q] tile");
 
 // the sequential kernel's dynamic shared memory
 constexpr uint32_t OFF_K = 0;          // two K tiles (chunks of even / odd index), 16 KB each: two
@@ -121,7 +121,7 @@ static_assert(OFF_DL % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_M % 1024 == 0 && O
                   OFF_T4 % 1024 == 0, "operand tiles 1024-aligned");
 static_assert(OFF_T4 + REC_QT == OFF_QT && OFF_T4 + REC_M == OFF_M && OFF_T4 + REC_VEC == OFF_VEC,
               "record parts land at their tiles");
-static_assert(2 * (P_SMEM + 1024) <= 228 * 1024, "two preparation CTAs per SM");
+static_assert(5 * (P_SMEM + 4096) <= 228 * 1024, "five preparation CTAs per SM");
 static_assert(SMEM_BYTES <= 227 * 1024, "sequential kernel shared memory");
 }  // namespace pf
 
@@ -225,102 +225,79 @@ __global__ void __launch_bounds__(kPfOffThreads)
 }
 
 // ------------------------------------------------------------------------------------------------
-// The state-independent part of every (chunk, value head) unit -> its chunk record.  Persistent:
-// CTA b takes units b, b + grid, ...; unit u is chunk f = u / Hv (the table gives its first token,
-// sequence and length) of value head h = u % Hv.  The next unit's k and q rows are fetched as soon
-// as the current unit's G and Q~ no longer need the tile; Tw and Tu go to the record with plain
-// stores, Q~, M~ and the vectors with one bulk store, waited for only when their buffer is reused.
-__global__ void __launch_bounds__(pf::NT, 2)
+// The state-independent part of one (chunk, value head) unit -> its chunk record.  Unit
+// u = blockIdx.x is chunk f = u / Hv (the table gives its first token and length) of value head
+// h = u % Hv.  CTAs of 256 threads, five per SM: the latency-bound phases of one unit (the inverse
+// runs 64, 128 and 256 threads wide) overlap with those of four others.  Every part of the record
+// is written to the workspace directly.
+__global__ void __launch_bounds__(pf::PNT, 5)
     gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(16) float Gf[C], betas[C], rks[C], rqs[C], gams[C];
-    __shared__ __align__(16) float wws[C], wus[C];  // Tw and Tu column weights
+    __shared__ __align__(16) float Gf[C], betas[C], rks[C], rqs[C], gams[C], wws[C], wus[C];
     __shared__ float scan_total;
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(8) uint64_t mbar;    // MMA completion
-    __shared__ __align__(8) uint64_t bar_kq;  // TMA of a unit's k and q rows
+    __shared__ __align__(8) uint64_t bar_kq;  // TMA of the unit's k and q rows
 
     const long long total = a.chunk_off[a.num_seqs] < a.cap ? a.chunk_off[a.num_seqs] : a.cap;
-    const long long units = total * a.Hv;
-    if (static_cast<long long>(blockIdx.x) >= units) return;
+    const long long u = blockIdx.x;
+    if (u >= total * a.Hv) return;
+    const long long f = u / a.Hv;
+    const int h = static_cast<int>(u - f * a.Hv);
+    const int hk = h / (a.Hv / a.Hk);
+    const longlong2 entry = a.chunk_tab[f];
+    const long long tok0 = entry.x;
+    const int L = static_cast<int>(entry.y & 0xffffffffLL);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = tid & 127;   // the TMEM lane this thread reads
-    const int qt = tid >> 7;     // which quarter of the columns
+    const int hf = tid >> 7;     // which half of the 64 G columns
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = tc::smem_u32(sm);
     float* Ls = reinterpret_cast<float*>(sm + P_L);
-    float* Ts = reinterpret_cast<float*>(sm + P_T);
     float* Xs = reinterpret_cast<float*>(sm + P_X);
-    float* vec = reinterpret_cast<float*>(sm + P_VEC);
-
-    // a unit's chunk: first token, length, and the key / value head
-    struct Unit {
-        long long tok0;
-        int L, h, hk;
-    };
-    auto unit_of = [&](long long u) -> Unit {
-        const long long f = u / a.Hv;
-        const longlong2 e = a.chunk_tab[f];
-        Unit r;
-        r.tok0 = e.x;
-        r.L = static_cast<int>(e.y & 0xffffffffLL);
-        r.h = static_cast<int>(u - f * a.Hv);
-        r.hk = r.h / (a.Hv / a.Hk);
-        return r;
-    };
-    auto fetch_kq = [&](const Unit& w) {  // thread 0
-        const int z = static_cast<int>(w.tok0);
-        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
-        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, w.hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, w.hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, w.hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, w.hk, z, &bar_kq);
-    };
+    uint8_t* rec = a.records + u * static_cast<long long>(REC_BYTES);
+    float* vec = reinterpret_cast<float*>(rec + REC_VEC);
 
     if (warp == 0) tc::tmem_alloc(&tmem_slot, P_TM_COLS);
-    Unit cur = unit_of(blockIdx.x);
     if (tid == 0) {
         tc::mbar_init(&mbar, 1);
         tc::mbar_init(&bar_kq, 1);
-        fetch_kq(cur);
+        const int z = static_cast<int>(tok0);
+        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
+        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_kq);
     }
-    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid of the current unit (threads < L)
-    if (tid < cur.L) {
-        const size_t gi = static_cast<size_t>(cur.tok0 + tid) * a.Hv + cur.h;
+    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < L)
+    if (tid < L) {
+        const size_t gi = static_cast<size_t>(tok0 + tid) * a.Hv + h;
         a_raw = a.a[gi];
         b_raw = a.b[gi];
     }
-    // T's blocks above the diagonal stay zero for every unit
-    for (int i = tid; i < C * LST; i += NT) Ts[i] = 0.f;
+    const float a_mul = expf(a.A_log[h]);
+    const float dtb = a.dt_bias[h];
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = tmem_slot;
     const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // TMEM lane base
-    bool timed_out = false, store_pending = false;
-    uint32_t ph = 0;
+    bool timed_out = false;
 
-    for (long long u = blockIdx.x; u < units; u += gridDim.x, ph ^= 1u) {
-        const int L = cur.L;
-        const int h = cur.h;
-        const long long nxt = u + gridDim.x;
-        const float a_mul = expf(a.A_log[h]);
-        const float dtb = a.dt_bias[h];
-        uint8_t* rec = a.records + u * static_cast<long long>(REC_BYTES);
-
+    do {
         // ---- 1. wait for the rows, zero the rows past the sequence end, row norms
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, ph, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, 0, kWaitLimit);
             if (!__syncthreads_and(ok ? 1 : 0)) {  // give the copies one more bounded wait
-                if (tid == 0) tc::mbar_wait(&bar_kq, ph, kWaitLimit);
+                if (tid == 0) tc::mbar_wait(&bar_kq, 0, kWaitLimit);
                 timed_out = true;
                 break;
             }
         }
         if (L < C) {
-            for (int e = tid; e < (C - L) * 16; e += NT) {
+            for (int e = tid; e < (C - L) * 16; e += PNT) {
                 const int s = L + (e >> 4), c = e & 15;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sm + P_KQ + tc::sw_chunk(s, c, 128)) = z;
@@ -329,10 +306,10 @@ __global__ void __launch_bounds__(pf::NT, 2)
             __syncthreads();
         }
         {
-            const int rp = tid >> 4, ch = tid & 15;  // 16 threads per row, rows rp and rp + 32
+            const int rp = tid >> 4, ch = tid & 15;  // 16 threads per row, rows rp + 16 p
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int s = p * 32 + rp;
+            for (int p = 0; p < 4; ++p) {
+                const int s = p * 16 + rp;
                 const uint4 kv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(s, ch, 128));
                 const uint4 qv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + s, ch, 128));
                 float sk = bf16_sumsq8(kv4), sq = bf16_sumsq8(qv4);
@@ -346,11 +323,6 @@ __global__ void __launch_bounds__(pf::NT, 2)
                     rqs[s] = rsqrtf(sq + a.eps);
                 }
             }
-        }
-        // the previous unit's bulk store must have read the staging area before it is rewritten
-        if (tid == 0 && store_pending) {
-            tc::bulk_wait_read();
-            store_pending = false;
         }
         tc::fence_proxy_async();
         tc::fence_before();
@@ -398,35 +370,38 @@ __global__ void __launch_bounds__(pf::NT, 2)
             wus[t] = betas[t];
             vec[V_DL + t] = t < L ? __expf(Gf[L - 1] - Gf[t]) : 0.f;
             vec[V_RK + t] = rks[t];
+            if (t == 0) vec[V_GL] = __expf(Gf[L - 1]);
         }
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&mbar, ph, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, kWaitLimit);
             if (!__syncthreads_and(ok ? 1 : 0)) {
-                if (tid == 0) tc::mbar_wait(&mbar, ph, kWaitLimit);
+                if (tid == 0) tc::mbar_wait(&mbar, 0, kWaitLimit);
                 timed_out = true;
                 break;
             }
             tc::fence_after();
         }
-        if (tid == 0) vec[V_GL] = gams[L - 1];
 
-        // ---- 4. Q~ = diag(gamma_t rq_t scale) Q (bf16, rows t, K-major) from the q rows; Lm (lanes
-        //         t < 64, fp32) and M~ = diag(rq_t scale) M (lanes 64 + t, bf16 hi / lo) from G, 16
-        //         columns each
-        for (int e = tid; e < C * 16; e += NT) {
+        // ---- 4. Q~ = diag(gamma_t rq_t scale) Q (bf16, rows t, K-major) from the q rows, to the record
+        for (int e = tid; e < C * 16; e += PNT) {
             const int t = e >> 4, cc = e & 15;
             const uint4 q8 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + t, cc, 128));
-            const float f = gams[t] * (rqs[t] * a.scale);
+            const float fq = gams[t] * (rqs[t] * a.scale);
             const float4 x0 = bf16x4_to_f32x4(make_uint2(q8.x, q8.y));
             const float4 x1 = bf16x4_to_f32x4(make_uint2(q8.z, q8.w));
-            const float y[8] = {x0.x * f, x0.y * f, x0.z * f, x0.w * f, x1.x * f, x1.y * f, x1.z * f, x1.w * f};
-            *reinterpret_cast<uint4*>(sm + P_QT + tc::sw_chunk(t, cc, 64)) = pack_bf16x8(y);
+            const float y[8] = {x0.x * fq, x0.y * fq, x0.z * fq, x0.w * fq, x1.x * fq, x1.y * fq, x1.z * fq, x1.w * fq};
+            *reinterpret_cast<uint4*>(rec + REC_QT + tc::sw_chunk(t, cc, 64)) = pack_bf16x8(y);
         }
-        {
+        __syncthreads();  // the [K;Q] tile is no longer needed: Lm takes its place
+
+        // ---- 5. Lm (lanes t < 64, fp32, in place of the tile) and M~ = diag(rq_t scale) M (lanes
+        //         64 + t, bf16 hi / lo, to the record) from G, 32 columns per thread
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            const int s0 = 32 * hf + 16 * qq;
             float g[16];
-            tc::ld16(trow + P_TM_G + 16 * qt, g);
+            tc::ld16(trow + P_TM_G + s0, g);
             tc::wait_ld();
-            const int s0 = 16 * qt;
             if (row < C) {
                 const int t = row;
                 const float bt = betas[t] * rks[t];
@@ -438,9 +413,9 @@ __global__ void __launch_bounds__(pf::NT, 2)
                     const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, GG[4] = {G4.x, G4.y, G4.z, G4.w};
                     float l4[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int s = s0 + 4 * i4 + u;
-                        l4[u] = s < t ? bt * rr[u] * g[4 * i4 + u] * __expf(Gt - GG[u]) : 0.f;
+                    for (int w = 0; w < 4; ++w) {
+                        const int s = s0 + 4 * i4 + w;
+                        l4[w] = s < t ? bt * rr[w] * g[4 * i4 + w] * __expf(Gt - GG[w]) : 0.f;
                     }
                     *reinterpret_cast<float4*>(Ls + t * LST + s0 + 4 * i4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
                 }
@@ -464,32 +439,25 @@ __global__ void __launch_bounds__(pf::NT, 2)
                     }
                     uint4 mh, ml;
                     split_bf16x8(m8, mh, ml);
-                    *reinterpret_cast<uint4*>(sm + P_M + tc::sw_chunk(t, 2 * qt + c, 64)) = mh;
-                    *reinterpret_cast<uint4*>(sm + P_M + 8192 + tc::sw_chunk(t, 2 * qt + c, 64)) = ml;
+                    const int cc = s0 / 8 + c;
+                    *reinterpret_cast<uint4*>(rec + REC_M + tc::sw_chunk(t, cc, 64)) = mh;
+                    *reinterpret_cast<uint4*>(rec + REC_M + 8192 + tc::sw_chunk(t, cc, 64)) = ml;
                 }
             }
         }
         __syncthreads();
-        // the [K;Q] tile is free: fetch the next unit's rows and gate inputs
-        Unit nu = cur;
-        if (nxt < units) {
-            nu = unit_of(nxt);
-            if (tid == 0) fetch_kq(nu);
-            if (tid < nu.L) {
-                const size_t gi = static_cast<size_t>(nu.tok0 + tid) * a.Hv + nu.h;
-                a_raw = a.a[gi];
-                b_raw = a.b[gi];
-            }
-        }
 
-        // ---- 5. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32):
-        //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution;
+        // ---- 6. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32), in place of Lm:
+        //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution (a block's
+        //      16 threads share a warp: the warp reads its blocks of Lm before writing them over);
         //   B: T_{2p+1,2p} = -T_{2p+1,2p+1} Lm_{2p+1,2p} T_{2p,2p}   (32 x 32 diagonal blocks);
         //   C: T_{[32,64),[0,32)} = -T_br Lm_bl T_tl                 (the whole matrix).
-        //   B and C give each thread one row and four consecutive columns (float4 operands).
+        //   B and C read a block of Lm into the scratch product before its T overwrites it; each
+        //   thread takes one row and four consecutive columns (float4 operands).  The blocks above
+        //   the diagonal are zero from Lm.
         if (tid < C) {
             const int blk = tid >> 4, j = tid & 15;
-            const float* Lb = Ls + (16 * blk) * LST + 16 * blk;
+            float* Lb = Ls + (16 * blk) * LST + 16 * blk;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -502,32 +470,33 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 if (i & 1) acc0 = fmaf(-Lb[i * LST + i - 1], x[i - 1], acc0);
                 x[i] = (i < j) ? 0.f : acc0 + acc1;
             }
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Ts[(16 * blk + i) * LST + 16 * blk + j] = x[i];
+            for (int i = 0; i < 16; ++i) Lb[i * LST + j] = x[i];
         }
         __syncthreads();
         float* Zs = Xs;
         const int pB = tid >> 6, rB = (tid >> 2) & 15, cB = 4 * (tid & 3);
         if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p}
             const float* Lr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB;
-            const float* Tc = Ts + (32 * pB) * LST + 32 * pB + cB;
+            const float* Tc = Ls + (32 * pB) * LST + 32 * pB + cB;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
                 const float lk[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + u) * LST);
-                    acc.x = fmaf(lk[u], t4.x, acc.x); acc.y = fmaf(lk[u], t4.y, acc.y);
-                    acc.z = fmaf(lk[u], t4.z, acc.z); acc.w = fmaf(lk[u], t4.w, acc.w);
+                for (int w = 0; w < 4; ++w) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
+                    acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
+                    acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
                 }
             }
             *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = acc;
         }
         __syncthreads();
-        if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p
-            const float* Tr = Ts + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
+        if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p}
+            const float* Tr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
             const float* Xc = Zs + (16 * pB) * ZST + cB;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -535,37 +504,37 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
                 const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 x4 = *reinterpret_cast<const float4*>(Xc + (4 * k4 + u) * ZST);
-                    acc.x = fmaf(tk[u], x4.x, acc.x); acc.y = fmaf(tk[u], x4.y, acc.y);
-                    acc.z = fmaf(tk[u], x4.z, acc.z); acc.w = fmaf(tk[u], x4.w, acc.w);
+                for (int w = 0; w < 4; ++w) {
+                    const float4 x4 = *reinterpret_cast<const float4*>(Xc + (4 * k4 + w) * ZST);
+                    acc.x = fmaf(tk[w], x4.x, acc.x); acc.y = fmaf(tk[w], x4.y, acc.y);
+                    acc.z = fmaf(tk[w], x4.z, acc.z); acc.w = fmaf(tk[w], x4.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4*>(Ts + (32 * pB + 16 + rB) * LST + 32 * pB + cB) =
+            *reinterpret_cast<float4*>(Ls + (32 * pB + 16 + rB) * LST + 32 * pB + cB) =
                 make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
         const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
-        if (tid < 256) {  // Z = Lm_bl T_tl
+        {  // Z = Lm_bl T_tl (all 256 threads)
             const float* Lr = Ls + (32 + rC) * LST;
-            const float* Tc = Ts + cC;
+            const float* Tc = Ls + cC;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int k4 = 0; k4 < 8; ++k4) {
                 const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
                 const float lk[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + u) * LST);
-                    acc.x = fmaf(lk[u], t4.x, acc.x); acc.y = fmaf(lk[u], t4.y, acc.y);
-                    acc.z = fmaf(lk[u], t4.z, acc.z); acc.w = fmaf(lk[u], t4.w, acc.w);
+                for (int w = 0; w < 4; ++w) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
+                    acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
+                    acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
                 }
             }
             *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = acc;
         }
         __syncthreads();
-        if (tid < 256) {  // T_bl = -T_br Z
-            const float* Tr = Ts + (32 + rC) * LST + 32;
+        {  // T_bl = -T_br Z, over Lm_bl
+            const float* Tr = Ls + (32 + rC) * LST + 32;
             const float* Zc = Zs + cC;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -573,31 +542,31 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
                 const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 z4 = *reinterpret_cast<const float4*>(Zc + (4 * k4 + u) * ZST);
-                    acc.x = fmaf(tk[u], z4.x, acc.x); acc.y = fmaf(tk[u], z4.y, acc.y);
-                    acc.z = fmaf(tk[u], z4.z, acc.z); acc.w = fmaf(tk[u], z4.w, acc.w);
+                for (int w = 0; w < 4; ++w) {
+                    const float4 z4 = *reinterpret_cast<const float4*>(Zc + (4 * k4 + w) * ZST);
+                    acc.x = fmaf(tk[w], z4.x, acc.x); acc.y = fmaf(tk[w], z4.y, acc.y);
+                    acc.z = fmaf(tk[w], z4.z, acc.z); acc.w = fmaf(tk[w], z4.w, acc.w);
                 }
             }
-            *reinterpret_cast<float4*>(Ts + (32 + rC) * LST + cC) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            *reinterpret_cast<float4*>(Ls + (32 + rC) * LST + cC) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
 
-        // ---- 6. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major),
-        //         stored straight into the record
+        // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major),
+        //         to the record
         {
             const int t = tid & (C - 1);
             const bool w_side = ((tid >> 6) & 1) == 0;
             uint8_t* base = rec + REC_T4 + (w_side ? 0u : 16384u);
+            const float* wsrc0 = w_side ? wws : wus;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int cc = 2 * qt + c;
-                const float4 ta = *reinterpret_cast<const float4*>(Ts + t * LST + cc * 8);
-                const float4 tb = *reinterpret_cast<const float4*>(Ts + t * LST + cc * 8 + 4);
+            for (int c = 0; c < 4; ++c) {
+                const int cc = 4 * hf + c;
+                const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
+                const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
                 const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-                const float* wsrc = (w_side ? wws : wus) + cc * 8;
-                const float4 wa = *reinterpret_cast<const float4*>(wsrc);
-                const float4 wb = *reinterpret_cast<const float4*>(wsrc + 4);
+                const float4 wa = *reinterpret_cast<const float4*>(wsrc0 + cc * 8);
+                const float4 wb = *reinterpret_cast<const float4*>(wsrc0 + cc * 8 + 4);
                 const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                 float x8[8];
 #pragma unroll
@@ -608,21 +577,9 @@ __global__ void __launch_bounds__(pf::NT, 2)
                 *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
             }
         }
-        // ---- 7. Q~, M~ and the vectors to the record (one bulk store of the staging area)
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {
-            tc::bulk_store(rec + REC_QT, sb + P_QT, REC_BYTES - REC_QT);
-            tc::bulk_commit();
-            store_pending = true;
-        }
-        cur = nu;
-    }
+    } while (false);
 
-    if (tid == 0) {
-        if (timed_out) atomicOr(a.status, 4);
-        if (store_pending) tc::bulk_wait_all();
-    }
+    if (timed_out && tid == 0) atomicOr(a.status, 4);
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, P_TM_COLS);
