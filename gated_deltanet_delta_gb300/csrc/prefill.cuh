@@ -97,8 +97,9 @@ constexpr uint32_t OFF_DT = OFF_DL + 32768;      // Delta~^T hi, lo (16 KB each)
 constexpr uint32_t SMEM_USED = OFF_DT + 32768;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 // TMEM columns (fp32, 128 lanes): the state, W, U and the outputs O = P~ + M~ Delta, the last two
-// in a buffer per chunk parity
-constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 320;
+// in a buffer per chunk parity; then the low bf16 parts of S0 (S - bf16(S), two per column, the
+// even feature in the low half), the A operand of P~'s second product
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 320, TM_SL = 448;
 constexpr uint32_t TM_COLS = 512;
 // the sequential kernel's threads: 16 worker warps (conversions, outputs) and one control warp
 // (lane 0 issues every MMA and every copy)
@@ -110,7 +111,8 @@ enum : int {
     B_C,       // M~ Delta and the state update computed
     B_WU,      // W and U of a chunk computed
     R_B,       // workers: Delta converted, state scaled
-    R_D,       // workers: S0 and W of the next chunk in place
+    R_S,       // workers: S0 (high parts in shared memory, low parts in TMEM) of the next chunk in place
+    R_D,       // workers: W of the next chunk in place
     R_Z,       // workers: the tail of a short chunk zeroed
     B_K0, B_K1, B_V, B_R1, B_QT, B_RM, B_RV0, B_RV1,
     NBAR
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
 
     if (warp == 0) tc::tmem_alloc(&tmem_slot, TM_COLS);
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&bars[i], (i == R_B || i == R_D || i == R_Z) ? NW : 1);
+        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&bars[i], (i == R_B || i == R_S || i == R_D || i == R_Z) ? NW : 1);
         abort_flag = 0;
     }
     tc::fence_before();
@@ -700,13 +702,22 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         for (int c = 0; c < 2; ++c)
             *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, 2 * qt + c, 128)) = pack_bf16x8(w16 + 8 * c);
     };
-    // S (TMEM) -> S0 (bf16, K-major) for the next chunk's P~ and Delta
+    // S (TMEM) -> S0 for the next chunk's P~ and Delta: bf16 high parts (K-major, shared memory)
+    // and, for P~ only, the bf16 low parts (TMEM, feature pairs packed per column)
     auto convert_s = [&]() {
-        float s32[32];
+        float s32[32], lo16[16];
         ld32(trow + TM_S + 32 * qt, s32);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, 4 * qt + q4, 128)) = pack_bf16x8(s32 + 8 * q4);
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 hi, lo;
+            split_bf16x8(s32 + 8 * q4, hi, lo);
+            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, 4 * qt + q4, 128)) = hi;
+            lo16[4 * q4] = __uint_as_float(lo.x);
+            lo16[4 * q4 + 1] = __uint_as_float(lo.y);
+            lo16[4 * q4 + 2] = __uint_as_float(lo.z);
+            lo16[4 * q4 + 3] = __uint_as_float(lo.w);
+        }
+        tc::st16(trow + TM_SL + 16 * qt, lo16);
     };
     // outputs of chunk c from O (TMEM), tokens 16*qt .. (lane v)
     auto outputs = [&](long long c) {
@@ -845,16 +856,26 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     const bool more = c + 1 < nch;
                     const uint32_t par = c & 1;
                     const uint64_t dK = dadd(dK0, (c & 1) * 16384);
-                    // ---- A. P~^T = S0 Q~^T and Delta^T = U^T - S0 W^T (accumulated onto U^T, B negated)
-                    if (!wait_bar(R_D, par) || !wait_bar(B_QT, par)) break;
+                    // ---- A. P~^T = S0 Q~^T once S0 is in place, as S0's high parts (shared memory)
+                    //      times Q~ plus its low parts (TMEM) times Q~; then, once W is in place,
+                    //      Delta^T = U^T - S0 W^T (high parts; accumulated onto U^T, B negated)
+                    if (!wait_bar(R_S, par) || !wait_bar(B_QT, par)) break;
                     tc::fence_after();
                     {
                         const uint32_t id = tc::idesc_bf16(128, 64, 0, 0, 0);
-                        const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
                             tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
                                          dadd(dQT, (ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16_ts(tm + TM_O + (c & 1) * 64, tm + TM_SL + 8 * ks,
+                                            dadd(dQT, (ks >> 2) * 8192 + (ks & 3) * 32), id, 1u);
+                    }
+                    if (!wait_bar(R_D, par)) break;
+                    tc::fence_after();
+                    {
+                        const uint32_t idd = tc::idesc_bf16(128, 64, 0, 1, 1);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
                             tc::mma_bf16(tm + TM_U + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
@@ -928,9 +949,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     } else {
         // ---- workers
         do {
-            // gather the state from its pool slot: row v, columns 32*qt .. -> TMEM and S0 (bf16)
+            // gather the state from its pool slot: row v, columns 32*qt .. -> TMEM and S0 (bf16
+            // high parts in shared memory, low parts in TMEM)
             {
                 const float4* src = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
+                float lo16[16];
 #pragma unroll
                 for (int c16 = 0; c16 < 2; ++c16) {
                     float v[16];
@@ -941,10 +964,20 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     }
                     tc::st16(trow + TM_S + 32 * qt + c16 * 16, v);
                     const int c8 = 4 * qt + 2 * c16;
-                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8, 128)) = pack_bf16x8(v);
-                    *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + 1, 128)) = pack_bf16x8(v + 8);
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        uint4 hi, lo;
+                        split_bf16x8(v + 8 * h8, hi, lo);
+                        *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw_chunk(row, c8 + h8, 128)) = hi;
+                        lo16[8 * c16 + 4 * h8] = __uint_as_float(lo.x);
+                        lo16[8 * c16 + 4 * h8 + 1] = __uint_as_float(lo.y);
+                        lo16[8 * c16 + 4 * h8 + 2] = __uint_as_float(lo.z);
+                        lo16[8 * c16 + 4 * h8 + 3] = __uint_as_float(lo.w);
+                    }
                 }
+                tc::st16(trow + TM_SL + 16 * qt, lo16);
             }
+            warp_arrive(R_S);  // S0 of chunk 0 in place
             if (nch == 1 && short_last) {
                 if (!warp_wait(B_K0, 0) || !warp_wait(B_V, 0)) break;
                 zero_tail(0);
@@ -952,7 +985,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             }
             if (!warp_wait(B_WU, 0)) break;
             convert_w();
-            warp_arrive(R_D);  // S0 and W of chunk 0 in place
+            warp_arrive(R_D);  // W of chunk 0 in place
             bool ok = true;
             for (long long c = 0; c < nch && ok; ++c) {
                 const bool more = c + 1 < nch;
@@ -964,6 +997,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 if (!warp_wait(B_C, par)) { ok = false; break; }
                 if (more) {
                     convert_s();
+                    warp_arrive(R_S);
                     const long long c1 = c + 1;
                     if (c1 == nch - 1 && short_last) {
                         if (!warp_wait(B_K0 + static_cast<int>(c1 & 1), (c1 >> 1) & 1) || !warp_wait(B_V, c1 & 1)) {

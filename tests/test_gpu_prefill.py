@@ -109,6 +109,52 @@ def test_full_workload_sampled_units():
             assert np.array_equal(pool[s], x["state_pool"][s].astype(np.float64))
 
 
+@pytest.mark.parametrize("Hk,Hv", [(3, 3), (1, 4)])
+def test_key_head_sharing_ratios(Hk, Hv):
+    # Hv / Hk = 1 (no sharing) and 4, over several chunks and a short tail
+    seqlens = [70, 129]
+    x = gi.gdn_prefill_inputs(gi.rng(100 + Hk * Hv), seqlens, Hk, Hv, 128, 128, pool=4, mild_gates=True)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_many_short_sequences():
+    # 1100 sequences of 0 to 3 tokens: the chunk offsets are scanned in tiles of 1024 sequences, and
+    # every chunk is a short one
+    g = gi.rng(77)
+    seqlens = [int(v) for v in g.integers(0, 4, size=1100)]
+    x = gi.gdn_prefill_inputs(g, seqlens, 1, 2, 128, 128, pool=1100)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_workspace_reused_by_two_calls():
+    # one workspace, two different batches: nothing of the first call leaks into the second
+    scale = 128 ** -0.5
+    xa = gi.gdn_prefill_inputs(gi.rng(21), [300, 20], 1, 2, 128, 128, pool=2)
+    xb = gi.gdn_prefill_inputs(gi.rng(22), [40, 190, 64], 1, 2, 128, 128, pool=3)
+    ws_bytes = max(gdn.gdn_prefill_workspace_size(2, xa["T"], 1, 2, 128, 128, 64),
+                   gdn.gdn_prefill_workspace_size(3, xb["T"], 1, 2, 128, 128, 64))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    for x in (xa, xb):
+        d = _to_dev(x)
+        T, Hv = d["v"].shape[0], d["v"].shape[1]
+        out = torch.full((T, Hv, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                d["state_pool"], d["cache_indices"], d["cu_seqlens"], 64, scale=scale,
+                                out=out, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _check_all(x, d, out, scale)
+
+
 def test_split_call_equals_one_call():
     # one sequence as one call, and as two calls that carry the state through the pool
     x = gi.gdn_prefill_inputs(gi.rng(9), [200], 1, 2, 128, 128, pool=1, mild_gates=True)
