@@ -406,12 +406,13 @@ def bench_comba(torch, gdn, dist, steps, warmup, seed):
     return dict(secs=secs, alg_bytes=comba_bytes(B, H, K, V), shape=(B, H, K, V))
 
 
-def bench_prefill(torch, gdn, dist, steps, warmup, seed):
+def bench_prefill(torch, gdn, dist, steps, warmup, seed, dtype="bf16"):
     c = gi.GDN_PREFILL
     Hk, Hv, K, V, C = c["Hk"], c["Hv"], c["K"], c["V"], c["chunk"]
-    x = gi.gdn_prefill_inputs(gi.rng(seed + 2), c["seqlens"], Hk, Hv, K, V, c["pool"])
+    x = gi.gdn_prefill_inputs(gi.rng(seed + 2), c["seqlens"], Hk, Hv, K, V, c["pool"], dtype=dtype)
     dev = torch.device("cuda")
-    b16, f32 = torch.bfloat16, torch.float32
+    b16 = torch.float16 if dtype == "f16" else torch.bfloat16  # the token arrays' type
+    f32 = torch.float32
     d = {n: torch.from_numpy(x[n]).to(dt).to(dev) for n, dt in
          (("q", b16), ("k", b16), ("v", b16), ("a", b16), ("b", b16), ("A_log", f32),
           ("dt_bias", f32), ("state_pool", f32), ("cache_indices", torch.int64),
@@ -509,6 +510,7 @@ def main_single_op(args, torch, gdn, dist, seed):
         "decode": lambda: bench_decode(torch, gdn, dist, args.steps, args.warmup, seed),
         "comba": lambda: bench_comba(torch, gdn, dist, args.steps, args.warmup, seed),
         "prefill": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed),
+        "prefill_f16": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed, "f16"),
         "window_verify": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, False),
         "window_commit": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, True),
         "decode_multi": lambda: bench_decode_multi(torch, gdn, dist, args.steps, args.warmup, seed),
@@ -530,7 +532,7 @@ def main():
     ap.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline (rank 0, N=1)")
-    ap.add_argument("--op", choices=("decode", "comba", "prefill", "window_verify", "window_commit",
+    ap.add_argument("--op", choices=("decode", "comba", "prefill", "prefill_f16", "window_verify", "window_commit",
                                      "decode_multi", "decode_pooled"),
                     help="time only this operation on its workload and print its time per call "
                          "(for profiling; not the benchmark line)")
@@ -564,6 +566,9 @@ def main():
                          ("prefill", lambda: bench_prefill(torch, gdn, dist,
                                                            max(3, args.steps // 10),
                                                            args.warmup, seed)),
+                         ("prefill_f16", lambda: bench_prefill(torch, gdn, dist,
+                                                               max(3, args.steps // 10),
+                                                               args.warmup, seed, "f16")),
                          ("window_verify", lambda: bench_window(torch, gdn, dist, args.steps,
                                                                 args.warmup, seed, False)),
                          ("window_commit", lambda: bench_window(torch, gdn, dist, args.steps,
@@ -603,15 +608,20 @@ def main():
                                                      "gated_deltanet_delta_gb300/csrc/comba.cuh")}}
     elif "comba" in extra:
         ops["comba_decode"] = extra["comba"]
-    if "secs" in extra.get("prefill", {}):
-        pf = extra["prefill"]
+    for key, op_name, dt_note in (("prefill", "prefill_chunked", ""),
+                                  ("prefill_f16", "prefill_chunked_f16", ", fp16 token arrays")):
+        pf = extra.get(key, {})
+        if "secs" not in pf:
+            if key in extra:
+                ops[op_name] = pf
+            continue
         steps_pf = max(3, args.steps // 10)
         t1 = pf["secs"] / steps_pf
         t_hbm = pf["alg_bytes"] / (hbm_peak * 1e9)
         t_tc = pf["flops"] / (tf_peak * 1e12)
         roof = max(t_hbm, t_tc)
-        ops["prefill_chunked"] = {
-            "workload": gi.GDN_PREFILL["name"], "value": N * pf["T"] / t1, "unit": "tokens/s",
+        ops[op_name] = {
+            "workload": gi.GDN_PREFILL["name"] + dt_note, "value": N * pf["T"] / t1, "unit": "tokens/s",
             "us_per_call": t1 * 1e6,
             "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                          "achieved": (pf["alg_bytes"] / t1 / 1e9) if t_hbm >= t_tc
@@ -621,9 +631,8 @@ def main():
                          "frac": roof / t1, "note": peak_note,
                          "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
                          "traffic": profiled_traffic("gdn_prefill_call",
-                                                     "gated_deltanet_delta_gb300/csrc/prefill.cuh")}}
-    elif "prefill" in extra:
-        ops["prefill_chunked"] = extra["prefill"]
+                                                     "gated_deltanet_delta_gb300/csrc/prefill.cuh")
+                         if key == "prefill" else None}}
     for key in ("window_verify", "window_commit"):
         w = extra.get(key, {})
         if "secs" in w:

@@ -24,7 +24,7 @@ STATUS_BAD_SEQLENS = 2
 
 # Every symbol that include/gdn.h declares.
 ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "gdn_prefill_workspace_size",
-               "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "gdn_window_fused",
+               "gdn_prefill_chunked", "gdn_prefill_chunked_f16", "gdn_prefill_chunked_noalloc", "gdn_window_fused",
                "gdn_status_string", "gdn_last_error")
 
 
@@ -65,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_chunked.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I, I, I,
                                             F, P, P, SZ, P, P]
         lib.gdn_prefill_chunked.restype = I
+        lib.gdn_prefill_chunked_f16.argtypes = lib.gdn_prefill_chunked.argtypes
+        lib.gdn_prefill_chunked_f16.restype = I
         lib.gdn_prefill_chunked_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I,
                                                     I, I, F, P, P, P]
         lib.gdn_prefill_chunked_noalloc.restype = I
@@ -251,19 +253,21 @@ def gdn_prefill_workspace_size(num_seqs: int, T: int, Hk: int, Hv: int, K: int, 
 def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, cu_seqlens,
                         chunk_size: int = 64, scale=None, out=None, workspace=None,
                         dev_status=None):
-    """Varlen chunkwise prefill.  q,k bf16 [T,Hk,K]; v bf16 [T,Hv,V]; a,b bf16 [T,Hv];
-    A_log, dt_bias f32 [Hv]; state_pool f32 [pool,Hv,V,K] (updated in place); cache_indices int64
-    [N]; cu_seqlens int64 [N+1].  Returns out bf16 [T,Hv,V].  dev_status (int32 [1], zeroed by
-    the caller) receives STATUS_* bits for skipped sequences; scale defaults to K^-0.5."""
+    """Varlen chunkwise prefill.  q,k [T,Hk,K]; v [T,Hv,V]; a,b [T,Hv], all bf16 or all float16
+    (q's dtype selects gdn_prefill_chunked or gdn_prefill_chunked_f16); A_log, dt_bias f32 [Hv];
+    state_pool f32 [pool,Hv,V,K] (updated in place); cache_indices int64 [N]; cu_seqlens int64
+    [N+1].  Returns out [T,Hv,V] in q's dtype.  dev_status (int32 [1], zeroed by the caller)
+    receives STATUS_* bits for skipped sequences; scale defaults to K^-0.5."""
     torch = _torch()
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cache_indices.shape[0]
-    _want(q, "q", torch.bfloat16)
-    _want(k, "k", torch.bfloat16, (T, Hk, K))
-    _want(v, "v", torch.bfloat16, (T, Hv, V))
-    _want(a, "a", torch.bfloat16, (T, Hv))
-    _want(b, "b", torch.bfloat16, (T, Hv))
+    dt = q.dtype if q.dtype == torch.float16 else torch.bfloat16
+    _want(q, "q", dt)
+    _want(k, "k", dt, (T, Hk, K))
+    _want(v, "v", dt, (T, Hv, V))
+    _want(a, "a", dt, (T, Hv))
+    _want(b, "b", dt, (T, Hv))
     _want(A_log, "A_log", torch.float32, (Hv,))
     _want(dt_bias, "dt_bias", torch.float32, (Hv,))
     _want(state_pool, "state_pool", torch.float32)
@@ -272,8 +276,8 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices
     _want(cache_indices, "cache_indices", torch.int64, (N,))
     _want(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,))
     if out is None:
-        out = torch.empty((T, Hv, V), dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, (T, Hv, V))
+        out = torch.empty((T, Hv, V), dtype=dt, device=q.device)
+    _want(out, "out", dt, (T, Hv, V))
     ws_bytes = gdn_prefill_workspace_size(N, T, Hk, Hv, K, V, chunk_size)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -282,11 +286,12 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices
     _want(dev_status, "dev_status", torch.int32, (1,))
     scale = K ** -0.5 if scale is None else float(scale)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().gdn_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
-                                      _ptr(dt_bias), _ptr(state_pool), state_pool.shape[0],
-                                      _ptr(cache_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
-                                      int(chunk_size), scale, _ptr(out), _ptr(workspace), wsz,
-                                      _ptr(dev_status), _stream(q.device)), "gdn_prefill_chunked")
+    name = "gdn_prefill_chunked_f16" if dt == torch.float16 else "gdn_prefill_chunked"
+    _check(getattr(load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                                 _ptr(dt_bias), _ptr(state_pool), state_pool.shape[0],
+                                 _ptr(cache_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
+                                 int(chunk_size), scale, _ptr(out), _ptr(workspace), wsz,
+                                 _ptr(dev_status), _stream(q.device)), name)
     return out
 
 

@@ -265,56 +265,55 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------------------
+// The chunk sizes accepted: the page's two entry points default to 64 (the CUDA chunkwise one) and
+// 128 (the fully batched torch one).  The chunked form computes the same function for every chunk
+// size, up to rounding, so both run the same 64-token kernels.
+static bool prefill_chunk_size_ok(int chunk_size) { return chunk_size == 64 || chunk_size == 128; }
+
 extern "C" size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
                                              int chunk_size) {
     if (num_seqs <= 0 || T < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || K != 128 || V != 128 ||
-        chunk_size != 64 || T >= (1LL << 31) - 64)
+        !prefill_chunk_size_ok(chunk_size) || T >= (1LL << 31) - 64)
         return 0;
     return gdn::prefill_workspace_bytes(T, num_seqs, Hv);
 }
 
-extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
-                                          const void* b, const float* A_log, const float* dt_bias,
-                                          float* state_pool, int pool_size,
-                                          const int64_t* cache_indices, const int64_t* cu_seqlens,
-                                          int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
-                                          int chunk_size, float scale, void* out, void* workspace,
-                                          size_t workspace_bytes, int32_t* dev_status,
-                                          gdn_stream_t stream) {
+// gdn_prefill_chunked and gdn_prefill_chunked_f16: the same checks and launch, the token arrays
+// (q, k, v, a, b, out) in bf16 or in IEEE binary16.
+static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const void* k, const void* v,
+                                const void* a, const void* b, const float* A_log, const float* dt_bias,
+                                float* state_pool, int pool_size, const int64_t* cache_indices,
+                                const int64_t* cu_seqlens, int num_seqs, int64_t T, int Hk, int Hv, int K,
+                                int V, int chunk_size, float scale, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, gdn_stream_t stream) {
     REQUIRE(num_seqs >= 0 && T >= 0 && pool_size >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1,
-            GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: sizes must be num_seqs, T, pool_size >= 0 and Hk, Hv, K, V >= 1");
-    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: Hv (%d) must be a multiple of Hk (%d)", Hv, Hk);
-    REQUIRE(K == 128 && V == 128, GDN_ERR_UNSUPPORTED,
-            "gdn_prefill_chunked: K and V must be 128 (got K=%d V=%d)", K, V);
-    REQUIRE(chunk_size == 64, GDN_ERR_UNSUPPORTED,
-            "gdn_prefill_chunked: chunk_size must be 64 (got %d)", chunk_size);
+            GDN_ERR_INVALID_ARG, "%s: sizes must be num_seqs, T, pool_size >= 0 and Hk, Hv, K, V >= 1", fn);
+    REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG, "%s: Hv (%d) must be a multiple of Hk (%d)", fn, Hv, Hk);
+    REQUIRE(K == 128 && V == 128, GDN_ERR_UNSUPPORTED, "%s: K and V must be 128 (got K=%d V=%d)", fn, K, V);
+    REQUIRE(prefill_chunk_size_ok(chunk_size), GDN_ERR_UNSUPPORTED, "%s: chunk_size must be 64 or 128 (got %d)",
+            fn, chunk_size);
     if (num_seqs == 0) return GDN_OK;
     REQUIRE(cache_indices && cu_seqlens && dev_status && A_log && dt_bias && state_pool,
-            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: null pointer");
-    REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: null token pointer");
+            GDN_ERR_INVALID_ARG, "%s: null pointer", fn);
+    REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG, "%s: null token pointer", fn);
     REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(state_pool, 16),
-            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: q, k, v and state_pool must be 16-byte aligned");
+            GDN_ERR_INVALID_ARG, "%s: q, k, v and state_pool must be 16-byte aligned", fn);
     REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(out, 2) && aligned(A_log, 4) &&
                 aligned(dt_bias, 4) && aligned(dev_status, 4) && aligned(cache_indices, 8) &&
                 aligned(cu_seqlens, 8),
-            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: misaligned argument");
+            GDN_ERR_INVALID_ARG, "%s: misaligned argument", fn);
     const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
-    REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: out overlaps state_pool");
+    REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG, "%s: out overlaps state_pool",
+            fn);
     REQUIRE((long long)num_seqs * Hv < (1LL << 31) && T < (1LL << 31) - 64 &&
                 gdn::prefill_chunk_cap(T, num_seqs) * Hv < (1LL << 31),
-            GDN_ERR_UNSUPPORTED, "gdn_prefill_chunked: grid or token count too large");
+            GDN_ERR_UNSUPPORTED, "%s: grid or token count too large", fn);
     const size_t ws_need = gdn::prefill_workspace_bytes(T, num_seqs, Hv);
     REQUIRE(workspace && workspace_bytes >= ws_need, GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: workspace of %zu bytes given, %zu needed", workspace ? workspace_bytes : 0,
-            ws_need);
-    REQUIRE(aligned(workspace, 256), GDN_ERR_INVALID_ARG,
-            "gdn_prefill_chunked: workspace must be 256-byte aligned");
+            "%s: workspace of %zu bytes given, %zu needed", fn, workspace ? workspace_bytes : 0, ws_need);
+    REQUIRE(aligned(workspace, 256), GDN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
     REQUIRE(!any_overlap(workspace, ws_need, out, obytes) && !any_overlap(workspace, ws_need, state_pool, pbytes),
-            GDN_ERR_INVALID_ARG, "gdn_prefill_chunked: workspace overlaps out or state_pool");
+            GDN_ERR_INVALID_ARG, "%s: workspace overlaps out or state_pool", fn);
 
     gdn::PrefillArgs p;
     p.q = static_cast<const uint16_t*>(q);
@@ -336,12 +335,37 @@ extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const vo
     p.Hv = Hv;
     p.scale = scale;
     p.eps = 1e-6f;
-    const cudaError_t e = gdn::launch_prefill(p, workspace, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = gdn::launch_prefill(p, workspace, static_cast<cudaStream_t>(stream), f16);
     if (e != cudaSuccess)
-        return fail(GDN_ERR_CUDA, "gdn_prefill_chunked: launch failed (TMA descriptors or kernel): %s",
-                    cudaGetErrorString(e));
+        return fail(GDN_ERR_CUDA, "%s: launch failed (TMA descriptors or kernel): %s", fn, cudaGetErrorString(e));
     g_last_error[0] = '\0';
     return GDN_OK;
+}
+
+extern "C" gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
+                                          const void* b, const float* A_log, const float* dt_bias,
+                                          float* state_pool, int pool_size,
+                                          const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                          int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                          int chunk_size, float scale, void* out, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status,
+                                          gdn_stream_t stream) {
+    return prefill_entry("gdn_prefill_chunked", false, q, k, v, a, b, A_log, dt_bias, state_pool, pool_size,
+                         cache_indices, cu_seqlens, num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out,
+                         workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" gdn_status gdn_prefill_chunked_f16(const void* q, const void* k, const void* v, const void* a,
+                                              const void* b, const float* A_log, const float* dt_bias,
+                                              float* state_pool, int pool_size,
+                                              const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                              int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
+                                              int chunk_size, float scale, void* out, void* workspace,
+                                              size_t workspace_bytes, int32_t* dev_status,
+                                              gdn_stream_t stream) {
+    return prefill_entry("gdn_prefill_chunked_f16", true, q, k, v, a, b, A_log, dt_bias, state_pool, pool_size,
+                         cache_indices, cu_seqlens, num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out,
+                         workspace, workspace_bytes, dev_status, stream);
 }
 
 

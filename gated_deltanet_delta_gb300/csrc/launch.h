@@ -23,6 +23,7 @@ inline size_t prefill_header_bytes(int num_seqs, long long cap) {
 }
 long long prefill_chunk_cap(long long T, int num_seqs);
 size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv);
-cudaError_t launch_prefill(const PrefillArgs& a, void* workspace, cudaStream_t stream);
+// f16: q, k, v, a, b and out are IEEE binary16 (else bf16).
+cudaError_t launch_prefill(const PrefillArgs& a, void* workspace, cudaStream_t stream, bool f16);
 
 }  // namespace gdn

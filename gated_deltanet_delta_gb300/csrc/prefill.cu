@@ -30,15 +30,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T, H, 128] bf16, boxes of 64 features x 1 head x 64 tokens, 128-byte swizzle, zero fill past T.
-bool encode_rows(CUtensorMap* map, const void* base, long long T, int H) {
+// [T, H, 128] bf16 or fp16, boxes of 64 features x 1 head x 64 tokens, 128-byte swizzle, zero fill
+// past T.
+bool encode_rows(CUtensorMap* map, const void* base, long long T, int H, bool f16) {
     const auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(H) * 128 * 2};
     const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t estride[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -52,17 +53,26 @@ size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) {
     return prefill_header_bytes(num_seqs, cap) + static_cast<size_t>(cap) * Hv * static_cast<size_t>(kPfRecordBytes);
 }
 
-cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_t stream) {
+namespace {
+template <bool F16>
+cudaError_t set_smem_limits() {
+    cudaError_t e = cudaFuncSetAttribute(gdn_prefill_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pf::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gdn_prefill_prep_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(pf::P_SMEM));
+}
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_t stream, bool f16) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!g_smem_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(pf::SMEM_BYTES));
+        e = set_smem_limits<false>();
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gdn_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(pf::P_SMEM));
+        e = set_smem_limits<true>();
         if (e != cudaSuccess) return e;
         g_smem_set[dev].store(1, std::memory_order_release);
     }
@@ -75,18 +85,20 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (a.T > 0) {  // with T = 0 every sequence is empty and no kernel reads the maps
-        if (!encode_rows(&maps.q, a.q, a.T, a.Hk) || !encode_rows(&maps.k, a.k, a.T, a.Hk) ||
-            !encode_rows(&maps.v, a.v, a.T, a.Hv))
+        if (!encode_rows(&maps.q, a.q, a.T, a.Hk, f16) || !encode_rows(&maps.k, a.k, a.T, a.Hk, f16) ||
+            !encode_rows(&maps.v, a.v, a.T, a.Hv, f16))
             return cudaErrorInvalidValue;
     }
     gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.cap, a.chunk_off,
                                                                 a.chunk_tab);
     if (a.T > 0) {  // one CTA per (chunk, value head) unit of the capacity; the ones past the last chunk exit
         const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hv);
-        gdn_prefill_prep_kernel<<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
+        if (f16) gdn_prefill_prep_kernel<true><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
+        else gdn_prefill_prep_kernel<false><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
     }
     const unsigned grid = static_cast<unsigned>(a.num_seqs) * static_cast<unsigned>(a.Hv);
-    gdn_prefill_kernel<<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
+    if (f16) gdn_prefill_kernel<true><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
+    else gdn_prefill_kernel<false><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
     return cudaGetLastError();
 }
 

@@ -41,9 +41,14 @@
 //     S += Delta~^T K            (Delta~ = diag(D_L rk) Delta)   M=128, N=128, K=64 (x2)
 // Raw bf16 k and v tiles are exact MMA operands; the row scales (norms, gates, decays) are folded
 // into the computed operands or applied in fp32 afterwards.  Computed operands are rounded to bf16,
-// except T, Delta~ and both factors of M~ Delta, which are split into a bf16 high part and a bf16
-// low part (x = hi + lo, two or three MMAs): with plain bf16 there the output and the carried state
-// miss their tolerances.  The triangular inverse runs in fp32 on CUDA cores, blockwise (16 x 16
+// except T, Delta~, both factors of M~ Delta and S0 in P~, which are split into a bf16 high part and
+// a bf16 low part (x = hi + lo, two or three MMAs): with plain bf16 there the output and the carried
+// state miss their tolerances.
+// fp16 inputs (q, k, v, a, b and the output in IEEE binary16, the F16 instances): an MMA takes both
+// operands in one type, so the products with raw tiles (G, W/U, the state update) run on fp16
+// operands, with their computed partners (Tw, Tu, Delta~) split into fp16 high and low parts; the
+// other products keep bf16.  fp16 high / low parts carry about 22 bits but only fp16's range: a
+// partner entry beyond 65504 in magnitude (a key row of norm below |Delta| / 65504) overflows.  The triangular inverse runs in fp32 on CUDA cores, blockwise (16 x 16
 // diagonal blocks by column-parallel forward substitution, then the off-diagonal blocks).
 // Chunks never straddle sequences; rows past a sequence's end are zero in the tiles and have
 // beta = 0 and l = 0, so they change nothing and their outputs are not written.
@@ -144,13 +149,61 @@ __device__ __forceinline__ void split_bf16x8(const float* x, uint4& hi, uint4& l
     }
     lo = pack_bf16x8(l);
 }
+// The input element type: bf16 (F16 = false) or IEEE binary16 (F16 = true).
+template <bool F16>
+__device__ __forceinline__ float in_to_f32(uint16_t h) {
+    if constexpr (F16) return __half2float(__ushort_as_half(h));
+    else return bf16_to_f32(h);
+}
+template <bool F16>
+__device__ __forceinline__ float4 in4_to_f32x4(uint2 p) {
+    if constexpr (F16) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&p.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&p.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return bf16x4_to_f32x4(p);
+    }
+}
+// One output element in the input type, round to nearest even.
+template <bool F16>
+__device__ __forceinline__ uint16_t f32_to_in(float x) {
+    if constexpr (F16) return __half_as_ushort(__float2half_rn(x));
+    else return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xffffu);
+}
+// Split 8 floats into high and low parts of the input type (the operands multiplied with raw tiles).
+template <bool F16>
+__device__ __forceinline__ void split_in_x8(const float* x, uint4& hi, uint4& lo) {
+    if constexpr (F16) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h2 = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+            const float2 hf = __half22float2(h2);
+            const __half2 l2 = __floats2half2_rn(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+            hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            lw[i] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+        hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+        split_bf16x8(x, hi, lo);
+    }
+}
+// The instruction descriptor of an MMA whose operands are both of the input type.
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc_in(int M, int N, int a_mn, int b_mn, int b_neg) {
+    return F16 ? (tc::idesc_bf16(M, N, a_mn, b_mn, b_neg) & ~((1u << 7) | (1u << 10)))
+               : tc::idesc_bf16(M, N, a_mn, b_mn, b_neg);
+}
 // A descriptor advanced by `bytes` (a multiple of 16): only the 14-bit start-address field changes,
 // and addresses stay inside the 256 KB shared window, so a plain add cannot carry out of it.
 __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
-__device__ __forceinline__ float bf16_sumsq8(const uint4& p) {
-    const float4 a = bf16x4_to_f32x4(make_uint2(p.x, p.y));
-    const float4 b = bf16x4_to_f32x4(make_uint2(p.z, p.w));
+template <bool F16>
+__device__ __forceinline__ float in_sumsq8(const uint4& p) {
+    const float4 a = in4_to_f32x4<F16>(make_uint2(p.x, p.y));
+    const float4 b = in4_to_f32x4<F16>(make_uint2(p.z, p.w));
     return fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w,
            fmaf(b.x, b.x, fmaf(b.y, b.y, fmaf(b.z, b.z, b.w * b.w)))))));
 }
@@ -232,6 +285,7 @@ __global__ void __launch_bounds__(kPfOffThreads)
 // h = u % Hv.  CTAs of 256 threads, five per SM: the latency-bound phases of one unit (the inverse
 // runs 64, 128 and 256 threads wide) overlap with those of four others.  Every part of the record
 // is written to the workspace directly.
+template <bool F16>
 __global__ void __launch_bounds__(pf::PNT, 5)
     gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
@@ -314,7 +368,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                 const int s = p * 16 + rp;
                 const uint4 kv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(s, ch, 128));
                 const uint4 qv4 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + s, ch, 128));
-                float sk = bf16_sumsq8(kv4), sq = bf16_sumsq8(qv4);
+                float sk = in_sumsq8<F16>(kv4), sq = in_sumsq8<F16>(qv4);
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) {
                     sk += __shfl_xor_sync(kFullMask, sk, o);
@@ -334,7 +388,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         // ---- 2. G = [K; Q] K^T
         if (tid == 0) {
             const uint64_t dKQ = tc::sdesc(sb + P_KQ, 16, 1024);
-            const uint32_t id = tc::idesc_bf16(128, 64, 0, 0, 0);
+            const uint32_t id = idesc_in<F16>(128, 64, 0, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t d = dadd(dKQ, (ks >> 2) * 16384 + (ks & 3) * 32);
@@ -347,10 +401,10 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             const int t = tid;
             float ell = 0.f, be = 0.f;
             if (t < L) {
-                const float x = bf16_to_f32(a_raw) + dtb;
+                const float x = in_to_f32<F16>(a_raw) + dtb;
                 const float sp = x > 20.f ? x : log1pf(__expf(x));
                 ell = -a_mul * sp;
-                be = __frcp_rn(1.f + __expf(-bf16_to_f32(b_raw)));
+                be = __frcp_rn(1.f + __expf(-in_to_f32<F16>(b_raw)));
             }
             float g = ell;
 #pragma unroll
@@ -389,8 +443,8 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             const int t = e >> 4, cc = e & 15;
             const uint4 q8 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + t, cc, 128));
             const float fq = gams[t] * (rqs[t] * a.scale);
-            const float4 x0 = bf16x4_to_f32x4(make_uint2(q8.x, q8.y));
-            const float4 x1 = bf16x4_to_f32x4(make_uint2(q8.z, q8.w));
+            const float4 x0 = in4_to_f32x4<F16>(make_uint2(q8.x, q8.y));
+            const float4 x1 = in4_to_f32x4<F16>(make_uint2(q8.z, q8.w));
             const float y[8] = {x0.x * fq, x0.y * fq, x0.z * fq, x0.w * fq, x1.x * fq, x1.y * fq, x1.z * fq, x1.w * fq};
             *reinterpret_cast<uint4*>(rec + REC_QT + tc::sw_chunk(t, cc, 64)) = pack_bf16x8(y);
         }
@@ -554,8 +608,8 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         }
         __syncthreads();
 
-        // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as bf16 hi / lo (rows t, K-major),
-        //         to the record
+        // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as hi / lo parts of the input type
+        //         (rows t, K-major), to the record
         {
             const int t = tid & (C - 1);
             const bool w_side = ((tid >> 6) & 1) == 0;
@@ -574,7 +628,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x8[i] = tv[i] * wv[i];
                 uint4 th, tl;
-                split_bf16x8(x8, th, tl);
+                split_in_x8<F16>(x8, th, tl);
                 *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
                 *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
             }
@@ -597,6 +651,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 // alternates too).  The output scales are folded into Q~ and M~ by the preparation kernel, so an
 // output is one TMEM read and one store.  The control lane issues the MMAs as soon as the
 // workers' hand-off arrives and each copy as soon as its buffer's last reader is done.
+template <bool F16>
 __global__ void __launch_bounds__(pf::NTS, 1)
     gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
@@ -729,7 +784,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         const int n_here = L - 16 * qt;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            if (i < n_here) o[i * vo_stride] = static_cast<uint16_t>(pack_bf16x2(o16[i], 0.f) & 0xffffu);
+            if (i < n_here) o[i * vo_stride] = f32_to_in<F16>(o16[i]);
     };
     // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
     // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates
@@ -756,7 +811,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             float x8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) x8[i] = d16[8 * cc2 + i] * dl[i] * rk[i];
-            split_bf16x8(x8, hi, lo);
+            split_in_x8<F16>(x8, hi, lo);
             *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, cc, 128)) = hi;
             *reinterpret_cast<uint4*>(sm + OFF_DT + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
         }
@@ -811,7 +866,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             auto issue_wu = [&](long long c) {
                 const uint64_t dK = dadd(dK0, (c & 1) * 16384);
                 const uint32_t tu = tm + TM_U + (c & 1) * 64;
-                const uint32_t idw = tc::idesc_bf16(128, 64, 1, 0, 0);
+                const uint32_t idw = idesc_in<F16>(128, 64, 1, 0, 0);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -902,7 +957,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     tc::fence_after();
                     {
                         const uint32_t idm = tc::idesc_bf16(128, 64, 0, 0, 0);
-                        const uint32_t ids = tc::idesc_bf16(128, 128, 0, 1, 0);
+                        const uint32_t ids = idesc_in<F16>(128, 128, 0, 1, 0);
 #pragma unroll
                         for (int pr = 0; pr < 3; ++pr) {
                             const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo

@@ -46,6 +46,11 @@ def bf16_round(x) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).reshape(a.shape)
 
 
+def f16_round(x) -> np.ndarray:
+    """Round float32 values to the nearest IEEE binary16 (ties to even); returned as float32."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
 def _randn(g: np.random.Generator, shape) -> np.ndarray:
     return g.standard_normal(shape, dtype=np.float32)
 
@@ -94,18 +99,20 @@ def comba_decode_token(g: np.random.Generator, B: int, H: int, K: int, V: int) -
 # Prefill
 # ------------------------------------------------------------------------------------------------
 def gdn_prefill_inputs(g: np.random.Generator, seqlens, Hk: int, Hv: int, K: int, V: int,
-                       pool: int, mild_gates: bool = False) -> dict:
+                       pool: int, mild_gates: bool = False, dtype: str = "bf16") -> dict:
     """Varlen prefill inputs.  mild_gates draws A_log = log(U(0.01, 0.1)) instead of
-    log(U(1, 16)), so that the state carried between chunks is not wiped out by the decay."""
+    log(U(1, 16)), so that the state carried between chunks is not wiped out by the decay.
+    dtype ("bf16" or "f16") is the type q, k, v, a and b are rounded to (the same draws)."""
+    rnd = {"bf16": bf16_round, "f16": f16_round}[dtype]
     seqlens = [int(s) for s in seqlens]
     T = int(sum(seqlens))
     cu = np.zeros(len(seqlens) + 1, dtype=np.int64)
     cu[1:] = np.cumsum(seqlens)
-    q = bf16_round(_randn(g, (T, Hk, K)))
-    k = bf16_round(_randn(g, (T, Hk, K)))
-    v = bf16_round(_randn(g, (T, Hv, V)))
-    a = bf16_round(_randn(g, (T, Hv)))
-    b = bf16_round(_randn(g, (T, Hv)))
+    q = rnd(_randn(g, (T, Hk, K)))
+    k = rnd(_randn(g, (T, Hk, K)))
+    v = rnd(_randn(g, (T, Hv, V)))
+    a = rnd(_randn(g, (T, Hv)))
+    b = rnd(_randn(g, (T, Hv)))
     lo, hi = (0.01, 0.1) if mild_gates else (1.0, 16.0)
     A_log = np.log(g.uniform(lo, hi, Hv)).astype(np.float32)
     dt_bias = g.uniform(-1.0, 1.0, Hv).astype(np.float32)

@@ -8,13 +8,15 @@
  *   gdn_decode_multi     T consecutive decode steps with the state held on chip
  *   comba_decode_step    one-token Comba step (state read with key p, written with key k)
  *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
+ *   gdn_prefill_chunked_f16  the same with IEEE binary16 token arrays
  *   gdn_prefill_chunked_noalloc  the same with the library's own fixed-size workspace
  *   gdn_window_fused     fused decode window: conv + SiLU, L2 norm, gates, recurrence over ntok
  *                        tokens, gated RMSNorm, with verify / commit / partial commit
  *
  * Conventions shared by every entry point
  *   - Every tensor argument is a DEVICE pointer to dense, contiguous, row-major memory in the layout
- *     given beside it.  "bf16" is IEEE bfloat16 (the upper half of a float32); "f32" is IEEE float.
+ *     given beside it.  "bf16" is IEEE bfloat16 (the upper half of a float32); "f16" is IEEE
+ *     binary16; "f32" is IEEE float.
  *   - The caller owns every buffer, including the prefill workspace.  The library allocates no
  *     device memory and keeps no global state besides a per-device table of kernel attributes and
  *     the fixed 64 MiB device scratch array of gdn_prefill_chunked_noalloc.
@@ -163,8 +165,10 @@ size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K
  *     beta_t = sigmoid(b_t);  k^ = k / sqrt(|k|^2 + 1e-6);  q^ = scale q / sqrt(|q|^2 + 1e-6);
  *     S <- g_t S (I - beta_t k^ k^^T) + beta_t v_t k^^T;  out_t = S q^;
  *     state_pool[cache_indices[n], h] <- S.
- * computed chunk by chunk (chunk_size tokens, chunks restart at each sequence start, the last one
- * may be short) with the WY representation; the inter-chunk carry is f32.
+ * computed chunk by chunk (64 tokens, chunks restart at each sequence start, the last one may be
+ * short) with the WY representation; the inter-chunk carry is f32.  The chunked form gives the same
+ * function for every chunk size up to rounding, so chunk_size selects nothing: the page's two
+ * defaults, 64 and 128, are accepted and both run 64-token chunks.
  *
  *   q, k           bf16 [T, Hk, K]    not pre-normalised
  *   v              bf16 [T, Hv, V]
@@ -182,7 +186,7 @@ size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K
  *   dev_status     device int32, zeroed by the caller; the kernels OR in GDN_STATUS_* bits for a
  *                  sequence they skip (slot out of range, malformed bounds)
  *   scale          query scale (K^-0.5 when the caller has no other value)
- * Supported: K = V = 128, chunk_size = 64, Hv % Hk == 0.
+ * Supported: K = V = 128, chunk_size 64 or 128, Hv % Hk == 0.
  */
 gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a,
                                const void* b, const float* A_log, const float* dt_bias,
@@ -191,6 +195,23 @@ gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, cons
                                int K, int V, int chunk_size, float scale, void* out,
                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                gdn_stream_t stream);
+
+/*
+ * gdn_prefill_chunked_f16 -- gdn_prefill_chunked with q, k, v, a, b and out in f16 instead of bf16
+ * ([gdn_chunkwise] gdn_extend_chunkwise: q, k, v "bf16/fp16").  Same arguments, layouts, workspace
+ * (gdn_prefill_workspace_size), checks and status bits; out is rounded to f16 (nearest even).
+ * Inputs are widened exactly.  The products of raw k and v rows run on f16 operands; their
+ * computed partners (the WY factors and the scaled Delta) are split into f16 high and low parts,
+ * whose range is f16's: a key row of norm below |Delta| / 65504 (|Delta| the size of a value
+ * correction) overflows them and gives non-finite outputs.  bf16 inputs have no such limit.
+ */
+gdn_status gdn_prefill_chunked_f16(const void* q, const void* k, const void* v, const void* a,
+                                   const void* b, const float* A_log, const float* dt_bias,
+                                   float* state_pool, int pool_size, const int64_t* cache_indices,
+                                   const int64_t* cu_seqlens, int num_seqs, int64_t T, int Hk, int Hv,
+                                   int K, int V, int chunk_size, float scale, void* out,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   gdn_stream_t stream);
 
 /*
  * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot allocate device memory

@@ -98,10 +98,15 @@ def test_prefill_workspace_size(lib):
     assert gdn.gdn_prefill_workspace_size(0, 100, 1, 1, 128, 128, 64) == 0
     assert gdn.gdn_prefill_workspace_size(1, 100, 1, 1, 64, 128, 64) == 0    # unsupported K
     assert gdn.gdn_prefill_workspace_size(1, 100, 2, 3, 128, 128, 64) == 0   # Hv % Hk != 0
+    # chunk size 128 (the page's batched default) runs the same 64-token chunks: same workspace
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 128) == \
+        gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64)
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 96) == 0
 
 
-def test_prefill_validation(lib):
-    f = lib.gdn_prefill_chunked
+@pytest.mark.parametrize("name", ["gdn_prefill_chunked", "gdn_prefill_chunked_f16"])
+def test_prefill_validation(lib, name):
+    f = getattr(lib, name)
     pool, out = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 40)
     need = gdn.gdn_prefill_workspace_size(2, 100, 1, 2, 128, 128, 64)
 
@@ -111,8 +116,9 @@ def test_prefill_validation(lib):
     ws = ctypes.c_void_p(1 << 44)
     assert call(N, 0) == gdn.GDN_ERR_INVALID_ARG and "workspace" in gdn.last_error()
     assert call(ws, need - 1) == gdn.GDN_ERR_INVALID_ARG and "needed" in gdn.last_error()
+    assert gdn.last_error().startswith(name + ":")
     assert call(ctypes.c_void_p((1 << 44) + 16), need) == gdn.GDN_ERR_INVALID_ARG   # misaligned
     assert call(ctypes.c_void_p((1 << 40) - 256), need) == gdn.GDN_ERR_INVALID_ARG  # overlaps out
-    assert call(ws, need, chunk=32) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(ws, need, chunk=32) == gdn.GDN_ERR_UNSUPPORTED and "64 or 128" in gdn.last_error()
     assert call(ws, need, K=64) == gdn.GDN_ERR_UNSUPPORTED
     assert call(N, 0, num_seqs=0) == gdn.GDN_OK

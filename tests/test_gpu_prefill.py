@@ -24,21 +24,21 @@ def _lib():
     library()
 
 
-def _to_dev(x):
-    b16, f32, i64 = torch.bfloat16, torch.float32, torch.int64
-    return {n: dev(x[n], dt) for n, dt in (("q", b16), ("k", b16), ("v", b16), ("a", b16),
-                                           ("b", b16), ("A_log", f32), ("dt_bias", f32),
+def _to_dev(x, tok=torch.bfloat16):
+    f32, i64 = torch.float32, torch.int64
+    return {n: dev(x[n], dt) for n, dt in (("q", tok), ("k", tok), ("v", tok), ("a", tok),
+                                           ("b", tok), ("A_log", f32), ("dt_bias", f32),
                                            ("state_pool", f32), ("cache_indices", i64),
                                            ("cu_seqlens", i64))}
 
 
-def _gpu(d, scale, out_fill=SENTINEL):
+def _gpu(d, scale, out_fill=SENTINEL, chunk_size=64):
     T, Hv = d["v"].shape[0], d["v"].shape[1]
-    out = torch.full((T, Hv, 128), out_fill, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((T, Hv, 128), out_fill, dtype=d["v"].dtype, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
-                            d["state_pool"], d["cache_indices"], d["cu_seqlens"], 64, scale=scale,
-                            out=out, dev_status=status)
+                            d["state_pool"], d["cache_indices"], d["cu_seqlens"], chunk_size,
+                            scale=scale, out=out, dev_status=status)
     torch.cuda.synchronize()
     return out, int(status.item())
 
@@ -119,6 +119,41 @@ def test_key_head_sharing_ratios(Hk, Hv):
     out, st = _gpu(d, scale)
     assert st == 0
     _check_all(x, d, out, scale)
+
+
+@pytest.mark.parametrize("mild", [False, True])
+@pytest.mark.parametrize("seqlens", [[1], [65, 100], [64, 0, 130, 1, 7], [300, 20]])
+def test_fp16_inputs(seqlens, mild):
+    # q, k, v, a, b and out in IEEE binary16 (gdn_prefill_chunked_f16), with a ratio-2 head sharing
+    x = gi.gdn_prefill_inputs(gi.rng(500 + sum(seqlens) + mild), seqlens, 2, 4, 128, 128,
+                              pool=len(seqlens) + 2, mild_gates=mild, dtype="f16")
+    d = _to_dev(x, torch.float16)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert out.dtype == torch.float16 and st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_fp16_long_mild_sequence_carries_the_state():
+    x = gi.gdn_prefill_inputs(gi.rng(4), [1280 + 33], 1, 2, 128, 128, pool=2, mild_gates=True,
+                              dtype="f16")
+    d = _to_dev(x, torch.float16)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_chunk_size_128_gives_the_same_call():
+    # chunk size 128 (the page's batched default) selects the same 64-token computation
+    x = gi.gdn_prefill_inputs(gi.rng(9), [200, 64, 3], 2, 4, 128, 128, pool=4, mild_gates=True)
+    scale = 128 ** -0.5
+    d64, d128 = _to_dev(x), _to_dev(x)
+    out64, st64 = _gpu(d64, scale)
+    out128, st128 = _gpu(d128, scale, chunk_size=128)
+    assert st64 == 0 and st128 == 0
+    assert torch.equal(out64, out128) and torch.equal(d64["state_pool"], d128["state_pool"])
+    _check_all(x, d128, out128, scale)
 
 
 def test_many_short_sequences():
@@ -202,5 +237,5 @@ def test_rejections():
     d = _to_dev(x)
     with pytest.raises(gdn.GdnError) as e:
         gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
-                                d["state_pool"], d["cache_indices"], d["cu_seqlens"], 128)
-    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+                                d["state_pool"], d["cache_indices"], d["cu_seqlens"], 96)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED  # chunk sizes other than 64 and 128
