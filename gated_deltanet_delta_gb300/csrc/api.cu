@@ -408,7 +408,7 @@ extern "C" gdn_status gdn_window_fused(float* state, const float* hist, float* h
                 aligned(beta, 4) && aligned(z, 4) && aligned(dt, 4) && aligned(ssm_a, 4) &&
                 aligned(gamma, 4) && aligned(y, 4),
             GDN_ERR_INVALID_ARG, "gdn_window_fused: float arrays must be 4-byte aligned");
-    REQUIRE(2LL * N * h_v < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_window_fused: grid too large");
+    REQUIRE(1LL * N * h_v < (1LL << 31), GDN_ERR_UNSUPPORTED, "gdn_window_fused: grid too large");
 
     gdn::WindowArgs a;
     a.state = state;
@@ -428,8 +428,11 @@ extern "C" gdn_status gdn_window_fused(float* state, const float* hist, float* h
     a.ntok = ntok;
     a.commit_at = commit_at;
     a.eps = eps;
-    gdn::launch_window(a, N, static_cast<cudaStream_t>(stream));
-    return launched("gdn_window_fused");
+    const cudaError_t e = gdn::launch_window(a, N, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "gdn_window_fused: launch failed: %s", cudaGetErrorString(e));
+    g_last_error[0] = '\0';
+    return GDN_OK;
 }
 
 // ------------------------------------------------------------------------------------------------

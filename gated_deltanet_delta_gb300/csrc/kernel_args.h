@@ -111,7 +111,6 @@ struct PrefillMaps {
 };
 
 constexpr int kWinD = 128;       // head dim
-constexpr int kWinHalf = 64;     // columns per CTA
 constexpr int kWinThreads = 128;
 constexpr int kWinMaxTok = 8;
 

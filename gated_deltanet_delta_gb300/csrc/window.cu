@@ -4,10 +4,11 @@
 
 namespace gdn {
 
-// Two CTAs (a cluster, one per column half) per (sequence, value head).
-void launch_window(const WindowArgs& a, int N, cudaStream_t stream) {
-    const unsigned grid = 2u * unsigned(N) * unsigned(a.h_v);
+// One CTA per (sequence, value head); registers hold two per SM.
+cudaError_t launch_window(const WindowArgs& a, int N, cudaStream_t stream) {
+    const unsigned grid = unsigned(N) * unsigned(a.h_v);
     gdn_window_kernel<<<grid, kWinThreads, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

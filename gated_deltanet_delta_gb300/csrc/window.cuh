@@ -11,24 +11,20 @@
 // The state and the conv history are written after token commit_at (commit 1: the last token;
 // 0x100|k: token k; 0: never).
 //
-// GB300 mapping.  A CTA of 128 threads owns one (n, h) head's 128 x 64 half of the state (columns
-// 64*half ..); each warp owns 16 whole columns: lane (column group cl, row block rb) holds 4 columns
-// of the 16 rows 16rb .. 16rb+15 in registers for the whole window, so the 64 KB head state is read
-// from HBM once and written at most once.  Both reductions over the 128 rows (kv and o) are a
-// register sum plus three xor-shuffles inside the warp, so a token needs one barrier (after the conv
-// outputs are written; the per-token buffers are double-buffered by token parity).  The kernel is
-// bound by instruction issue and latency, not memory, so the per-element work is three packed
-// f32x2 FMAs per two elements and token: the state is held as c * R with a per-head scalar c (the
-// gate multiplies c; R += k (rk delta / c) is the rank-1 update; c is folded back into R when it
-// drops below 2^-40), and the q/k norms are applied to reduced sums.  The two halves of a head form
-// a thread-block cluster of 2: the output RMSNorm needs sum_j o_j^2 over all 128 columns, so each
-// half keeps its o_t and partial sums for every token in shared memory and the pair exchanges the
-// partial sums once, through distributed shared memory, after the last token.  Each CTA convolves
-// the 256 q/k channels of key head hk and its own 64 v channels (thread t: q channel t, k channel
-// t, v channel t < 64), with histories and taps in registers, a token ahead of their use.
+// GB300 mapping.  A CTA of 128 threads owns one (n, h) head: lane (column group cg, row block rb)
+// of warp w holds the 4 columns 32w + 4cg .. of the 32 rows 32rb .. 32rb+31 in registers for the
+// whole window, so the 64 KB head state is read from HBM once and written at most once.  Both
+// reductions over the 128 rows (kv and o) are a register sum plus two xor-shuffles inside the warp,
+// so a token needs one barrier (after the conv outputs are written; the per-token buffers are
+// double-buffered by token parity).  The kernel is bound by instruction issue and latency, not
+// memory, so the per-element work is three packed f32x2 FMAs per two elements and token, and the
+// per-token scalar work (conv, norms, gates) is shared by 128 state elements per thread: the state
+// is held as c * R with a per-head scalar c (the gate multiplies c; R += k (rk delta / c) is the
+// rank-1 update; c is folded back into R when it drops below 2^-40), and the q/k norms are applied
+// to reduced sums.  Each thread convolves q and k channel t of key head hk and v channel t of its
+// value head, with histories and taps in registers, a token ahead of their use; the gated RMSNorm
+// reads the head's outputs of every token from shared memory after the last token.
 #pragma once
-
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernel_args.h"
@@ -53,43 +49,39 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
-    gdn_window_kernel(const WindowArgs a) {
-    namespace cg = cooperative_groups;
-    constexpr int D = kWinD, NR = 16;  // rows per lane
-    static_assert(kWinThreads == 128 && kWinHalf == 64, "window tile");
+__global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const WindowArgs a) {
+    constexpr int D = kWinD, NR = 32;  // rows per lane
+    static_assert(kWinThreads == 128 && D == 128, "window tile");
 
-    // per-token buffers, double-buffered by token parity: one barrier per token
-    // q and k of a token by row block of 16, padded to a stride of 20 floats so that the eight row
-    // blocks a warp reads at once fall in different banks
-    constexpr int RBS = 20;
-    __shared__ __align__(16) float qraw[2][8 * RBS];
-    __shared__ __align__(16) float kraw[2][8 * RBS];
-    __shared__ __align__(16) float vraw[2][kWinHalf];
+    // per-token buffers, double-buffered by token parity: one barrier per token.  q and k of a
+    // token by row block of 32, padded to a stride of 36 floats so that the four row blocks a warp
+    // reads at once fall in different banks
+    constexpr int RBS = 36;
+    __shared__ __align__(16) float qraw[2][4 * RBS];
+    __shared__ __align__(16) float kraw[2][4 * RBS];
+    __shared__ __align__(16) float vraw[2][D];
     __shared__ float part_q[2][4], part_k[2][4];
     __shared__ float gates[kWinMaxTok][2];  // gate and beta of every token, computed up front
-    __shared__ __align__(16) float osm[kWinMaxTok][kWinHalf];
+    __shared__ __align__(16) float osm[kWinMaxTok][D];
     __shared__ float ssw[kWinMaxTok][4];  // per-warp sums of o^2
     __shared__ float ss[kWinMaxTok];
-    __shared__ float zs[kWinMaxTok * kWinHalf];  // the epilogue's z and gamma, fetched up front
-    __shared__ float gs[kWinThreads];
+    __shared__ float zs[kWinMaxTok * D];  // the epilogue's z and gamma, fetched up front
+    __shared__ float gs[D];
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const int half = int(cluster.block_rank());
-    const int unit = blockIdx.x >> 1;  // n * h_v + h
+    const int unit = blockIdx.x;  // n * h_v + h
     const int h = unit % a.h_v;
     const int n = unit / a.h_v;
     const int hk = h % a.h_k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cl = lane & 3;           // column group inside the warp
-    const int rb = lane >> 2;          // block of 16 rows
-    const int col = 16 * warp + 4 * cl;  // first of this lane's 4 columns inside the half
+    const int cg = lane & 7;              // column group inside the warp
+    const int rb = lane >> 3;             // block of 32 rows
+    const int col = 32 * warp + 4 * cg;   // first of this lane's 4 columns
     const int C = (2 * a.h_k + a.h_v) * D;
     const int ntok = a.ntok;
 
-    // ---- the state: rows 16rb .. 16rb+15, columns half*64 + col .. +3, held as cs * R
+    // ---- the state: rows 32rb .. 32rb+31, columns col .. col+3, held as cs * R
     const size_t row_stride = size_t(a.h_v) * D;
-    float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + half * kWinHalf + col;
+    float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + col;
     // packed along rows: R[p][j] = (S[2p][j], S[2p+1][j]) of this lane's rows and 4 columns, so that
     // the per-row k and q pairs come straight from float4 loads
     float2 R[NR / 2][4];
@@ -104,42 +96,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
     }
     float cs = 1.0f;
 
-    // ---- this thread's conv channels: q and k of key head hk, and (tid < 64) one v channel
+    // ---- this thread's conv channels: q, k of key head hk and v of value head h, channel tid
     const int ch_q = hk * D + tid;
     const int ch_k = (a.h_k + hk) * D + tid;
-    const bool has_v = tid < kWinHalf;
-    const int ch_v = (2 * a.h_k + h) * D + half * kWinHalf + (tid & (kWinHalf - 1));
+    const int ch_v = (2 * a.h_k + h) * D + tid;
     const float* hist_n = a.hist + size_t(n) * C * 3;
     float hq[3], hk3[3], hv[3];
 #pragma unroll
     for (int e = 0; e < 3; ++e) {
         hq[e] = hist_n[size_t(ch_q) * 3 + e];
         hk3[e] = hist_n[size_t(ch_k) * 3 + e];
-        hv[e] = has_v ? hist_n[size_t(ch_v) * 3 + e] : 0.f;
+        hv[e] = hist_n[size_t(ch_v) * 3 + e];
     }
     const float4 wq = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_q) * 4);
     const float4 wk = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_k) * 4);
-    const float4 wv = has_v ? *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_v) * 4)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool own_qk = h < a.h_k;  // q/k history: head h == hk owns it (half 0: q, half 1: k)
+    const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_v) * 4);
+    const bool own_qk = h < a.h_k;  // the q/k history of key head hk is written by head h == hk
     const float dth = a.dt[h], ssm = a.ssm_a[h];
     const float* x_n = a.qkv + size_t(n) * ntok * C;
-    float xq = x_n[ch_q], xk = x_n[ch_k], xv = has_v ? x_n[ch_v] : 0.f;
+    float xq = x_n[ch_q], xk = x_n[ch_k], xv = x_n[ch_v];
     // every token's gate and beta (thread t), read after the first token's barrier
     if (tid < ntok) {
         const size_t gi = (size_t(n) * ntok + tid) * a.h_v + h;
         gates[tid][0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
         gates[tid][1] = sigmoid_f32(a.beta[gi]);
     }
-    // the epilogue's z (this thread's items tid + 128 i) and gamma, copied asynchronously now
+    // the epilogue's z (token i, column tid) and gamma, copied asynchronously now
 #pragma unroll
-    for (int i = 0; i < kWinMaxTok / 2; ++i) {
-        const int idx = tid + kWinThreads * i;
-        const int t = idx / kWinHalf, j = idx % kWinHalf;
-        if (t < ntok)
-            cp_async4(&zs[idx], a.z + ((size_t(n) * ntok + t) * a.h_v + h) * D + half * kWinHalf + j);
-    }
-    cp_async4(&gs[tid], a.gamma + half * kWinHalf + (tid & (kWinHalf - 1)));
+    for (int i = 0; i < kWinMaxTok; ++i)
+        if (i < ntok) cp_async4(&zs[i * D + tid], a.z + ((size_t(n) * ntok + i) * a.h_v + h) * D + tid);
+    cp_async4(&gs[tid], a.gamma + tid);
 
     for (int t = 0; t < ntok; ++t) {
         const int b = t & 1;
@@ -148,7 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
             const float* xn = x_n + size_t(t + 1) * C;
             nq = xn[ch_q];
             nk = xn[ch_k];
-            nv = has_v ? xn[ch_v] : 0.f;
+            nv = xn[ch_v];
         }
         // conv + SiLU, history shift, committed history
         const float cq = silu_f32(fmaf(xq, wq.w, fmaf(hq[2], wq.z, fmaf(hq[1], wq.y, hq[0] * wq.x))));
@@ -160,22 +146,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         if (t + 1 == a.commit_at) {
             float* ho = a.hist_out + size_t(n) * C * 3;
             if (own_qk) {
-                const int ch = half == 0 ? ch_q : ch_k;
-                const float* hh = half == 0 ? hq : hk3;
-                ho[size_t(ch) * 3 + 0] = hh[0];
-                ho[size_t(ch) * 3 + 1] = hh[1];
-                ho[size_t(ch) * 3 + 2] = hh[2];
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    ho[size_t(ch_q) * 3 + e] = hq[e];
+                    ho[size_t(ch_k) * 3 + e] = hk3[e];
+                }
             }
-            if (has_v) {
-                ho[size_t(ch_v) * 3 + 0] = hv[0];
-                ho[size_t(ch_v) * 3 + 1] = hv[1];
-                ho[size_t(ch_v) * 3 + 2] = hv[2];
-            }
+#pragma unroll
+            for (int e = 0; e < 3; ++e) ho[size_t(ch_v) * 3 + e] = hv[e];
         }
         xq = nq; xk = nk; xv = nv;
-        qraw[b][(tid >> 4) * RBS + (tid & 15)] = cq;
-        kraw[b][(tid >> 4) * RBS + (tid & 15)] = ck;
-        if (has_v) vraw[b][tid] = cv;
+        qraw[b][(tid >> 5) * RBS + (tid & 31)] = cq;
+        kraw[b][(tid >> 5) * RBS + (tid & 31)] = ck;
+        vraw[b][tid] = cv;
         const float sq = group_sum<32>(cq * cq);
         const float sk = group_sum<32>(ck * ck);
         if (lane == 0) {
@@ -184,15 +167,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
         }
         __syncthreads();
 
-        // everything below is warp-local: the warp owns 16 whole columns
+        // everything below is warp-local: the warp owns 32 whole columns
         const float rk = rsqrtf(((part_k[b][0] + part_k[b][1]) + (part_k[b][2] + part_k[b][3])) + a.eps);
         const float rq = rsqrtf(((part_q[b][0] + part_q[b][1]) + (part_q[b][2] + part_q[b][3])) + a.eps);
         const float gate = gates[t][0], beta = gates[t][1];
         const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * RBS);
         const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * RBS);
 
-        // kv = cs rk sum_i R_ij k_i: 16 rows in registers (as 8 row pairs), then the 8 row blocks
-        // by shuffles
+        // kv = cs rk sum_i R_ij k_i: 32 rows in registers (as 16 row pairs), then the 4 row blocks
+        // by two shuffles
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
 #pragma unroll
@@ -209,7 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
 #pragma unroll
         for (int j = 0; j < 4; ++j) kvs[j] = acc[j].x + acc[j].y;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1)
+        for (int o = 8; o < 32; o <<= 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) kvs[j] += __shfl_xor_sync(kFullMask, kvs[j], o);
         const float4 vv = *reinterpret_cast<const float4*>(vraw[b] + col);
@@ -262,36 +245,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWinThreads, 4)
 #pragma unroll
         for (int j = 0; j < 4; ++j) os[j] = oacc[j].x + oacc[j].y;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1)
+        for (int o = 8; o < 32; o <<= 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) os[j] += __shfl_xor_sync(kFullMask, os[j], o);
         const float sc = cs * rq * 0.08838834764831845f;  // cs rq / sqrt(128)
         const float4 ot = make_float4(os[0] * sc, os[1] * sc, os[2] * sc, os[3] * sc);
+        // lanes 0 .. 7 (row block 0) hold the warp's 32 outputs
         float e = rb == 0 ? ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w : 0.f;
         if (rb == 0) *reinterpret_cast<float4*>(&osm[t][col]) = ot;
         e += __shfl_xor_sync(kFullMask, e, 1);
         e += __shfl_xor_sync(kFullMask, e, 2);
+        e += __shfl_xor_sync(kFullMask, e, 4);
         if (lane == 0) ssw[t][warp] = e;
     }
     cp_async_wait_all();  // this thread's z and gamma (read only by this thread)
     __syncthreads();
     if (tid < ntok) ss[tid] = (ssw[tid][0] + ssw[tid][1]) + (ssw[tid][2] + ssw[tid][3]);
-
-    // the gated RMSNorm needs both halves' sums of o^2: exchange them once through the cluster
-    cluster.sync();
-    const float* peer_ss = cluster.map_shared_rank(ss, half ^ 1);
+    __syncthreads();
+    // the gated RMSNorm over the head's 128 outputs of each token
 #pragma unroll
-    for (int i = 0; i < kWinMaxTok / 2; ++i) {
-        const int idx = tid + kWinThreads * i;
-        const int t = idx / kWinHalf, j = idx % kWinHalf;
-        if (t < ntok) {
-            const float tot = ss[t] + peer_ss[t];
-            const float rs = rsqrtf(tot / float(D) + a.eps);
-            const size_t yi = ((size_t(n) * ntok + t) * a.h_v + h) * D + half * kWinHalf + j;
-            a.y[yi] = osm[t][j] * rs * gs[tid] * sigmoid_f32(zs[idx]);
+    for (int i = 0; i < kWinMaxTok; ++i) {
+        if (i < ntok) {
+            const float rs = rsqrtf(ss[i] / float(D) + a.eps);
+            const size_t yi = ((size_t(n) * ntok + i) * a.h_v + h) * D + tid;
+            a.y[yi] = osm[i][tid] * rs * gs[tid] * sigmoid_f32(zs[i * D + tid]);
         }
     }
-    cluster.sync();  // the peer has read this CTA's sums before it exits
 }
 
 }  // namespace gdn
