@@ -28,6 +28,8 @@ GDN_DECODE_TINY = dict(name="gdn decode B1 Hk2 Hv4 D64", B=1, Hk=2, Hv=4, Dk=64,
 GDN_DECODE_BATCHED = dict(name="gdn decode B64 Hk16 Hv32 D128", B=64, Hk=16, Hv=32, Dk=128, Dv=128,
                           warmup=16, steps=100)
 COMBA_DECODE = dict(name="comba decode B256 H32 K128 V128", B=256, H=32, K=128, V=128, warmup=16)
+# the Comba forward over T tokens per call on the decode workload's heads
+COMBA_FORWARD = dict(name="comba forward B256 T8 H32 K128 V128", B=256, T=8, H=32, K=128, V=128)
 GDN_PREFILL = dict(name="gdn chunked prefill T15360 (4096+2048+1024+8192) Hk16 Hv32 K128 V128 C64",
                    seqlens=(4096, 2048, 1024, 8192), Hk=16, Hv=32, K=128, V=128, pool=16, chunk=64)
 GDN_WINDOW = dict(name="gdn fused window N32 h_k16 h_v48 D128 ntok8", N=32, h_k=16, h_v=48, D=128,
@@ -93,6 +95,19 @@ def comba_decode_token(g: np.random.Generator, B: int, H: int, K: int, V: int) -
     beta = bf16_round(_sigmoid(g.random((B, H), dtype=np.float32)))
     g_log = (_logsigmoid(_randn(g, (B, H))) / np.float32(4.0)).astype(np.float32)
     return dict(q=q, k=k, v=v, p=p, beta=beta, g_log=g_log)
+
+
+def comba_forward_inputs(g: np.random.Generator, B: int, T: int, H: int, K: int, V: int) -> dict:
+    """T tokens of Comba inputs per sequence (each token drawn as comba_decode_token draws one) and
+    an initial state: q,k,p [B,T,H,K] bf16; v [B,T,H,V] bf16; beta, g_log [B,T,H];
+    state [B,H,K,V] fp32 = 0.05 randn."""
+    toks = [comba_decode_token(g, B, H, K, V) for _ in range(T)]
+    x = {n: np.ascontiguousarray(np.stack([t[n] for t in toks], axis=1)) for n in toks[0]} if T else \
+        dict(q=np.zeros((B, 0, H, K), np.float32), k=np.zeros((B, 0, H, K), np.float32),
+             v=np.zeros((B, 0, H, V), np.float32), p=np.zeros((B, 0, H, K), np.float32),
+             beta=np.zeros((B, 0, H), np.float32), g_log=np.zeros((B, 0, H), np.float32))
+    x["state"] = (_randn(g, (B, H, K, V)) * np.float32(0.05)).astype(np.float32)
+    return x
 
 
 # ------------------------------------------------------------------------------------------------

@@ -61,6 +61,8 @@ def _load():
             lib.oracle_comba_decode_head.restype = None
             lib.oracle_comba_decode.argtypes = [i, i, i, i, D, D, D, D, D, D, D, d, D, D]
             lib.oracle_comba_decode.restype = i
+            lib.oracle_comba_forward.argtypes = [i, i, i, i, i, D, D, D, D, D, D, D, d, D, D]
+            lib.oracle_comba_forward.restype = i
             lib.oracle_gdn_prefill_unit.argtypes = [l, i, i, i, i, i, D, D, D, D, D, d, d, d, d, D, D]
             lib.oracle_gdn_prefill_unit.restype = None
             lib.oracle_gdn_prefill.argtypes = [i, I64, I64, i, l, i, i, i, i, D, D, D, D, D, D, D,
@@ -115,6 +117,20 @@ def comba_decode(state, q, k, v, p, beta, g_log, scale: float):
                                        _p(beta), _p(g_log), float(scale), _p(state_new), _p(o)),
            "comba_decode")
     return state_new, o
+
+
+def comba_forward(state, q, k, v, p, beta, g_log, scale: float):
+    """T Comba steps per head: state [B,H,K,V]; q,k,p [B,T,H,K]; v [B,T,H,V]; beta,g_log [B,T,H].
+    Returns (final state [B,H,K,V], o [B,T,H,V])."""
+    state, q, k, v, p, beta, g_log = map(_f64, (state, q, k, v, p, beta, g_log))
+    B, H, K, V = state.shape
+    T = q.shape[1]
+    state_out = np.empty_like(state)
+    o = np.empty((B, T, H, V))
+    _check(_load().oracle_comba_forward(B, T, H, K, V, _p(state), _p(q), _p(k), _p(v), _p(p),
+                                        _p(beta), _p(g_log), float(scale), _p(state_out), _p(o)),
+           "comba_forward")
+    return state_out, o
 
 
 # ------------------------------------------------------------------------------------------------

@@ -112,6 +112,28 @@ int oracle_comba_decode(int B, int H, int K, int V, const double* state, const d
 }
 
 /* ------------------------------------------------------------------------------------------------ */
+/* Comba forward over T tokens.  [comba spec] spec_md: the decode step is the comba-forward task's   */
+/* recurrence run for one token, and running the step T times reproduces that task; so each (b, h)  */
+/* head carries its state through oracle_comba_decode_head once per token, in token order.           */
+/* ------------------------------------------------------------------------------------------------ */
+int oracle_comba_forward(int B, int T, int H, int K, int V, const double* state, const double* q,
+                         const double* k, const double* v, const double* p, const double* beta,
+                         const double* g_log, double scale, double* state_out, double* o) {
+    if (B < 0 || T < 0 || H <= 0 || K <= 0 || V <= 0) return ORACLE_EINVAL;
+    for (long b = 0; b < B; ++b)
+        for (long h = 0; h < H; ++h) {
+            double* S = state_out + (b * H + h) * K * V;
+            memcpy(S, state + (b * H + h) * K * V, sizeof(double) * (size_t)K * (size_t)V);
+            for (long t = 0; t < T; ++t) {
+                const long n = (b * T + t) * H + h; /* token t of head (b, h) */
+                oracle_comba_decode_head(K, V, S, q + n * K, k + n * K, v + n * V, p + n * K, beta[n],
+                                         g_log[n], scale, S, o + n * V);
+            }
+        }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------------------ */
 /* Prefill: the sequential recurrence over the tokens of one sequence, one value head.               */
 /* Per token ([gdn_chunkwise] gdn_extend_chunkwise parameters; gate form as in [gdn.metal] header):  */
 /*   log g = -exp(A_log) softplus(a + dt_bias);  g = exp(log g);  beta = sigmoid(b);                 */

@@ -56,6 +56,13 @@ int oracle_comba_decode(int B, int H, int K, int V, const double* state, const d
                         const double* k, const double* v, const double* p, const double* beta,
                         const double* g_log, double scale, double* state_new, double* o);
 
+/* Comba forward over T tokens, [comba spec] spec_md ("running this step T times reproduces" the
+ * comba-forward task): state [B][H][K][V] in, state_out [B][H][K][V] out (no aliasing);
+ * q,k,p [B][T][H][K], v,o [B][T][H][V], beta,g_log [B][T][H]. */
+int oracle_comba_forward(int B, int T, int H, int K, int V, const double* state, const double* q,
+                         const double* k, const double* v, const double* p, const double* beta,
+                         const double* g_log, double scale, double* state_out, double* o);
+
 /* Sequential prefill of one (sequence, value head) unit: the recurrence that the chunkwise WY form
  * reproduces ([gdn_chunkwise] module doc), with the gates derived from the raw inputs
  * ([gdn_chunkwise] gdn_extend_chunkwise parameters a, b, A_log, dt_bias).
