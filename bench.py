@@ -62,6 +62,12 @@ def comba_bytes(B, H, K, V):
     return 2 * B * H * K * V * 4 + B * H * (6 * K + 4 * V + 6)
 
 
+def comba_forward_bytes(B, T, H, K, V):
+    """State read and written once; per token q, k, p, v, beta (bf16), g (f32) read and o (bf16)
+    written."""
+    return 2 * B * H * K * V * 4 + B * T * H * (3 * K * 2 + V * 2 + 2 + 4 + V * 2)
+
+
 def prefill_bytes(seqlens, Hk, Hv, K, V):
     T, n = sum(seqlens), len(seqlens)
     return (2 * T * Hk * K * 2 + T * Hv * V * 2 + 2 * T * Hv * 2 + T * Hv * V * 2
@@ -406,6 +412,25 @@ def bench_comba(torch, gdn, dist, steps, warmup, seed):
     return dict(secs=secs, alg_bytes=comba_bytes(B, H, K, V), shape=(B, H, K, V))
 
 
+def bench_comba_forward(torch, gdn, dist, steps, warmup, seed):
+    c = gi.COMBA_FORWARD
+    B, T, H, K, V = c["B"], c["T"], c["H"], c["K"], c["V"]
+    x = gi.comba_forward_inputs(gi.rng(seed + 5), B, T, H, K, V)
+    dev = torch.device("cuda")
+    b16, f32 = torch.bfloat16, torch.float32
+    d = {n: torch.from_numpy(x[n]).to(dt).to(dev) for n, dt in
+         (("q", b16), ("k", b16), ("v", b16), ("p", b16), ("beta", b16), ("g_log", f32), ("state", f32))}
+    o = torch.empty((B, T, H, V), dtype=b16, device=dev)
+
+    def step(i):  # the 537 MB state is larger than L2; it is carried from call to call
+        gdn.comba_forward(d["state"], d["q"], d["k"], d["v"], d["p"], d["beta"], d["g_log"], o=o)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, alg_bytes=comba_forward_bytes(B, T, H, K, V), B=B, T=T, H=H)
+
+
 def bench_prefill(torch, gdn, dist, steps, warmup, seed, dtype="bf16"):
     c = gi.GDN_PREFILL
     Hk, Hv, K, V, C = c["Hk"], c["Hv"], c["K"], c["V"], c["chunk"]
@@ -509,6 +534,7 @@ def main_single_op(args, torch, gdn, dist, seed):
     fns = {
         "decode": lambda: bench_decode(torch, gdn, dist, args.steps, args.warmup, seed),
         "comba": lambda: bench_comba(torch, gdn, dist, args.steps, args.warmup, seed),
+        "comba_forward": lambda: bench_comba_forward(torch, gdn, dist, args.steps, args.warmup, seed),
         "prefill": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed),
         "prefill_f16": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed, "f16"),
         "window_verify": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, False),
@@ -532,7 +558,7 @@ def main():
     ap.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline (rank 0, N=1)")
-    ap.add_argument("--op", choices=("decode", "comba", "prefill", "prefill_f16", "window_verify", "window_commit",
+    ap.add_argument("--op", choices=("decode", "comba", "comba_forward", "prefill", "prefill_f16", "window_verify", "window_commit",
                                      "decode_multi", "decode_pooled"),
                     help="time only this operation on its workload and print its time per call "
                          "(for profiling; not the benchmark line)")
@@ -576,6 +602,9 @@ def main():
                          ("decode_multi", lambda: bench_decode_multi(torch, gdn, dist, args.steps,
                                                                      args.warmup, seed)),
                          ("decode_pooled", lambda: bench_decode_pooled(torch, gdn, dist, args.steps,
+                                                                       args.warmup, seed)),
+                         ("comba_forward", lambda: bench_comba_forward(torch, gdn, dist,
+                                                                       max(3, args.steps // 5),
                                                                        args.warmup, seed)),
                          ("comba_sweep", lambda: bench_comba_sweep(torch, gdn, dist,
                                                                    max(3, args.steps // 5),
@@ -667,6 +696,17 @@ def main():
             "unit": "GB/s", "us_per_step": t1 * 1e6,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+    cf = extra.get("comba_forward", {})
+    if "secs" in cf:
+        t1 = cf["secs"] / max(3, K // 5)
+        gbs = cf["alg_bytes"] / t1 / 1e9
+        ops["comba_forward"] = {
+            "workload": gi.COMBA_FORWARD["name"], "value": N * cf["B"] * cf["H"] * cf["T"] / t1,
+            "unit": "head-token steps/s", "us_per_call": t1 * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+    elif "comba_forward" in extra:
+        ops["comba_forward"] = cf
     if isinstance(extra.get("comba_sweep"), list):
         ksw = max(3, args.steps // 5)
         rows = []

@@ -23,7 +23,8 @@ STATUS_BAD_CACHE_INDEX = 1
 STATUS_BAD_SEQLENS = 2
 
 # Every symbol that include/gdn.h declares.
-ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "gdn_prefill_workspace_size",
+ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "comba_forward",
+               "gdn_prefill_workspace_size",
                "gdn_prefill_chunked", "gdn_prefill_chunked_f16", "gdn_prefill_chunked_noalloc", "gdn_window_fused",
                "gdn_status_string", "gdn_last_error")
 
@@ -60,6 +61,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_decode_step_pooled.restype = I
         lib.comba_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.comba_decode_step.restype = I
+        lib.comba_forward.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.comba_forward.restype = I
         lib.gdn_prefill_workspace_size.argtypes = [I, I64, I, I, I, I, I]
         lib.gdn_prefill_workspace_size.restype = SZ
         lib.gdn_prefill_chunked.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I, I, I,
@@ -243,6 +246,30 @@ def comba_decode_step(state, q, k, v, p, beta, g, scale=None, state_new=None, o=
                                     _ptr(p), _ptr(beta), _ptr(g), _ptr(o), _out_code(o.dtype), B, H,
                                     K, V, scale, _stream(state.device)), "comba_decode_step")
     return state_new, o
+
+
+def comba_forward(state, q, k, v, p, beta, g, scale=None, o=None, o_dtype=None):
+    """The Comba recurrence over T tokens.  state f32 [B,H,K,V] (updated in place); q,k,p bf16
+    [B,T,H,K]; v bf16 [B,T,H,V]; beta bf16 [B,T,H]; g f32 [B,T,H] (log-decay).  Returns o
+    [B,T,H,V] (bf16 unless o / o_dtype say float32); scale defaults to K^-0.5."""
+    torch = _torch()
+    B, H, K, V = state.shape
+    T = q.shape[1]
+    _want(state, "state", torch.float32)
+    _want(q, "q", torch.bfloat16, (B, T, H, K))
+    _want(k, "k", torch.bfloat16, (B, T, H, K))
+    _want(p, "p", torch.bfloat16, (B, T, H, K))
+    _want(v, "v", torch.bfloat16, (B, T, H, V))
+    _want(beta, "beta", torch.bfloat16, (B, T, H))
+    _want(g, "g", torch.float32, (B, T, H))
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=o_dtype or torch.bfloat16, device=state.device)
+    _want(o, "o", o.dtype, (B, T, H, V))
+    scale = K ** -0.5 if scale is None else float(scale)
+    _check(load().comba_forward(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(p), _ptr(beta), _ptr(g),
+                                _ptr(o), _out_code(o.dtype), B, T, H, K, V, scale,
+                                _stream(state.device)), "comba_forward")
+    return o
 
 
 def gdn_prefill_workspace_size(num_seqs: int, T: int, Hk: int, Hv: int, K: int, V: int,

@@ -262,6 +262,47 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
     return launched("comba_decode_step");
 }
 
+gdn_status comba_forward(float* state, const void* q, const void* k, const void* v, const void* p,
+                         const void* beta, const float* g, void* o, gdn_dtype o_dtype, int B, int T, int H,
+                         int K, int V, float scale, gdn_stream_t stream) {
+    REQUIRE(B >= 0 && T >= 0 && H >= 1 && K >= 1 && V >= 1, GDN_ERR_INVALID_ARG,
+            "comba_forward: sizes must be B, T >= 0 and H, K, V >= 1 (got B=%d T=%d H=%d K=%d V=%d)", B, T, H,
+            K, V);
+    REQUIRE(o_dtype == GDN_BF16 || o_dtype == GDN_F32, GDN_ERR_INVALID_ARG,
+            "comba_forward: o_dtype must be GDN_BF16 or GDN_F32");
+    REQUIRE((K == 64 || K == 128) && (V == 64 || V == 128), GDN_ERR_UNSUPPORTED,
+            "comba_forward: K and V must each be 64 or 128 (got K=%d V=%d)", K, V);
+    if (B == 0) return GDN_OK;
+    REQUIRE(state, GDN_ERR_INVALID_ARG, "comba_forward: null state");
+    REQUIRE(T == 0 || (q && k && v && p && beta && g && o), GDN_ERR_INVALID_ARG, "comba_forward: null pointer");
+    REQUIRE(aligned(state, 16), GDN_ERR_INVALID_ARG, "comba_forward: state must be 16-byte aligned");
+    REQUIRE(aligned(q, 8) && aligned(k, 8) && aligned(p, 8) && aligned(v, 8), GDN_ERR_INVALID_ARG,
+            "comba_forward: q, k, p and v must be 8-byte aligned");
+    REQUIRE(aligned(o, o_dtype == GDN_F32 ? 16 : 8) && aligned(beta, 2) && aligned(g, 4), GDN_ERR_INVALID_ARG,
+            "comba_forward: misaligned o, beta or g");
+    const size_t sbytes = size_t(B) * H * K * V * sizeof(float);
+    const size_t ob = size_t(B) * T * H * V * (o_dtype == GDN_F32 ? 4 : 2);
+    REQUIRE(!any_overlap(o, ob, state, sbytes), GDN_ERR_INVALID_ARG, "comba_forward: o overlaps state");
+    REQUIRE((long long)B * H < (1LL << 31) && (long long)B * T * H * (K > V ? K : V) < (1LL << 62),
+            GDN_ERR_UNSUPPORTED, "comba_forward: sizes too large");
+
+    gdn::CombaFwdArgs a;
+    a.state = state;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.p = static_cast<const uint16_t*>(p);
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.g = g;
+    a.o = o;
+    a.o_f32 = o_dtype == GDN_F32;
+    a.T = T;
+    a.H = H;
+    a.scale = scale;
+    gdn::launch_comba_forward(a, B * H, K, V, static_cast<cudaStream_t>(stream));
+    return launched("comba_forward");
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------------------

@@ -56,6 +56,22 @@ struct CombaArgs {
     float scale;
 };
 
+// The Comba recurrence over T tokens per head: q, k, p [B, T, H, K], v [B, T, H, V], beta [B, T, H]
+// (bf16), g [B, T, H] (fp32 log-decay), o [B, T, H, V]; state [B, H, K, V] fp32, updated in place.
+struct CombaFwdArgs {
+    float* state;
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const uint16_t* p;
+    const uint16_t* beta;
+    const float* g;
+    void* o;
+    int o_f32;
+    int T, H;
+    float scale;
+};
+
 struct WindowArgs {
     float* state;
     const float* hist;

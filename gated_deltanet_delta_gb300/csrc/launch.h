@@ -12,6 +12,7 @@ namespace gdn {
 void launch_decode(DecodeArgs a, int B, int Dk, cudaStream_t stream);
 void launch_decode_multi(DecodeMultiArgs a, int B, int Dk, cudaStream_t stream);
 void launch_comba(const CombaArgs& a, int heads, int K, int V, cudaStream_t stream);
+void launch_comba_forward(const CombaFwdArgs& a, int heads, int K, int V, cudaStream_t stream);
 cudaError_t launch_window(const WindowArgs& a, int N, cudaStream_t stream);
 // Raises the kernel's shared-memory limit once per device, then launches; returns the launch error.
 // The prefill workspace: the chunk offsets (8 bytes per sequence + 1, padded to 16 bytes) and the

@@ -7,6 +7,7 @@
  *   gdn_decode_step_pooled  the same on a pooled state indexed by cache_indices
  *   gdn_decode_multi     T consecutive decode steps with the state held on chip
  *   comba_decode_step    one-token Comba step (state read with key p, written with key k)
+ *   comba_forward        the Comba recurrence over T tokens with the state held on chip
  *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
  *   gdn_prefill_chunked_f16  the same with IEEE binary16 token arrays
  *   gdn_prefill_chunked_noalloc  the same with the library's own fixed-size workspace
@@ -144,6 +145,29 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
                              const void* v, const void* p, const void* beta, const float* g,
                              void* o, gdn_dtype o_dtype, int B, int H, int K, int V, float scale,
                              gdn_stream_t stream);
+
+/*
+ * comba_forward -- the Comba recurrence over T consecutive tokens of each of B sequences.
+ * [comba spec] spec_md: the decode step is the comba-forward task's recurrence run for one token,
+ * and running it T times reproduces that task.  Per (b, h) head and token t, exactly the
+ * comba_decode_step arithmetic on the state carried from token t - 1:
+ *     S = exp(g_t) S;  u_j = beta_t (v_j - sum_i p_i S_ij);  S_ij += k_i u_j;
+ *     o_t,j = sum_i (scale q_i) S_ij.
+ *
+ *   state      f32  [B, H, K, V]   V contiguous; the initial state, overwritten IN PLACE with the
+ *                                  state after the last token (left as given when T = 0)
+ *   q, k, p    bf16 [B, T, H, K]   k writes the state, p reads it
+ *   v          bf16 [B, T, H, V]
+ *   beta       bf16 [B, T, H]
+ *   g          f32  [B, T, H]      log-decay (the gate is exp(g))
+ *   o          [B, T, H, V] of o_dtype (GDN_BF16 round to nearest even, or GDN_F32); must not
+ *              overlap state
+ * Supported: K, V in {64, 128}.  The state is read once and written once per call; all arithmetic
+ * is f32.
+ */
+gdn_status comba_forward(float* state, const void* q, const void* k, const void* v, const void* p,
+                         const void* beta, const float* g, void* o, gdn_dtype o_dtype, int B, int T, int H,
+                         int K, int V, float scale, gdn_stream_t stream);
 
 /*
  * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_chunked needs for these

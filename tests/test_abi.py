@@ -122,3 +122,19 @@ def test_prefill_validation(lib, name):
     assert call(ws, need, chunk=32) == gdn.GDN_ERR_UNSUPPORTED and "64 or 128" in gdn.last_error()
     assert call(ws, need, K=64) == gdn.GDN_ERR_UNSUPPORTED
     assert call(N, 0, num_seqs=0) == gdn.GDN_OK
+
+
+def test_comba_forward_validation(lib):
+    f = lib.comba_forward
+    st, o = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 40)
+
+    def call(state=st, K=128, V=128, o_dtype=gdn.GDN_BF16, B=2, T=4, ptr=P, out=o):
+        return f(state, ptr, ptr, ptr, ptr, ptr, ptr, out, o_dtype, B, T, 2, K, V, 0.1, N)
+    assert call(K=96) == gdn.GDN_ERR_UNSUPPORTED and "64 or 128" in gdn.last_error()
+    assert call(o_dtype=7) == gdn.GDN_ERR_INVALID_ARG
+    assert call(state=N) == gdn.GDN_ERR_INVALID_ARG
+    assert call(ptr=N) == gdn.GDN_ERR_INVALID_ARG
+    assert call(state=ctypes.c_void_p((1 << 20) + 4)) == gdn.GDN_ERR_INVALID_ARG      # misaligned
+    assert call(out=ctypes.c_void_p((1 << 20) + 64)) == gdn.GDN_ERR_INVALID_ARG       # o overlaps state
+    assert call(B=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(B=0, state=N, ptr=N, out=N) == gdn.GDN_OK                               # no heads: no-op
