@@ -787,13 +787,18 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             if (i < n_here) o[i * vo_stride] = f32_to_in<F16>(o16[i]);
     };
     // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
-    // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates
+    // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates.
+    // When gamma_L is 0 in fp32 (the chunk's decay underflows) the scaled state is exactly 0: the
+    // pass is skipped and the update overwrites the state instead (uniform over the CTA)
     auto convert_delta = [&](long long c) {
         const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * REC_VEC_BYTES);
+        const float gL = vec[V_GL];
         float d16[16], sa[16], sb16[16];
         tc::ld16(trow + TM_U + (c & 1) * 64 + 16 * qt, d16);
-        tc::ld16(trow + TM_S + 32 * qt, sa);
-        tc::ld16(trow + TM_S + 32 * qt + 16, sb16);
+        if (gL != 0.f) {
+            tc::ld16(trow + TM_S + 32 * qt, sa);
+            tc::ld16(trow + TM_S + 32 * qt + 16, sb16);
+        }
         tc::wait_ld();
 #pragma unroll
         for (int cc2 = 0; cc2 < 2; ++cc2) {
@@ -815,15 +820,16 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             *reinterpret_cast<uint4*>(sm + OFF_DT + tc::sw_chunk(row, cc, 128)) = hi;
             *reinterpret_cast<uint4*>(sm + OFF_DT + 16384 + tc::sw_chunk(row, cc, 128)) = lo;
         }
-        const float gL = vec[V_GL];
-        float lo16[16], hi16[16];
+        if (gL != 0.f) {
+            float lo16[16], hi16[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            lo16[i] = sa[i] * gL;
-            hi16[i] = sb16[i] * gL;
+            for (int i = 0; i < 16; ++i) {
+                lo16[i] = sa[i] * gL;
+                hi16[i] = sb16[i] * gL;
+            }
+            tc::st16(trow + TM_S + 32 * qt, lo16);
+            tc::st16(trow + TM_S + 32 * qt + 16, hi16);
         }
-        tc::st16(trow + TM_S + 32 * qt, lo16);
-        tc::st16(trow + TM_S + 32 * qt + 16, hi16);
     };
 
     if (control) {
@@ -967,11 +973,15 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                                 tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dDL, pa + ks * 32), dadd(dM, pb + ks * 32),
                                              idm, 1u);
                         }
+                        // gamma_L == 0: the decayed state is 0 and the update overwrites it
+                        const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * REC_VEC_BYTES);
+                        const uint32_t keep = vec[V_GL] != 0.f ? 1u : 0u;
 #pragma unroll
                         for (int part = 0; part < 2; ++part)
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
-                                tc::mma_bf16(tm + TM_S, dadd(dDT, part * 16384 + ks * 32), dadd(dK, ks * 2048), ids, 1u);
+                                tc::mma_bf16(tm + TM_S, dadd(dDT, part * 16384 + ks * 32), dadd(dK, ks * 2048), ids,
+                                             (part | ks) != 0 ? 1u : keep);
                         tc::commit(&bars[B_C]);
                         mark(B_C, par);
                     }
