@@ -106,9 +106,9 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 // even feature in the low half), the A operand of P~'s second product
 constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 320, TM_SL = 448;
 constexpr uint32_t TM_COLS = 512;
-// the sequential kernel's threads: 16 worker warps (conversions, outputs) and one control warp
-// (lane 0 issues every MMA and every copy)
-constexpr int NW = 16, NTS = 32 * (NW + 1);
+// the sequential kernel's threads: 16 worker warps (conversions, outputs), one control warp (lane 0
+// issues every MMA) and one producer warp (lane 0 issues every TMA and bulk copy)
+constexpr int NW = 16, NTS = 32 * (NW + 2);
 // its mbarriers: MMA completions (tcgen05.commit), worker hand-offs (one arrival per worker warp)
 // and copies
 enum : int {
@@ -665,6 +665,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     const int hk = h / (a.Hv / a.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == NW;
+    const bool producer = warp == NW + 1;
     const int row = tid & 127;   // workers: the TMEM lane this thread reads and writes
     const int qt = tid >> 7;     // workers: which quarter of the columns
 
@@ -841,33 +842,6 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 inflight |= 1u << i;
                 lastpar = (lastpar & ~(1u << i)) | (parity << i);
             };
-            // k or v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
-            auto fetch_rows = [&](const CUtensorMap* map, int head, long long c, uint32_t dst, int bar,
-                                  uint32_t parity) {
-                const int z = static_cast<int>(bos + c * C);
-                tc::mbar_expect_tx(&bars[bar], 2 * 8192);
-                tc::tma_load_3d(sb + dst, map, 0, head, z, &bars[bar]);
-                tc::tma_load_3d(sb + dst + 8192, map, 64, head, z, &bars[bar]);
-                mark(bar, parity);
-            };
-            // a part of chunk c's record by a bulk copy
-            auto fetch_rec = [&](long long c, uint32_t from, uint32_t bytes, uint32_t dst, int bar, uint32_t parity) {
-                const uint8_t* rec = a.records + ((chunk0 + c) * a.Hv + h) * static_cast<long long>(REC_BYTES);
-                tc::mbar_expect_tx(&bars[bar], bytes);
-                tc::bulk_load(sb + dst, rec + from, bytes, &bars[bar]);
-                mark(bar, parity);
-            };
-            auto fetch_k = [&](long long c) {
-                fetch_rows(&maps.k, hk, c, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
-            };
-            auto fetch_v = [&](long long c) { fetch_rows(&maps.v, h, c, OFF_V, B_V, c & 1); };
-            auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_QT - REC_T4, OFF_T4, B_R1, c & 1); };
-            auto fetch_qt = [&](long long c) { fetch_rec(c, REC_QT, REC_M - REC_QT, OFF_QT, B_QT, c & 1); };
-            auto fetch_rm = [&](long long c) { fetch_rec(c, REC_M, REC_VEC - REC_M, OFF_M, B_RM, c & 1); };
-            auto fetch_rv = [&](long long c) {
-                fetch_rec(c, REC_VEC, REC_VEC_BYTES, OFF_VEC + (c & 1) * REC_VEC_BYTES, B_RV0 + static_cast<int>(c & 1),
-                          (c >> 1) & 1);
-            };
             // W^T = K^T Tw^T and U^T = V^T Tu^T of chunk c (A MN-major from the token tiles)
             auto issue_wu = [&](long long c) {
                 const uint64_t dK = dadd(dK0, (c & 1) * 16384);
@@ -897,22 +871,10 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                        tc::mbar_test(&bars[B_V], c & 1) && tc::mbar_test(&bars[B_R1], c & 1);
             };
 
-            fetch_k(0);
-            fetch_v(0);
-            fetch_r1(0);
-            fetch_qt(0);
-            fetch_rm(0);
-            fetch_rv(0);
-            if (nch > 1) fetch_k(1);
             do {
                 if (!wu_inputs(0)) break;
                 tc::fence_after();
                 issue_wu(0);
-                if (!wait_bar(B_WU, 0)) break;
-                if (nch > 1) {  // U read the v tile, W and U the record part
-                    fetch_v(1);
-                    fetch_r1(1);
-                }
                 for (long long c = 0; c < nch; ++c) {
                     const bool more = c + 1 < nch;
                     const uint32_t par = c & 1;
@@ -951,15 +913,13 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         issue_wu(c + 1);
                         wu_done = true;
                     }
-                    if (!wait_bar(B_A, par)) break;
-                    if (more) fetch_qt(c + 1);  // P~ read Q~
+                    // ---- C. O^T = P~^T + Delta^T M~^T (three hi / lo products) and S += Delta~^T K
+                    if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
                     if (!wu_done && wu_ready_now(c + 1)) {
                         tc::fence_after();
                         issue_wu(c + 1);
                         wu_done = true;
                     }
-                    // ---- C. O^T = P~^T + Delta^T M~^T (three hi / lo products) and S += Delta~^T K
-                    if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
                     tc::fence_after();
                     {
                         const uint32_t idm = tc::idesc_bf16(128, 64, 0, 0, 0);
@@ -990,7 +950,70 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         tc::fence_after();
                         issue_wu(c + 1);
                     }
+                }
+            } while (false);
+            if (abort_flag) {  // give what is still in flight one more bounded wait
+                for (int i = 0; i < NBAR; ++i)
+                    if (inflight & (1u << i)) tc::mbar_wait(&bars[i], (lastpar >> i) & 1u, 1u << 20);
+            }
+        }
+        __syncwarp();  // the control warp reconverges before the CTA barrier
+    } else if (producer) {
+        // ---- producer: every copy, issued as soon as its buffer's last reader is done
+        if (lane == 0) {
+            // barriers with an operation of this lane in flight, and the parity of its phase (for
+            // the bounded drain after an abort)
+            uint32_t inflight = 0, lastpar = 0;
+            auto mark = [&](int i, uint32_t parity) {
+                inflight |= 1u << i;
+                lastpar = (lastpar & ~(1u << i)) | (parity << i);
+            };
+            // k or v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
+            auto fetch_rows = [&](const CUtensorMap* map, int head, long long c, uint32_t dst, int bar,
+                                  uint32_t parity) {
+                const int z = static_cast<int>(bos + c * C);
+                tc::mbar_expect_tx(&bars[bar], 2 * 8192);
+                tc::tma_load_3d(sb + dst, map, 0, head, z, &bars[bar]);
+                tc::tma_load_3d(sb + dst + 8192, map, 64, head, z, &bars[bar]);
+                mark(bar, parity);
+            };
+            // a part of chunk c's record by a bulk copy
+            auto fetch_rec = [&](long long c, uint32_t from, uint32_t bytes, uint32_t dst, int bar, uint32_t parity) {
+                const uint8_t* rec = a.records + ((chunk0 + c) * a.Hv + h) * static_cast<long long>(REC_BYTES);
+                tc::mbar_expect_tx(&bars[bar], bytes);
+                tc::bulk_load(sb + dst, rec + from, bytes, &bars[bar]);
+                mark(bar, parity);
+            };
+            auto fetch_k = [&](long long c) {
+                fetch_rows(&maps.k, hk, c, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
+            };
+            auto fetch_v = [&](long long c) { fetch_rows(&maps.v, h, c, OFF_V, B_V, c & 1); };
+            auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_QT - REC_T4, OFF_T4, B_R1, c & 1); };
+            auto fetch_qt = [&](long long c) { fetch_rec(c, REC_QT, REC_M - REC_QT, OFF_QT, B_QT, c & 1); };
+            auto fetch_rm = [&](long long c) { fetch_rec(c, REC_M, REC_VEC - REC_M, OFF_M, B_RM, c & 1); };
+            auto fetch_rv = [&](long long c) {
+                fetch_rec(c, REC_VEC, REC_VEC_BYTES, OFF_VEC + (c & 1) * REC_VEC_BYTES, B_RV0 + static_cast<int>(c & 1),
+                          (c >> 1) & 1);
+            };
+            fetch_k(0);
+            fetch_v(0);
+            fetch_r1(0);
+            fetch_qt(0);
+            fetch_rm(0);
+            fetch_rv(0);
+            if (nch > 1) fetch_k(1);
+            do {
+                if (!wait_bar(B_WU, 0)) break;
+                if (nch > 1) {  // U read the v tile, W and U the record part
+                    fetch_v(1);
+                    fetch_r1(1);
+                }
+                for (long long c = 0; c < nch; ++c) {
+                    const bool more = c + 1 < nch;
+                    const uint32_t par = c & 1;
+                    if (!wait_bar(B_A, par)) break;  // P~, issued before Delta, read Q~
                     if (more) {
+                        fetch_qt(c + 1);
                         fetch_rv(c + 1);  // its buffer's last reader, chunk c - 1's Delta conversion, is done
                         if (!wait_bar(B_WU, (c + 1) & 1)) break;
                         if (c + 2 < nch) {  // U read the v tile, W and U the record part
@@ -1010,7 +1033,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     if (inflight & (1u << i)) tc::mbar_wait(&bars[i], (lastpar >> i) & 1u, 1u << 20);
             }
         }
-        __syncwarp();  // the control warp reconverges before the CTA barrier
+        __syncwarp();  // the producer warp reconverges before the CTA barrier
     } else {
         // ---- workers
         do {
@@ -1087,8 +1110,8 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     tc::fence_after();
     if (abort_flag) {
         if (tid == 0) atomicOr(a.status, 4);
-    } else if (!control) {
-        // ---- scatter the final state back to its pool slot (row v, columns 32*qt ..)
+    } else if (warp < NW) {
+        // ---- workers: scatter the final state back to its pool slot (row v, columns 32*qt ..)
         float4* dst = reinterpret_cast<float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
         float s32[32];
         ld32(trow + TM_S + 32 * qt, s32);
