@@ -113,7 +113,8 @@ constexpr int NW = 16, NTS = 32 * (NW + 2);
 // and copies
 enum : int {
     B_A = 0,   // P~ and Delta of a chunk computed
-    B_C,       // M~ Delta and the state update computed
+    B_C,       // the state update of a chunk computed
+    B_O,       // O = P~ + M~ Delta of a chunk computed
     B_WU,      // W and U of a chunk computed
     R_B,       // workers: Delta converted, state scaled
     R_S,       // workers: S0 (high parts in shared memory, low parts in TMEM) of the next chunk in place
@@ -913,7 +914,8 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         issue_wu(c + 1);
                         wu_done = true;
                     }
-                    // ---- C. O^T = P~^T + Delta^T M~^T (three hi / lo products) and S += Delta~^T K
+                    // ---- C. S += Delta~^T K, which the workers wait for, then O^T = P~^T + Delta^T M~^T
+                    //      (three hi / lo products), stored by the workers while they wait for Delta
                     if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
                     if (!wu_done && wu_ready_now(c + 1)) {
                         tc::fence_after();
@@ -924,15 +926,6 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     {
                         const uint32_t idm = tc::idesc_bf16(128, 64, 0, 0, 0);
                         const uint32_t ids = idesc_in<F16>(128, 128, 0, 1, 0);
-#pragma unroll
-                        for (int pr = 0; pr < 3; ++pr) {
-                            const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo
-                            const uint32_t pb = pr == 1 ? 8192u : 0u;   // M~ hi, lo, hi
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)
-                                tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dDL, pa + ks * 32), dadd(dM, pb + ks * 32),
-                                             idm, 1u);
-                        }
                         // gamma_L == 0: the decayed state is 0 and the update overwrites it
                         const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC + (c & 1) * REC_VEC_BYTES);
                         const uint32_t keep = vec[V_GL] != 0.f ? 1u : 0u;
@@ -944,6 +937,17 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                                              (part | ks) != 0 ? 1u : keep);
                         tc::commit(&bars[B_C]);
                         mark(B_C, par);
+#pragma unroll
+                        for (int pr = 0; pr < 3; ++pr) {
+                            const uint32_t pa = pr == 2 ? 16384u : 0u;  // Delta hi, hi, lo
+                            const uint32_t pb = pr == 1 ? 8192u : 0u;   // M~ hi, lo, hi
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                tc::mma_bf16(tm + TM_O + (c & 1) * 64, dadd(dDL, pa + ks * 32), dadd(dM, pb + ks * 32),
+                                             idm, 1u);
+                        }
+                        tc::commit(&bars[B_O]);
+                        mark(B_O, par);
                     }
                     if (!wu_done) {  // the tiles came late, or the next chunk is the short last one
                         if (!wu_inputs(c + 1)) break;
@@ -1022,10 +1026,9 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         }
                     }
                     if (!wait_bar(B_C, par)) break;
-                    if (more) {
-                        fetch_rm(c + 1);                   // M~ Delta read M~
-                        if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
-                    }
+                    if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
+                    if (!wait_bar(B_O, par)) break;
+                    if (more) fetch_rm(c + 1);         // M~ Delta read M~
                 }
             } while (false);
             if (abort_flag) {  // give what is still in flight one more bounded wait
@@ -1081,7 +1084,6 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 if (!warp_wait(B_A, par) || !warp_wait(B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1)) { ok = false; break; }
                 convert_delta(c);
                 warp_arrive(R_B);
-                if (c > 0) outputs(c - 1);  // while O and the update of chunk c are computed
                 if (!warp_wait(B_C, par)) { ok = false; break; }
                 if (more) {
                     convert_s();
@@ -1099,9 +1101,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     convert_w();
                     warp_arrive(R_D);
                 }
+                // chunk c's outputs, while the next chunk's P~ and Delta are computed
+                if (!warp_wait(B_O, par)) { ok = false; break; }
+                outputs(c);
             }
             if (!ok) break;
-            outputs(nch - 1);
         } while (false);
     }
 
