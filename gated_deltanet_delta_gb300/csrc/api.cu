@@ -337,9 +337,9 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     REQUIRE(cache_indices && cu_seqlens && dev_status && A_log && dt_bias && state_pool,
             GDN_ERR_INVALID_ARG, "%s: null pointer", fn);
     REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG, "%s: null token pointer", fn);
-    REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(state_pool, 16),
-            GDN_ERR_INVALID_ARG, "%s: q, k, v and state_pool must be 16-byte aligned", fn);
-    REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(out, 2) && aligned(A_log, 4) &&
+    REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) && aligned(state_pool, 16),
+            GDN_ERR_INVALID_ARG, "%s: q, k, v, out and state_pool must be 16-byte aligned", fn);
+    REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(A_log, 4) &&
                 aligned(dt_bias, 4) && aligned(dev_status, 4) && aligned(cache_indices, 8) &&
                 aligned(cu_seqlens, 8),
             GDN_ERR_INVALID_ARG, "%s: misaligned argument", fn);

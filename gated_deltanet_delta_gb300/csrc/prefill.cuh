@@ -172,6 +172,21 @@ __device__ __forceinline__ uint16_t f32_to_in(float x) {
     if constexpr (F16) return __half_as_ushort(__float2half_rn(x));
     else return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xffffu);
 }
+// 8 floats to 8 elements of the input type (round to nearest even) in a uint4.
+template <bool F16>
+__device__ __forceinline__ uint4 pack_in_x8(const float* x) {
+    if constexpr (F16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h2 = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        return pack_bf16x8(x);
+    }
+}
 // Split 8 floats into high and low parts of the input type (the operands multiplied with raw tiles).
 template <bool F16>
 __device__ __forceinline__ void split_in_x8(const float* x, uint4& hi, uint4& lo) {
@@ -777,16 +792,35 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         tc::st16(trow + TM_SL + 16 * qt, lo16);
     };
     // outputs of chunk c from O (TMEM), tokens 16*qt .. (lane v)
+    // Lane v holds tokens 16*qt .. 16*qt+15 of its column; an 8 x 8 transpose inside each group of
+    // 8 lanes (three xor-shuffle stages) gives lane 8b + j the columns 8b .. 8b+7 (of the warp's
+    // 32) of token 8s + j, stored as one 16-byte vector per set s of 8 tokens.
     auto outputs = [&](long long c) {
         const int L = chunk_len(c);
         float o16[16];
         tc::ld16(trow + TM_O + (c & 1) * 64 + 16 * qt, o16);
         tc::wait_ld();
-        uint16_t* o = a.out + static_cast<size_t>(bos + c * C + 16 * qt) * vo_stride + h * D + row;
-        const int n_here = L - 16 * qt;
+        const int j8 = lane & 7;
+        uint16_t* o = a.out + static_cast<size_t>(bos + c * C) * vo_stride + h * D + (row - j8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i < n_here) o[i * vo_stride] = f32_to_in<F16>(o16[i]);
+        for (int set = 0; set < 2; ++set) {
+            float r[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[i] = o16[8 * set + i];
+#pragma unroll
+            for (int k = 4; k >= 1; k >>= 1) {
+                const bool up = (lane & k) != 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i & k) continue;
+                    const float recv = __shfl_xor_sync(kFullMask, up ? r[i] : r[i | k], k);
+                    if (up) r[i] = recv;
+                    else r[i | k] = recv;
+                }
+            }
+            const int t = 16 * qt + 8 * set + j8;
+            if (t < L) *reinterpret_cast<uint4*>(o + static_cast<size_t>(t) * vo_stride) = pack_in_x8<F16>(r);
+        }
     };
     // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
     // which Delta has read); the state is scaled by gamma_L in TMEM before the update accumulates.

@@ -202,7 +202,7 @@ size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K
  *                                     other slots are not touched
  *   cache_indices  int64 [num_seqs]   distinct slots; duplicates give an undefined result
  *   cu_seqlens     int64 [num_seqs + 1]
- *   out            bf16 [T, Hv, V]    tokens of skipped sequences are not written
+ *   out            bf16 [T, Hv, V]    16-byte aligned; tokens of skipped sequences are not written
  *   workspace      device buffer of at least gdn_prefill_workspace_size(...) bytes, 256-byte
  *                  aligned, overlapping neither out nor state_pool (NULL only when num_seqs is 0);
  *                  contents need not be initialised and are scratch after the call; calls that
