@@ -81,11 +81,12 @@ constexpr int V_DL = 0, V_RK = 64, V_GL = 128;
 constexpr int PNT = 256;
 constexpr uint32_t P_KQ = 0;          // [K;Q] tile: two 16 KB feature halves, 64 k rows + 64 q rows
 constexpr uint32_t P_L = 0;           // fp32 [64][LST]: Lm, then T = (I + Lm)^-1
-constexpr uint32_t P_X = P_L + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse
-constexpr uint32_t P_USED = 32768;
+constexpr uint32_t P_X = P_L + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse; before
+                                               // it, M~ hi / lo staged in the record's layout (16 KB)
+constexpr uint32_t P_USED = P_X + 16384;
 constexpr uint32_t P_SMEM = P_USED + 1024;
 constexpr uint32_t P_TM_G = 0, P_TM_COLS = 64;
-static_assert(P_X + 32 * ZST * 4 <= P_USED, "Lm, T and the scratch fit in the [K;Q] tile");
+static_assert(P_X + 32 * ZST * 4 <= P_USED && P_X % 16 == 0, "Lm, T, the M~ staging and the scratch fit");
 
 // the sequential kernel's dynamic shared memory
 constexpr uint32_t OFF_K = 0;          // two K tiles (chunks of even / odd index), 16 KB each: two
@@ -467,7 +468,8 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         __syncthreads();  // the [K;Q] tile is no longer needed: Lm takes its place
 
         // ---- 5. Lm (lanes t < 64, fp32, in place of the tile) and M~ = diag(rq_t scale) M (lanes
-        //         64 + t, bf16 hi / lo, to the record) from G, 32 columns per thread
+        //         64 + t, bf16 hi / lo, staged in shared memory in the record's layout) from G, 32
+        //         columns per thread
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
             const int s0 = 32 * hf + 16 * qq;
@@ -512,12 +514,20 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                     uint4 mh, ml;
                     split_bf16x8(m8, mh, ml);
                     const int cc = s0 / 8 + c;
-                    *reinterpret_cast<uint4*>(rec + REC_M + tc::sw_chunk(t, cc, 64)) = mh;
-                    *reinterpret_cast<uint4*>(rec + REC_M + 8192 + tc::sw_chunk(t, cc, 64)) = ml;
+                    *reinterpret_cast<uint4*>(sm + P_X + tc::sw_chunk(t, cc, 64)) = mh;
+                    *reinterpret_cast<uint4*>(sm + P_X + 8192 + tc::sw_chunk(t, cc, 64)) = ml;
                 }
             }
         }
         __syncthreads();
+
+        // M~ to the record: consecutive threads write consecutive 16-byte chunks (the scratch of the
+        // inverse takes its place after the next barrier)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = tid + PNT * k;
+            *reinterpret_cast<uint4*>(rec + REC_M + 16 * e) = *reinterpret_cast<const uint4*>(sm + P_X + 16 * e);
+        }
 
         // ---- 6. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32), in place of Lm:
         //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution (a block's
@@ -625,29 +635,25 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         __syncthreads();
 
         // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as hi / lo parts of the input type
-        //         (rows t, K-major), to the record
-        {
-            const int t = tid & (C - 1);
-            const bool w_side = ((tid >> 6) & 1) == 0;
+        //         (rows t, K-major), to the record: item e is chunk e & 7 of row (e >> 3) & 63 of
+        //         side e >> 9, so 8 consecutive threads write one row's 128 bytes
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = tid + PNT * k;
+            const int cc = e & 7, t = (e >> 3) & (C - 1);
+            const bool w_side = (e >> 9) == 0;
             uint8_t* base = rec + REC_T4 + (w_side ? 0u : 16384u);
-            const float* wsrc0 = w_side ? wws : wus;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int cc = 4 * hf + c;
-                const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
-                const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
-                const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-                const float4 wa = *reinterpret_cast<const float4*>(wsrc0 + cc * 8);
-                const float4 wb = *reinterpret_cast<const float4*>(wsrc0 + cc * 8 + 4);
-                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-                float x8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x8[i] = tv[i] * wv[i];
-                uint4 th, tl;
-                split_in_x8<F16>(x8, th, tl);
-                *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
-                *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
-            }
+            const float* wsrc = w_side ? wws : wus;
+            const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
+            const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
+            const float4 wa = *reinterpret_cast<const float4*>(wsrc + cc * 8);
+            const float4 wb = *reinterpret_cast<const float4*>(wsrc + cc * 8 + 4);
+            const float x8[8] = {ta.x * wa.x, ta.y * wa.y, ta.z * wa.z, ta.w * wa.w,
+                                 tb.x * wb.x, tb.y * wb.y, tb.z * wb.z, tb.w * wb.w};
+            uint4 th, tl;
+            split_in_x8<F16>(x8, th, tl);
+            *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
+            *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
         }
     } while (false);
 
