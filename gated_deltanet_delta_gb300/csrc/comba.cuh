@@ -185,18 +185,21 @@ __global__ void __launch_bounds__(NT) comba_forward_kernel(const CombaFwdArgs a)
         const float4 vv = bf16x4_to_f32x4(nv);
         if (t + 1 < T) fetch(t + 1);
 
-        // 3. decay and this thread's part of S^T p
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        // 3. decay and this thread's part of S^T p (packed f32x2 arithmetic on column pairs)
+        const float2 g2 = make_float2(gate, gate);
+        float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < NR; ++m) {
             const float pi = psf[bf * K + rg + RG * m];
+            const float2 p2 = make_float2(pi, pi);
             float4& x = s[m];
-            x.x *= gate; x.y *= gate; x.z *= gate; x.w *= gate;
-            r.x = fmaf(pi, x.x, r.x);
-            r.y = fmaf(pi, x.y, r.y);
-            r.z = fmaf(pi, x.z, r.z);
-            r.w = fmaf(pi, x.w, r.w);
+            float2 x01 = __fmul2_rn(make_float2(x.x, x.y), g2);
+            float2 x23 = __fmul2_rn(make_float2(x.z, x.w), g2);
+            r01 = __ffma2_rn(p2, x01, r01);
+            r23 = __ffma2_rn(p2, x23, r23);
+            x = make_float4(x01.x, x01.y, x23.x, x23.y);
         }
+        float4 r = make_float4(r01.x, r01.y, r23.x, r23.y);
         red_u[bf][rg][c] = r;
         __syncthreads();
         r = red_u[bf][0][c];
@@ -209,21 +212,21 @@ __global__ void __launch_bounds__(NT) comba_forward_kernel(const CombaFwdArgs a)
                                      beta * (vv.w - r.w));
 
         // 4. rank-1 write with k and this thread's part of the readout
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 u01 = make_float2(u.x, u.y), u23 = make_float2(u.z, u.w);
+        float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < NR; ++m) {
             const int i = rg + RG * m;
             const float ki = ksf[bf * K + i], qi = qsf[bf * K + i];
+            const float2 k2 = make_float2(ki, ki), q2 = make_float2(qi, qi);
             float4& x = s[m];
-            x.x = fmaf(ki, u.x, x.x);
-            x.y = fmaf(ki, u.y, x.y);
-            x.z = fmaf(ki, u.z, x.z);
-            x.w = fmaf(ki, u.w, x.w);
-            o.x = fmaf(qi, x.x, o.x);
-            o.y = fmaf(qi, x.y, o.y);
-            o.z = fmaf(qi, x.z, o.z);
-            o.w = fmaf(qi, x.w, o.w);
+            const float2 x01 = __ffma2_rn(k2, u01, make_float2(x.x, x.y));
+            const float2 x23 = __ffma2_rn(k2, u23, make_float2(x.z, x.w));
+            o01 = __ffma2_rn(q2, x01, o01);
+            o23 = __ffma2_rn(q2, x23, o23);
+            x = make_float4(x01.x, x01.y, x23.x, x23.y);
         }
+        float4 o = make_float4(o01.x, o01.y, o23.x, o23.y);
         red_o[bf][rg][c] = o;
         if (t + 1 < T) stage(bf ^ 1);  // its last readers (token t - 1) passed this token's first barrier
         __syncthreads();
