@@ -704,7 +704,9 @@ def main():
             "workload": gi.COMBA_FORWARD["name"], "value": N * cf["B"] * cf["H"] * cf["T"] / t1,
             "unit": "head-token steps/s", "us_per_call": t1 * 1e6,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+                         "frac": gbs / hbm_peak, "note": peak_note,
+                         "traffic": profiled_traffic("comba_forward_kernel",
+                                                     "gated_deltanet_delta_gb300/csrc/comba_forward.cuh")}}
     elif "comba_forward" in extra:
         ops["comba_forward"] = cf
     if isinstance(extra.get("comba_sweep"), list):

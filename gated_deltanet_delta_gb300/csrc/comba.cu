@@ -1,5 +1,6 @@
 // comba.cu -- launch configurations of the Comba decode kernel (kernel in comba.cuh).
 #include "comba.cuh"
+#include "comba_forward.cuh"
 #include "launch.h"
 
 namespace gdn {
