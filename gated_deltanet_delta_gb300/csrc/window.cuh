@@ -60,7 +60,6 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
     __shared__ __align__(16) float qraw[2][4 * RBS];
     __shared__ __align__(16) float kraw[2][4 * RBS];
     __shared__ __align__(16) float vraw[2][D];
-    __shared__ float part_q[2][4], part_k[2][4];
     __shared__ float gates[kWinMaxTok][2];  // gate and beta of every token, computed up front
     __shared__ __align__(16) float osm[kWinMaxTok][D];
     __shared__ float ssw[kWinMaxTok][4];  // per-warp sums of o^2
@@ -159,29 +158,27 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
         qraw[b][(tid >> 5) * RBS + (tid & 31)] = cq;
         kraw[b][(tid >> 5) * RBS + (tid & 31)] = ck;
         vraw[b][tid] = cv;
-        const float sq = group_sum<32>(cq * cq);
-        const float sk = group_sum<32>(ck * ck);
-        if (lane == 0) {
-            part_q[b][warp] = sq;
-            part_k[b][warp] = sk;
-        }
         __syncthreads();
 
         // everything below is warp-local: the warp owns 32 whole columns
-        const float rk = rsqrtf(((part_k[b][0] + part_k[b][1]) + (part_k[b][2] + part_k[b][3])) + a.eps);
-        const float rq = rsqrtf(((part_q[b][0] + part_q[b][1]) + (part_q[b][2] + part_q[b][3])) + a.eps);
         const float gate = gates[t][0], beta = gates[t][1];
         const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * RBS);
         const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * RBS);
 
         // kv = cs rk sum_i R_ij k_i: 32 rows in registers (as 16 row pairs), then the 4 row blocks
-        // by two shuffles
+        // by two shuffles; |k|^2 and |q|^2 (the L2 norms) ride along: each lane sums its row
+        // block's 32 squares and the same two shuffles add the 4 blocks
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
+        float2 nk2 = make_float2(0.f, 0.f), nq2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m4 = 0; m4 < NR / 4; ++m4) {
             const float4 kk = k4[m4];
+            const float4 qq = q4[m4];
             const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+            const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
+            nk2 = __ffma2_rn(k01, k01, __ffma2_rn(k23, k23, nk2));
+            nq2 = __ffma2_rn(q01, q01, __ffma2_rn(q23, q23, nq2));
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 acc[j] = __ffma2_rn(R[2 * m4][j], k01, acc[j]);
@@ -191,10 +188,16 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
         float kvs[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) kvs[j] = acc[j].x + acc[j].y;
+        float ksq = nk2.x + nk2.y, qsq = nq2.x + nq2.y;
 #pragma unroll
-        for (int o = 8; o < 32; o <<= 1)
+        for (int o = 8; o < 32; o <<= 1) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) kvs[j] += __shfl_xor_sync(kFullMask, kvs[j], o);
+            ksq += __shfl_xor_sync(kFullMask, ksq, o);
+            qsq += __shfl_xor_sync(kFullMask, qsq, o);
+        }
+        const float rk = rsqrtf(ksq + a.eps);
+        const float rq = rsqrtf(qsq + a.eps);
         const float4 vv = *reinterpret_cast<const float4*>(vraw[b] + col);
         const float gk = gate * cs * rk;
         float cn = gate * cs;
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
                 for (int j = 0; j < 4; ++j) R[p][j] = __fmul2_rn(R[p][j], make_float2(cn, cn));
             cn = 1.0f;
         }
-        const float ek = beta * rk / cn;
+        const float ek = beta * rk * __frcp_rn(cn);
         const float vj[4] = {vv.x, vv.y, vv.z, vv.w};
         float2 e2[4];
 #pragma unroll
