@@ -156,6 +156,45 @@ def test_chunk_size_128_gives_the_same_call():
     _check_all(x, d128, out128, scale)
 
 
+def test_zero_key_and_query_rows():
+    # k = 0 gives k^ = 0 (rk = 1/sqrt(eps) = 1000 multiplies a zero row): the token updates nothing;
+    # q = 0 gives a zero output row
+    x = gi.gdn_prefill_inputs(gi.rng(31), [70, 5], 1, 2, 128, 128, pool=2, mild_gates=True)
+    x["k"][[0, 3, 63, 64, 69, 71]] = 0.0
+    x["q"][[1, 64, 72]] = 0.0
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+    assert not host(out)[[1, 64, 72]].any()
+
+
+@pytest.mark.parametrize("case", ["no_update", "no_decay"])
+def test_gate_extremes(case):
+    # b -> -inf: beta = 0, the state only decays; a -> -inf: the log-gate is 0 (no decay), so the
+    # state carries unchanged in scale over 3 chunks and gamma_L = 1 on every chunk
+    x = gi.gdn_prefill_inputs(gi.rng(41), [150, 64], 1, 2, 128, 128, pool=2, mild_gates=True)
+    if case == "no_update":
+        x["b"][:] = -60.0
+    else:
+        x["a"][:] = -60.0
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    _check_all(x, d, out, scale)
+
+
+def test_all_sequences_empty():
+    # num_seqs > 0 but every sequence is empty (T = 0): nothing is written, the pool is untouched
+    x = gi.gdn_prefill_inputs(gi.rng(51), [0, 0, 0], 1, 2, 128, 128, pool=4)
+    d = _to_dev(x)
+    out, st = _gpu(d, 128 ** -0.5)
+    assert st == 0 and out.numel() == 0
+    assert np.array_equal(host(d["state_pool"]), x["state_pool"].astype(np.float64))
+
+
 def test_many_short_sequences():
     # 1100 sequences of 0 to 3 tokens: the chunk offsets are scanned in tiles of 1024 sequences, and
     # every chunk is a short one
