@@ -91,8 +91,10 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
     }
     gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.cap, a.chunk_off,
                                                                 a.chunk_tab);
-    if (a.T > 0) {  // one CTA per (chunk, value head) unit of the capacity; the ones past the last chunk exit
-        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hv);
+    if (a.T > 0) {  // one CTA per (chunk, key head, pair of value heads) of the capacity; the ones past
+                    // the last chunk exit
+        const int ngrp = (a.Hv / a.Hk + pf::PH - 1) / pf::PH;
+        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hk) * static_cast<unsigned>(ngrp);
         if (f16) gdn_prefill_prep_kernel<true><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
         else gdn_prefill_prep_kernel<false><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
     }

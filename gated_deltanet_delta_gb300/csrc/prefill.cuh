@@ -79,6 +79,7 @@ constexpr int V_DL = 0, V_RK = 64, V_GL = 128;
 // from a 1024-aligned base) is the [K;Q] tile, reused once G, the norms and Q~ are done for the fp32
 // Lm, which the blockwise inverse turns into T in place, and the inverse's scratch
 constexpr int PNT = 256;
+constexpr int PH = 2;          // value heads per preparation CTA (at most)
 constexpr uint32_t P_KQ = 0;          // [K;Q] tile: two 16 KB feature halves, 64 k rows + 64 q rows
 constexpr uint32_t P_L = 0;           // fp32 [64][LST]: Lm, then T = (I + Lm)^-1
 constexpr uint32_t P_X = P_L + 64 * LST * 4;  // fp32 [32][ZST] scratch of the blockwise inverse; before
@@ -297,28 +298,35 @@ __global__ void __launch_bounds__(kPfOffThreads)
 }
 
 // ------------------------------------------------------------------------------------------------
-// The state-independent part of one (chunk, value head) unit -> its chunk record.  Unit
-// u = blockIdx.x is chunk f = u / Hv (the table gives its first token and length) of value head
-// h = u % Hv.  CTAs of 256 threads, five per SM: the latency-bound phases of one unit (the inverse
-// runs 64, 128 and 256 threads wide) overlap with those of four others.  Every part of the record
-// is written to the workspace directly.
+// The state-independent part of one chunk for up to two value heads of one key head -> their chunk
+// records.  The heads of a key head share the k and q rows, their norms and G = [K; Q] K^T, so a
+// CTA loads and multiplies them once and repeats only the gate-dependent phases per head.  CTA
+// b = (f * Hk + hk) * ngrp + g is chunk f (the table gives its first token and length), key head
+// hk, value heads hk * R + 2g and, when R - 2g > 1, the next (R = Hv / Hk, ngrp = ceil(R / 2)).
+// CTAs of 256 threads, five per SM: the latency-bound phases of one CTA (the inverse runs 64, 128
+// and 256 threads wide) overlap with those of four others.  Every part of a record is written to
+// the workspace directly.
 template <bool F16>
 __global__ void __launch_bounds__(pf::PNT, 5)
     gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(16) float Gf[C], betas[C], rks[C], rqs[C], gams[C], wws[C], wus[C];
-    __shared__ float scan_total;
+    __shared__ __align__(16) float Gf[PH][C], betas[PH][C], gams[PH][C], wws[PH][C], wus[PH][C];
+    __shared__ __align__(16) float rks[C], rqs[C];
+    __shared__ float scan_total[PH];
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(8) uint64_t mbar;    // MMA completion
     __shared__ __align__(8) uint64_t bar_kq;  // TMA of the unit's k and q rows
 
     const long long total = a.chunk_off[a.num_seqs] < a.cap ? a.chunk_off[a.num_seqs] : a.cap;
+    const int R = a.Hv / a.Hk, ngrp = (R + PH - 1) / PH;
     const long long u = blockIdx.x;
-    if (u >= total * a.Hv) return;
-    const long long f = u / a.Hv;
-    const int h = static_cast<int>(u - f * a.Hv);
-    const int hk = h / (a.Hv / a.Hk);
+    if (u >= total * a.Hk * ngrp) return;
+    const long long f = u / (static_cast<long long>(a.Hk) * ngrp);
+    const int rem = static_cast<int>(u - f * a.Hk * ngrp);
+    const int hk = rem / ngrp;
+    const int h0 = hk * R + PH * (rem - hk * ngrp);  // first value head of this CTA
+    const int nh = R - (h0 - hk * R) < PH ? R - (h0 - hk * R) : PH;
     const longlong2 entry = a.chunk_tab[f];
     const long long tok0 = entry.x;
     const int L = static_cast<int>(entry.y & 0xffffffffLL);
@@ -330,8 +338,8 @@ __global__ void __launch_bounds__(pf::PNT, 5)
     const uint32_t sb = tc::smem_u32(sm);
     float* Ls = reinterpret_cast<float*>(sm + P_L);
     float* Xs = reinterpret_cast<float*>(sm + P_X);
-    uint8_t* rec = a.records + u * static_cast<long long>(REC_BYTES);
-    float* vec = reinterpret_cast<float*>(rec + REC_VEC);
+    // the record of value head h0 + j
+    auto record = [&](int j) { return a.records + (f * a.Hv + h0 + j) * static_cast<long long>(REC_BYTES); };
 
     if (warp == 0) tc::tmem_alloc(&tmem_slot, P_TM_COLS);
     if (tid == 0) {
@@ -344,14 +352,19 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, hk, z, &bar_kq);
         tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_kq);
     }
-    uint16_t a_raw = 0, b_raw = 0;  // gate inputs of token tid (threads < L)
-    if (tid < L) {
-        const size_t gi = static_cast<size_t>(tok0 + tid) * a.Hv + h;
-        a_raw = a.a[gi];
-        b_raw = a.b[gi];
+    // gate inputs: thread jg * 64 + t takes token t of value head h0 + jg
+    const int jg = tid >> 6, tg = tid & (C - 1);
+    uint16_t a_raw = 0, b_raw = 0;
+    float a_mul = 0.f, dtb = 0.f;
+    if (jg < nh) {
+        if (tg < L) {
+            const size_t gi = static_cast<size_t>(tok0 + tg) * a.Hv + h0 + jg;
+            a_raw = a.a[gi];
+            b_raw = a.b[gi];
+        }
+        a_mul = expf(a.A_log[h0 + jg]);
+        dtb = a.dt_bias[h0 + jg];
     }
-    const float a_mul = expf(a.A_log[h]);
-    const float dtb = a.dt_bias[h];
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -413,9 +426,10 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             }
             tc::commit(&mbar);
         }
-        // ---- 3. gates and their in-chunk cumulative sum (while G is computed)
-        if (tid < C) {
-            const int t = tid;
+        // ---- 3. gates and their in-chunk cumulative sum (while G is computed), every head at once:
+        //         threads jg * 64 .. jg * 64 + 63 scan value head h0 + jg
+        if (jg < nh) {
+            const int t = tg;
             float ell = 0.f, be = 0.f;
             if (t < L) {
                 const float x = in_to_f32<F16>(a_raw) + dtb;
@@ -429,21 +443,23 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                 const float y = __shfl_up_sync(kFullMask, g, o);
                 if (lane >= o) g += y;
             }
-            if (t == 31) scan_total = g;
-            asm volatile("bar.sync 1, 64;" ::: "memory");
-            if (t >= 32) g += scan_total;
-            Gf[t] = g;
-            betas[t] = be;
+            if (t == 31) scan_total[jg] = g;
+            if (jg == 0) asm volatile("bar.sync 1, 64;" ::: "memory");
+            else asm volatile("bar.sync 2, 64;" ::: "memory");
+            if (t >= 32) g += scan_total[jg];
+            Gf[jg][t] = g;
+            betas[jg][t] = be;
         }
         __syncthreads();
-        if (tid < C) {
-            const int t = tid;
-            gams[t] = __expf(Gf[t]);
-            wws[t] = betas[t] * gams[t] * rks[t];
-            wus[t] = betas[t];
-            vec[V_DL + t] = t < L ? __expf(Gf[L - 1] - Gf[t]) : 0.f;
+        if (jg < nh) {
+            const int t = tg;
+            float* vec = reinterpret_cast<float*>(record(jg) + REC_VEC);
+            gams[jg][t] = __expf(Gf[jg][t]);
+            wws[jg][t] = betas[jg][t] * gams[jg][t] * rks[t];
+            wus[jg][t] = betas[jg][t];
+            vec[V_DL + t] = t < L ? __expf(Gf[jg][L - 1] - Gf[jg][t]) : 0.f;
             vec[V_RK + t] = rks[t];
-            if (t == 0) vec[V_GL] = __expf(Gf[L - 1]);
+            if (t == 0) vec[V_GL] = __expf(Gf[jg][L - 1]);
         }
         {
             const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, kWaitLimit);
@@ -455,11 +471,13 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             tc::fence_after();
         }
 
-        // ---- 4. Q~ = diag(gamma_t rq_t scale) Q (bf16, rows t, K-major) from the q rows, to the record
-        for (int e = tid; e < C * 16; e += PNT) {
-            const int t = e >> 4, cc = e & 15;
+        // ---- 4. Q~ = diag(gamma_t rq_t scale) Q (bf16, rows t, K-major) from the q rows, to the
+        //         record of every head (before Lm takes the tile's place)
+        for (int e = tid; e < nh * C * 16; e += PNT) {
+            const int j = e / (C * 16), t = (e >> 4) & (C - 1), cc = e & 15;
+            uint8_t* rec = record(j);
             const uint4 q8 = *reinterpret_cast<const uint4*>(sm + P_KQ + tc::sw_chunk(64 + t, cc, 128));
-            const float fq = gams[t] * (rqs[t] * a.scale);
+            const float fq = gams[j][t] * (rqs[t] * a.scale);
             const float4 x0 = in4_to_f32x4<F16>(make_uint2(q8.x, q8.y));
             const float4 x1 = in4_to_f32x4<F16>(make_uint2(q8.z, q8.w));
             const float y[8] = {x0.x * fq, x0.y * fq, x0.z * fq, x0.w * fq, x1.x * fq, x1.y * fq, x1.z * fq, x1.w * fq};
@@ -467,193 +485,202 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         }
         __syncthreads();  // the [K;Q] tile is no longer needed: Lm takes its place
 
-        // ---- 5. Lm (lanes t < 64, fp32, in place of the tile) and M~ = diag(rq_t scale) M (lanes
-        //         64 + t, bf16 hi / lo, staged in shared memory in the record's layout) from G, 32
-        //         columns per thread
+        // ---- 5 .. 7 per value head (Lm, T and the scratch reuse the same shared memory)
+        for (int j = 0; j < nh; ++j) {
+            const float* Gfj = Gf[j];
+            const float* betasj = betas[j];
+            const float* wwsj = wws[j];
+            const float* wusj = wus[j];
+            uint8_t* recj = record(j);
+            // ---- 5. Lm (lanes t < 64, fp32, in place of the tile) and M~ = diag(rq_t scale) M (lanes
+            //         64 + t, bf16 hi / lo, staged in shared memory in the record's layout) from G, 32
+            //         columns per thread
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int s0 = 32 * hf + 16 * qq;
-            float g[16];
-            tc::ld16(trow + P_TM_G + s0, g);
-            tc::wait_ld();
-            if (row < C) {
-                const int t = row;
-                const float bt = betas[t] * rks[t];
-                const float Gt = Gf[t];
+            for (int qq = 0; qq < 2; ++qq) {
+                const int s0 = 32 * hf + 16 * qq;
+                float g[16];
+                tc::ld16(trow + P_TM_G + s0, g);
+                tc::wait_ld();
+                if (row < C) {
+                    const int t = row;
+                    const float bt = betasj[t] * rks[t];
+                    const float Gt = Gfj[t];
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
-                    const float4 r4 = *reinterpret_cast<const float4*>(rks + s0 + 4 * i4);
-                    const float4 G4 = *reinterpret_cast<const float4*>(Gf + s0 + 4 * i4);
-                    const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, GG[4] = {G4.x, G4.y, G4.z, G4.w};
-                    float l4[4];
+                    for (int i4 = 0; i4 < 4; ++i4) {
+                        const float4 r4 = *reinterpret_cast<const float4*>(rks + s0 + 4 * i4);
+                        const float4 G4 = *reinterpret_cast<const float4*>(Gfj + s0 + 4 * i4);
+                        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, GG[4] = {G4.x, G4.y, G4.z, G4.w};
+                        float l4[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int s = s0 + 4 * i4 + w;
+                            l4[w] = s < t ? bt * rr[w] * g[4 * i4 + w] * __expf(Gt - GG[w]) : 0.f;
+                        }
+                        *reinterpret_cast<float4*>(Ls + t * LST + s0 + 4 * i4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
+                    }
+                } else {
+                    const int t = row - C;
+                    const float Gt = Gfj[t];
+                    const float rt = rqs[t] * a.scale;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const float4 ra = *reinterpret_cast<const float4*>(rks + s0 + 8 * c);
+                        const float4 rb = *reinterpret_cast<const float4*>(rks + s0 + 8 * c + 4);
+                        const float4 Ga = *reinterpret_cast<const float4*>(Gfj + s0 + 8 * c);
+                        const float4 Gb = *reinterpret_cast<const float4*>(Gfj + s0 + 8 * c + 4);
+                        const float rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+                        const float GG[8] = {Ga.x, Ga.y, Ga.z, Ga.w, Gb.x, Gb.y, Gb.z, Gb.w};
+                        float m8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int s = s0 + c * 8 + i;
+                            m8[i] = s <= t ? rt * (rr[i] * g[c * 8 + i] * __expf(Gt - GG[i])) : 0.f;
+                        }
+                        uint4 mh, ml;
+                        split_bf16x8(m8, mh, ml);
+                        const int cc = s0 / 8 + c;
+                        *reinterpret_cast<uint4*>(sm + P_X + tc::sw_chunk(t, cc, 64)) = mh;
+                        *reinterpret_cast<uint4*>(sm + P_X + 8192 + tc::sw_chunk(t, cc, 64)) = ml;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // M~ to the record: consecutive threads write consecutive 16-byte chunks (the scratch of the
+            // inverse takes its place after the next barrier)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + PNT * k;
+                *reinterpret_cast<uint4*>(recj + REC_M + 16 * e) = *reinterpret_cast<const uint4*>(sm + P_X + 16 * e);
+            }
+
+            // ---- 6. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32), in place of Lm:
+            //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution (a block's
+            //      16 threads share a warp: the warp reads its blocks of Lm before writing them over);
+            //   B: T_{2p+1,2p} = -T_{2p+1,2p+1} Lm_{2p+1,2p} T_{2p,2p}   (32 x 32 diagonal blocks);
+            //   C: T_{[32,64),[0,32)} = -T_br Lm_bl T_tl                 (the whole matrix).
+            //   B and C read a block of Lm into the scratch product before its T overwrites it; each
+            //   thread takes one row and four consecutive columns (float4 operands).  The blocks above
+            //   the diagonal are zero from Lm.
+            if (tid < C) {
+                const int blk = tid >> 4, j = tid & 15;
+                float* Lb = Ls + (16 * blk) * LST + 16 * blk;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 + 1 < i; s2 += 2) {
+                        acc0 = fmaf(-Lb[i * LST + s2], x[s2], acc0);
+                        acc1 = fmaf(-Lb[i * LST + s2 + 1], x[s2 + 1], acc1);
+                    }
+                    if (i & 1) acc0 = fmaf(-Lb[i * LST + i - 1], x[i - 1], acc0);
+                    x[i] = (i < j) ? 0.f : acc0 + acc1;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Lb[i * LST + j] = x[i];
+            }
+            __syncthreads();
+            float* Zs = Xs;
+            const int pB = tid >> 6, rB = (tid >> 2) & 15, cB = 4 * (tid & 3);
+            if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p}
+                const float* Lr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB;
+                const float* Tc = Ls + (32 * pB) * LST + 32 * pB + cB;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
+                    const float lk[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        const int s = s0 + 4 * i4 + w;
-                        l4[w] = s < t ? bt * rr[w] * g[4 * i4 + w] * __expf(Gt - GG[w]) : 0.f;
+                        const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
+                        acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
+                        acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
                     }
-                    *reinterpret_cast<float4*>(Ls + t * LST + s0 + 4 * i4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
                 }
-            } else {
-                const int t = row - C;
-                const float Gt = Gf[t];
-                const float rt = rqs[t] * a.scale;
+                *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = acc;
+            }
+            __syncthreads();
+            if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p}
+                const float* Tr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
+                const float* Xc = Zs + (16 * pB) * ZST + cB;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const float4 ra = *reinterpret_cast<const float4*>(rks + s0 + 8 * c);
-                    const float4 rb = *reinterpret_cast<const float4*>(rks + s0 + 8 * c + 4);
-                    const float4 Ga = *reinterpret_cast<const float4*>(Gf + s0 + 8 * c);
-                    const float4 Gb = *reinterpret_cast<const float4*>(Gf + s0 + 8 * c + 4);
-                    const float rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-                    const float GG[8] = {Ga.x, Ga.y, Ga.z, Ga.w, Gb.x, Gb.y, Gb.z, Gb.w};
-                    float m8[8];
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
+                    const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int s = s0 + c * 8 + i;
-                        m8[i] = s <= t ? rt * (rr[i] * g[c * 8 + i] * __expf(Gt - GG[i])) : 0.f;
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 x4 = *reinterpret_cast<const float4*>(Xc + (4 * k4 + w) * ZST);
+                        acc.x = fmaf(tk[w], x4.x, acc.x); acc.y = fmaf(tk[w], x4.y, acc.y);
+                        acc.z = fmaf(tk[w], x4.z, acc.z); acc.w = fmaf(tk[w], x4.w, acc.w);
                     }
-                    uint4 mh, ml;
-                    split_bf16x8(m8, mh, ml);
-                    const int cc = s0 / 8 + c;
-                    *reinterpret_cast<uint4*>(sm + P_X + tc::sw_chunk(t, cc, 64)) = mh;
-                    *reinterpret_cast<uint4*>(sm + P_X + 8192 + tc::sw_chunk(t, cc, 64)) = ml;
                 }
+                *reinterpret_cast<float4*>(Ls + (32 * pB + 16 + rB) * LST + 32 * pB + cB) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
             }
-        }
-        __syncthreads();
+            __syncthreads();
+            const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
+            {  // Z = Lm_bl T_tl (all 256 threads)
+                const float* Lr = Ls + (32 + rC) * LST;
+                const float* Tc = Ls + cC;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
+                    const float lk[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
+                        acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
+                        acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
+                    }
+                }
+                *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = acc;
+            }
+            __syncthreads();
+            {  // T_bl = -T_br Z, over Lm_bl
+                const float* Tr = Ls + (32 + rC) * LST + 32;
+                const float* Zc = Zs + cC;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
+                    const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 z4 = *reinterpret_cast<const float4*>(Zc + (4 * k4 + w) * ZST);
+                        acc.x = fmaf(tk[w], z4.x, acc.x); acc.y = fmaf(tk[w], z4.y, acc.y);
+                        acc.z = fmaf(tk[w], z4.z, acc.z); acc.w = fmaf(tk[w], z4.w, acc.w);
+                    }
+                }
+                *reinterpret_cast<float4*>(Ls + (32 + rC) * LST + cC) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
 
-        // M~ to the record: consecutive threads write consecutive 16-byte chunks (the scratch of the
-        // inverse takes its place after the next barrier)
+            // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as hi / lo parts of the input type
+            //         (rows t, K-major), to the record: item e is chunk e & 7 of row (e >> 3) & 63 of
+            //         side e >> 9, so 8 consecutive threads write one row's 128 bytes
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int e = tid + PNT * k;
-            *reinterpret_cast<uint4*>(rec + REC_M + 16 * e) = *reinterpret_cast<const uint4*>(sm + P_X + 16 * e);
-        }
-
-        // ---- 6. T = (I + Lm)^-1 (unit lower triangular, 64 x 64, fp32), in place of Lm:
-        //   A: the four 16 x 16 diagonal blocks by column-parallel forward substitution (a block's
-        //      16 threads share a warp: the warp reads its blocks of Lm before writing them over);
-        //   B: T_{2p+1,2p} = -T_{2p+1,2p+1} Lm_{2p+1,2p} T_{2p,2p}   (32 x 32 diagonal blocks);
-        //   C: T_{[32,64),[0,32)} = -T_br Lm_bl T_tl                 (the whole matrix).
-        //   B and C read a block of Lm into the scratch product before its T overwrites it; each
-        //   thread takes one row and four consecutive columns (float4 operands).  The blocks above
-        //   the diagonal are zero from Lm.
-        if (tid < C) {
-            const int blk = tid >> 4, j = tid & 15;
-            float* Lb = Ls + (16 * blk) * LST + 16 * blk;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 + 1 < i; s2 += 2) {
-                    acc0 = fmaf(-Lb[i * LST + s2], x[s2], acc0);
-                    acc1 = fmaf(-Lb[i * LST + s2 + 1], x[s2 + 1], acc1);
-                }
-                if (i & 1) acc0 = fmaf(-Lb[i * LST + i - 1], x[i - 1], acc0);
-                x[i] = (i < j) ? 0.f : acc0 + acc1;
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + PNT * k;
+                const int cc = e & 7, t = (e >> 3) & (C - 1);
+                const bool w_side = (e >> 9) == 0;
+                uint8_t* base = recj + REC_T4 + (w_side ? 0u : 16384u);
+                const float* wsrc = w_side ? wwsj : wusj;
+                const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
+                const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
+                const float4 wa = *reinterpret_cast<const float4*>(wsrc + cc * 8);
+                const float4 wb = *reinterpret_cast<const float4*>(wsrc + cc * 8 + 4);
+                const float x8[8] = {ta.x * wa.x, ta.y * wa.y, ta.z * wa.z, ta.w * wa.w,
+                                     tb.x * wb.x, tb.y * wb.y, tb.z * wb.z, tb.w * wb.w};
+                uint4 th, tl;
+                split_in_x8<F16>(x8, th, tl);
+                *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
+                *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
             }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Lb[i * LST + j] = x[i];
-        }
-        __syncthreads();
-        float* Zs = Xs;
-        const int pB = tid >> 6, rB = (tid >> 2) & 15, cB = 4 * (tid & 3);
-        if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p}
-            const float* Lr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB;
-            const float* Tc = Ls + (32 * pB) * LST + 32 * pB + cB;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
-                const float lk[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
-                    acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
-                    acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = acc;
-        }
-        __syncthreads();
-        if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p}
-            const float* Tr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
-            const float* Xc = Zs + (16 * pB) * ZST + cB;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
-                const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float4 x4 = *reinterpret_cast<const float4*>(Xc + (4 * k4 + w) * ZST);
-                    acc.x = fmaf(tk[w], x4.x, acc.x); acc.y = fmaf(tk[w], x4.y, acc.y);
-                    acc.z = fmaf(tk[w], x4.z, acc.z); acc.w = fmaf(tk[w], x4.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4*>(Ls + (32 * pB + 16 + rB) * LST + 32 * pB + cB) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-        const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
-        {  // Z = Lm_bl T_tl (all 256 threads)
-            const float* Lr = Ls + (32 + rC) * LST;
-            const float* Tc = Ls + cC;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-                const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
-                const float lk[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
-                    acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
-                    acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = acc;
-        }
-        __syncthreads();
-        {  // T_bl = -T_br Z, over Lm_bl
-            const float* Tr = Ls + (32 + rC) * LST + 32;
-            const float* Zc = Zs + cC;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-                const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
-                const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float4 z4 = *reinterpret_cast<const float4*>(Zc + (4 * k4 + w) * ZST);
-                    acc.x = fmaf(tk[w], z4.x, acc.x); acc.y = fmaf(tk[w], z4.y, acc.y);
-                    acc.z = fmaf(tk[w], z4.z, acc.z); acc.w = fmaf(tk[w], z4.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4*>(Ls + (32 + rC) * LST + cC) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-
-        // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as hi / lo parts of the input type
-        //         (rows t, K-major), to the record: item e is chunk e & 7 of row (e >> 3) & 63 of
-        //         side e >> 9, so 8 consecutive threads write one row's 128 bytes
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int e = tid + PNT * k;
-            const int cc = e & 7, t = (e >> 3) & (C - 1);
-            const bool w_side = (e >> 9) == 0;
-            uint8_t* base = rec + REC_T4 + (w_side ? 0u : 16384u);
-            const float* wsrc = w_side ? wws : wus;
-            const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
-            const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
-            const float4 wa = *reinterpret_cast<const float4*>(wsrc + cc * 8);
-            const float4 wb = *reinterpret_cast<const float4*>(wsrc + cc * 8 + 4);
-            const float x8[8] = {ta.x * wa.x, ta.y * wa.y, ta.z * wa.z, ta.w * wa.w,
-                                 tb.x * wb.x, tb.y * wb.y, tb.z * wb.z, tb.w * wb.w};
-            uint4 th, tl;
-            split_in_x8<F16>(x8, th, tl);
-            *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
-            *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
+            __syncthreads();  // this head's reads of Lm, T and the scratch are done
         }
     } while (false);
 
