@@ -18,20 +18,21 @@
 // GB300 mapping: three kernels on one stream.
 //   gdn_prefill_offsets_kernel (one CTA): the first chunk of every sequence (a scan of the chunk
 //     counts) and a table entry per chunk (first token, sequence, length).
-//   gdn_prefill_prep_kernel (one CTA of 256 threads per (chunk, value head), five per SM): all the
-//     work that does not depend on the carried state -- row norms, gates, G = [K; Q] K^T on the
+//   gdn_prefill_prep_kernel (one CTA of 256 threads per (chunk, key head) and up to two of its value
+//     heads, five per SM): all the work that does not depend on the carried state -- row norms,
+//     gates, G = [K; Q] K^T (shared by the CTA's value heads) on the
 //     tensor core, Lm, the triangular inverse, Tw = T diag(beta gamma rk) and Tu = T diag(beta),
 //     M~ = diag(rq scale) M (all split into bf16 high and low parts) and Q~ = diag(gamma rq scale) Q
 //     -- written as one chunk record (kPfRecordBytes, laid out as the sequential kernel's
 //     shared-memory image).  This is the bulk of the CUDA-core work; here every chunk of every
 //     sequence runs in parallel.
-//   gdn_prefill_kernel (one CTA of 16 worker warps and a control warp per (sequence, value head)):
-//     the chunk recurrence.  The fp32 state S (V x K = 128 x 128) lives in TMEM for the whole
-//     sequence and reaches HBM only at the start (gather from the pool slot) and at the end
-//     (scatter back).  Per chunk it takes k and v rows by TMA (cp.async.bulk.tensor, 64 tokens x 64
-//     features per box) and the parts of the chunk record by bulk copies, each fetched as soon as
-//     its buffer is free; worker threads i, i + 128, i + 256 and i + 384 share TMEM lane i (each
-//     takes a quarter of the columns).
+//   gdn_prefill_kernel (one CTA of 16 worker warps, a control warp and a producer warp per
+//     (sequence, value head)): the chunk recurrence.  The fp32 state S (V x K = 128 x 128) lives in
+//     TMEM for the whole sequence and reaches HBM only at the start (gather from the pool slot) and
+//     at the end (scatter back).  The control lane issues the MMAs; the producer lane takes k and v
+//     rows by TMA (cp.async.bulk.tensor, 64 tokens x 64 features per box) and the parts of the
+//     chunk record by bulk copies, each as soon as its buffer is free; worker threads i, i + 128,
+//     i + 256 and i + 384 share TMEM lane i (each takes a quarter of the columns).
 // Every contraction is a tcgen05.mma with M = 128 (the transposed forms keep V or the feature index
 // on M):
 //     G   = [K; Q] K^T              M=128 (64 k rows + 64 q rows), N=64,  K=128   bf16 (exact inputs)
@@ -693,13 +694,14 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 // ------------------------------------------------------------------------------------------------
 // The chunk recurrence of one (sequence, value head), from its chunk records, warp-specialized.
 // Per chunk c the state path is: P~ = S0 Q~^T and Delta = U - S0 W^T (tensor core) -> Delta to
-// bf16 hi / lo and the state scaled by gamma_L (workers) -> O = P~ + M~ Delta and S += Delta~^T K
-// (tensor core) -> S and the next chunk's W to bf16 (workers).  W and U of chunk c + 1 are
-// multiplied while the workers convert Delta (U alternates between two TMEM buffers), and chunk
-// c's outputs are converted and stored while chunk c + 1's O and state update are computed (O
-// alternates too).  The output scales are folded into Q~ and M~ by the preparation kernel, so an
-// output is one TMEM read and one store.  The control lane issues the MMAs as soon as the
-// workers' hand-off arrives and each copy as soon as its buffer's last reader is done.
+// bf16 hi / lo and the state scaled by gamma_L (workers) -> S += Delta~^T K, then O = P~ + M~ Delta
+// (tensor core) -> S and the next chunk's W to bf16 (workers) -> chunk c's outputs stored by the
+// workers while chunk c + 1's P~ and Delta are computed.  W and U of chunk c + 1 are multiplied
+// while the workers convert Delta (U and O alternate between two TMEM buffers).  The output scales
+// are folded into Q~ and M~ by the preparation kernel, so an output is one TMEM read, an in-warp
+// transpose and one 16-byte store per 8 columns.  The control lane issues each MMA batch as soon as
+// the workers' hand-off arrives; the producer lane issues each copy as soon as its buffer's last
+// reader is done.
 template <bool F16>
 __global__ void __launch_bounds__(pf::NTS, 1)
     gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
