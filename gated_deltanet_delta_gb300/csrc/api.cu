@@ -346,14 +346,15 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
     REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG, "%s: out overlaps state_pool",
             fn);
-    REQUIRE((long long)num_seqs * Hv < (1LL << 31) && T < (1LL << 31) - 64 &&
+    REQUIRE((long long)(num_seqs + 2 * gdn::kPfMaxSplits) * Hv < (1LL << 31) && T < (1LL << 31) - 64 &&
                 gdn::prefill_chunk_cap(T, num_seqs) * Hv < (1LL << 31),
             GDN_ERR_UNSUPPORTED, "%s: grid or token count too large", fn);
-    const size_t ws_need = gdn::prefill_workspace_bytes(T, num_seqs, Hv);
-    REQUIRE(workspace && workspace_bytes >= ws_need, GDN_ERR_INVALID_ARG,
-            "%s: workspace of %zu bytes given, %zu needed", fn, workspace ? workspace_bytes : 0, ws_need);
+    const gdn::PrefillLayout lay = gdn::prefill_layout(T, num_seqs, Hv);
+    REQUIRE(workspace && workspace_bytes >= lay.bytes_min, GDN_ERR_INVALID_ARG,
+            "%s: workspace of %zu bytes given, %zu needed", fn, workspace ? workspace_bytes : 0, lay.bytes_min);
     REQUIRE(aligned(workspace, 256), GDN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
-    REQUIRE(!any_overlap(workspace, ws_need, out, obytes) && !any_overlap(workspace, ws_need, state_pool, pbytes),
+    const size_t ws_used = gdn::prefill_splits(lay, workspace_bytes, num_seqs) ? lay.bytes_full : lay.bytes_min;
+    REQUIRE(!any_overlap(workspace, ws_used, out, obytes) && !any_overlap(workspace, ws_used, state_pool, pbytes),
             GDN_ERR_INVALID_ARG, "%s: workspace overlaps out or state_pool", fn);
 
     gdn::PrefillArgs p;
@@ -376,7 +377,7 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     p.Hv = Hv;
     p.scale = scale;
     p.eps = 1e-6f;
-    const cudaError_t e = gdn::launch_prefill(p, workspace, static_cast<cudaStream_t>(stream), f16);
+    const cudaError_t e = gdn::launch_prefill(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), f16);
     if (e != cudaSuccess)
         return fail(GDN_ERR_CUDA, "%s: launch failed (TMA descriptors or kernel): %s", fn, cudaGetErrorString(e));
     g_last_error[0] = '\0';
@@ -502,11 +503,15 @@ extern "C" gdn_status gdn_prefill_chunked_noalloc(const void* q, const void* k, 
                                                   int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
                                                   int chunk_size, float scale, void* out,
                                                   int32_t* dev_status, gdn_stream_t stream) {
-    const size_t need = gdn_prefill_workspace_size(num_seqs, T, Hk, Hv, K, V, chunk_size);
+    // the scratch must hold the records; long sequences are split only when it also holds the
+    // split scratch
+    const size_t full = gdn_prefill_workspace_size(num_seqs, T, Hk, Hv, K, V, chunk_size);
+    const size_t need = full == 0 ? 0 : gdn::prefill_layout(T, num_seqs, Hv).bytes_min;
     REQUIRE(need <= kNoallocScratchBytes, GDN_ERR_UNSUPPORTED,
-            "gdn_prefill_chunked_noalloc: these sizes need %zu bytes of workspace; the library's static "
-            "scratch holds %zu (use gdn_prefill_chunked with a caller-owned workspace)",
-            need, kNoallocScratchBytes);
+            "gdn_prefill_chunked_noalloc: these sizes need %zu bytes of workspace (%zu without splitting "
+            "long sequences); the library's static scratch holds %zu (use gdn_prefill_chunked with a "
+            "caller-owned workspace)",
+            full, need, kNoallocScratchBytes);
     if (num_seqs == 0)  // nothing runs; the scratch is not needed
         return gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, pool_size, cache_indices,
                                    cu_seqlens, num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out, nullptr, 0,

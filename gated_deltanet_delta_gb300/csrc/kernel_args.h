@@ -89,6 +89,20 @@ struct WindowArgs {
     float eps;
 };
 
+// The sequential kernel's schedule.  A task is one chain of chunks, run for every value head: a
+// whole sequence, or one of the three chains of a sequence split into a first and a second part
+// (the first part from the pooled state; the second part once from a zero state and once from the
+// identity with v = 0, the two combined with the first part's end state by the fix-up kernel).
+constexpr int kPfOffThreads = 1024;      // the offsets kernel's CTA; more sequences: no split
+constexpr int kPfMaxSplits = 8;
+constexpr int kPfMinSplitChunks = 8;     // shorter sequences are never split
+constexpr long long kPfScratchRowBytes = 65536;
+enum PfTaskKind : int { kPfWhole = 0, kPfFirst = 1, kPfZero = 2, kPfOper = 3 };
+struct PfPlan {
+    int ntask, nsplit;
+    long long nscr;  // scratch chunks in use
+};
+
 struct PrefillArgs {
     const uint16_t* q;
     const uint16_t* k;
@@ -105,9 +119,20 @@ struct PrefillArgs {
     long long* chunk_off;  // workspace: first chunk of every sequence, [num_seqs + 1]
     longlong2* chunk_tab;  // workspace: per chunk (first token, sequence << 32 | length), [cap]
     uint8_t* records;      // workspace: one record per (chunk, value head), kPfRecordBytes each
+    // the schedule of the sequential kernel (written by the offsets kernel) and the scratch of the
+    // sequences it splits in two
+    PfPlan* plan;
+    int4* tasks;           // [num_seqs + 2 * max_splits]: (sequence, kind, split, 0)
+    int4* splits;          // [kPfMaxSplits]: (sequence, chunks of the first part, first scratch chunk, 0)
+    longlong2* scr_tab;    // per scratch chunk: (first token, split << 32 | length), [cap2]
+    float* scr_state;      // [max_splits][3][Hv][128][128] fp32: S_a, B', P (see prefill.cuh)
+    uint8_t* scr_rows;     // [cap2][Hv] kPfScratchRowBytes: O'^T (fp32) and F (bf16 hi, lo tiles)
     long long T;
     long long cap;         // chunk capacity of the workspace
+    long long cap2;        // scratch chunk capacity (second parts of split sequences)
     int pool_size, num_seqs, Hk, Hv;
+    int max_splits;        // 0: no sequence is split
+    int nsm;               // multiprocessors of the device (the split rule's measure of width)
     float scale, eps;
 };
 

@@ -47,24 +47,46 @@ bool encode_rows(CUtensorMap* map, const void* base, long long T, int H, bool f1
 
 long long prefill_chunk_cap(long long T, int num_seqs) { return (T + pf::C - 1) / pf::C + num_seqs; }
 
-size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) {
-    if (num_seqs <= 0) return 0;
-    const long long cap = prefill_chunk_cap(T, num_seqs);
-    return prefill_header_bytes(num_seqs, cap) + static_cast<size_t>(cap) * Hv * static_cast<size_t>(kPfRecordBytes);
+PrefillLayout prefill_layout(long long T, int num_seqs, int Hv) {
+    PrefillLayout l;
+    std::memset(&l, 0, sizeof(l));
+    if (num_seqs <= 0) return l;
+    auto up = [](size_t x, size_t m) { return (x + m - 1) / m * m; };
+    l.cap = prefill_chunk_cap(T, num_seqs);
+    l.cap2 = l.cap / 2;
+    l.tab = up(static_cast<size_t>(num_seqs + 1) * 8, 16);
+    l.plan = l.tab + static_cast<size_t>(l.cap) * 16;
+    l.tasks = l.plan + 16;
+    l.splits = l.tasks + static_cast<size_t>(num_seqs + 2 * kPfMaxSplits) * 16;
+    l.scr_tab = l.splits + static_cast<size_t>(kPfMaxSplits) * 16;
+    l.records = up(l.scr_tab + static_cast<size_t>(l.cap2) * 16, 1024);
+    l.scr_state = l.records + static_cast<size_t>(l.cap) * Hv * static_cast<size_t>(kPfRecordBytes);
+    l.bytes_min = l.scr_state;
+    l.scr_rows = l.scr_state + static_cast<size_t>(kPfMaxSplits) * 3 * Hv * pf::D * pf::D * sizeof(float);
+    l.bytes_full = l.scr_rows + static_cast<size_t>(l.cap2) * Hv * static_cast<size_t>(kPfScratchRowBytes);
+    return l;
 }
 
+size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) { return prefill_layout(T, num_seqs, Hv).bytes_full; }
+
 namespace {
+std::atomic<int> g_nsm[kMaxDevices];  // per device: multiprocessor count (0: not read yet)
+
 template <bool F16>
 cudaError_t set_smem_limits() {
     cudaError_t e = cudaFuncSetAttribute(gdn_prefill_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gdn_prefill_fixup_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pf::FX_SMEM));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(gdn_prefill_prep_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(pf::P_SMEM));
 }
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_t stream, bool f16) {
+cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                           bool f16) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -74,14 +96,29 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
         if (e != cudaSuccess) return e;
         e = set_smem_limits<true>();
         if (e != cudaSuccess) return e;
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_nsm[dev].store(nsm, std::memory_order_relaxed);
         g_smem_set[dev].store(1, std::memory_order_release);
     }
     PrefillArgs a = args;
+    const PrefillLayout l = prefill_layout(a.T, a.num_seqs, a.Hv);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    a.cap = prefill_chunk_cap(a.T, a.num_seqs);
+    a.cap = l.cap;
+    a.cap2 = l.cap2;
     a.chunk_off = reinterpret_cast<long long*>(ws);
-    a.chunk_tab = reinterpret_cast<longlong2*>(ws + prefill_tab_offset(a.num_seqs));
-    a.records = ws + prefill_header_bytes(a.num_seqs, a.cap);
+    a.chunk_tab = reinterpret_cast<longlong2*>(ws + l.tab);
+    a.plan = reinterpret_cast<PfPlan*>(ws + l.plan);
+    a.tasks = reinterpret_cast<int4*>(ws + l.tasks);
+    a.splits = reinterpret_cast<int4*>(ws + l.splits);
+    a.scr_tab = reinterpret_cast<longlong2*>(ws + l.scr_tab);
+    a.records = ws + l.records;
+    const bool split = prefill_splits(l, workspace_bytes, a.num_seqs);
+    a.max_splits = split ? kPfMaxSplits : 0;
+    a.scr_state = split ? reinterpret_cast<float*>(ws + l.scr_state) : nullptr;
+    a.scr_rows = split ? ws + l.scr_rows : nullptr;
+    a.nsm = g_nsm[dev].load(std::memory_order_relaxed);
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (a.T > 0) {  // with T = 0 every sequence is empty and no kernel reads the maps
@@ -89,8 +126,7 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
             !encode_rows(&maps.v, a.v, a.T, a.Hv, f16))
             return cudaErrorInvalidValue;
     }
-    gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.T, a.cap, a.chunk_off,
-                                                                a.chunk_tab);
+    gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a);
     if (a.T > 0) {  // one CTA per (chunk, key head, pair of value heads) of the capacity; the ones past
                     // the last chunk exit
         const int ngrp = (a.Hv / a.Hk + pf::PH - 1) / pf::PH;
@@ -98,9 +134,15 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, cudaStream_
         if (f16) gdn_prefill_prep_kernel<true><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
         else gdn_prefill_prep_kernel<false><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
     }
-    const unsigned grid = static_cast<unsigned>(a.num_seqs) * static_cast<unsigned>(a.Hv);
+    // one CTA per (task, value head); tasks past the schedule's count exit
+    const unsigned grid = static_cast<unsigned>(a.num_seqs + 2 * a.max_splits) * static_cast<unsigned>(a.Hv);
     if (f16) gdn_prefill_kernel<true><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
     else gdn_prefill_kernel<false><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
+    if (split && a.T > 0) {  // one CTA per SM, looping over the jobs (none when nothing was split)
+        const unsigned fgrid = static_cast<unsigned>(a.nsm > 0 ? a.nsm : 1);
+        if (f16) gdn_prefill_fixup_kernel<true><<<fgrid, pf::FX_NT, pf::FX_SMEM, stream>>>(a);
+        else gdn_prefill_fixup_kernel<false><<<fgrid, pf::FX_NT, pf::FX_SMEM, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -175,6 +175,16 @@ __device__ __forceinline__ uint16_t f32_to_in(float x) {
     if constexpr (F16) return __half_as_ushort(__float2half_rn(x));
     else return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xffffu);
 }
+// 2 floats to 2 elements of the input type (round to nearest even), the first in the low half.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_in_x2(float lo, float hi) {
+    if constexpr (F16) {
+        const __half2 h2 = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h2);
+    } else {
+        return pack_bf16x2(lo, hi);
+    }
+}
 // 8 floats to 8 elements of the input type (round to nearest even) in a uint4.
 template <bool F16>
 __device__ __forceinline__ uint4 pack_in_x8(const float* x) {
@@ -245,12 +255,32 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // The first chunk of every sequence, chunk_off[n] = sum over n' < n of ceil(len_n' / 64) (0 chunks
 // for a sequence whose bounds are invalid: the sequential kernel flags it), and the chunk table:
 // for chunk f of sequence n, (first token, n << 32 | length), for f < cap.  One CTA.
-constexpr int kPfOffThreads = 1024;
-__global__ void __launch_bounds__(kPfOffThreads)
-    gdn_prefill_offsets_kernel(const int64_t* cu_seqlens, int num_seqs, long long T, long long cap,
-                               long long* chunk_off, longlong2* chunk_tab) {
+//
+// Then the sequential kernel's schedule.  Its CTAs each run one chain (a sequence, a value head),
+// one CTA per SM, so a call takes about max(longest chain, chunk-steps / SMs) chunk times.  When one
+// sequence is much longer than the rest, its chain sets that time while most SMs idle.  The state
+// recurrence is affine per chunk, S_{c+1} = S_c A_c + B_c (A_c = gamma_L I - W^T diag(D_L rk) K,
+// B_c = U^T diag(D_L rk) K), and so are the chunk's outputs in its start state.  A sequence can
+// therefore be cut after n1 chunks into a first part, run as usual, and a second part, run twice
+// at the same time: from a zero state (outputs O', end state B') and, with v = 0, from the identity
+// (outputs F, end state P = the product of the A_c).  With S_a the first part's end state, the true
+// outputs of the second part are O' + S_a F and its end state is S_a P + B'; the fix-up kernel
+// forms them.  The rule: take the longest sequences in turn (at most max_splits, each at least
+// kPfMinSplitChunks chunks) and cut one in half when that lowers the estimate by at least 10 %
+// (the second part's two chains add n2 chunk-steps per head; the fix-up is not counted).  The tasks
+// list the split sequences' chains first (they are the longest), then the other sequences in order.
+// With more than kPfOffThreads sequences nothing is split.
+__global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(const __grid_constant__ PrefillArgs a) {
     __shared__ long long warp_tot[kPfOffThreads / 32];
     __shared__ long long carry;
+    __shared__ unsigned long long cand[kPfOffThreads / 32][kPfMaxSplits + 1];
+    __shared__ int top_seq[kPfMaxSplits + 1];
+    __shared__ long long top_cnt[kPfMaxSplits + 1];
+    __shared__ int s_nsplit, s_seq[kPfMaxSplits], s_n1[kPfMaxSplits], s_base[kPfMaxSplits];
+    const int num_seqs = a.num_seqs;
+    const long long T = a.T, cap = a.cap;
+    long long* chunk_off = a.chunk_off;
+    longlong2* chunk_tab = a.chunk_tab;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) carry = 0;
     __syncthreads();
@@ -258,8 +288,8 @@ __global__ void __launch_bounds__(kPfOffThreads)
         const int i = base + tid;
         long long cnt = 0, bos = 0, len = 0;
         if (i < num_seqs) {
-            bos = cu_seqlens[i];
-            const long long eos = cu_seqlens[i + 1];
+            bos = a.cu_seqlens[i];
+            const long long eos = a.cu_seqlens[i + 1];
             if (bos >= 0 && eos >= bos && eos <= T) {
                 len = eos - bos;
                 cnt = (len + pf::C - 1) / pf::C;
@@ -296,6 +326,111 @@ __global__ void __launch_bounds__(kPfOffThreads)
         __syncthreads();
     }
     if (tid == 0) chunk_off[num_seqs] = carry;
+
+    // ---- the schedule: the ms + 1 longest sequences (keys chunks << 16 | 0xffff - index, unique):
+    //      each warp takes its own top ms + 1 by rounds of a warp maximum, then warp 0 merges the
+    //      warps' sorted lists
+    const int ms = (a.max_splits > 0 && num_seqs <= kPfOffThreads)
+                       ? (a.max_splits < kPfMaxSplits ? a.max_splits : kPfMaxSplits) : 0;
+    if (ms > 0) {
+        unsigned long long key = 0;
+        if (tid < num_seqs) {
+            const long long b0 = a.cu_seqlens[tid], e0 = a.cu_seqlens[tid + 1];
+            if (b0 >= 0 && e0 >= b0 && e0 <= T && e0 > b0)
+                key = (static_cast<unsigned long long>((e0 - b0 + pf::C - 1) / pf::C) << 16) |
+                      static_cast<unsigned>(0xffff - tid);
+        }
+        const bool any = __syncthreads_or(key != 0) != 0;
+        if (any && warp * 32 < num_seqs) {
+            for (int r = 0; r <= ms; ++r) {
+                unsigned long long m = key;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const unsigned long long y = __shfl_xor_sync(kFullMask, m, o);
+                    m = y > m ? y : m;
+                }
+                if (key == m) key = 0;  // taken (keys are unique; 0 stays 0)
+                if (lane == 0) cand[warp][r] = m;
+            }
+        } else if (lane == 0) {
+            for (int r = 0; r <= ms; ++r) cand[warp][r] = 0;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int ptr = 0;
+            for (int r = 0; r <= ms; ++r) {
+                const unsigned long long mine = ptr <= ms ? cand[lane][ptr] : 0ull;
+                unsigned long long m = mine;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const unsigned long long y = __shfl_xor_sync(kFullMask, m, o);
+                    m = y > m ? y : m;
+                }
+                if (m != 0 && mine == m) ++ptr;
+                if (lane == 0) {
+                    top_seq[r] = m ? 0xffff - static_cast<int>(m & 0xffffu) : -1;
+                    top_cnt[r] = static_cast<long long>(m >> 16);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        int ns = 0;
+        long long nscr = 0;
+        if (ms > 0) {
+            const long long Hv = a.Hv, nsm = a.nsm > 0 ? a.nsm : 1;
+            long long W = Hv * carry;  // chunk-steps
+            long long longest_split = 0;
+            for (int j = 0; j < ms; ++j) {
+                const long long cj = top_cnt[j];
+                if (top_seq[j] < 0 || cj < kPfMinSplitChunks) break;
+                const long long next = top_seq[j + 1] >= 0 ? top_cnt[j + 1] : 0;
+                const long long n1 = (cj + 1) / 2, n2 = cj - n1;
+                if (nscr + n2 > a.cap2) break;
+                const long long old_b = max(max(longest_split, cj), (W + nsm - 1) / nsm);
+                const long long new_b = max(max(max(longest_split, n1), next), (W + Hv * n2 + nsm - 1) / nsm);
+                if (10 * new_b > 9 * old_b) break;
+                s_seq[ns] = top_seq[j];
+                s_n1[ns] = static_cast<int>(n1);
+                s_base[ns] = static_cast<int>(nscr);
+                a.splits[ns] = make_int4(top_seq[j], static_cast<int>(n1), static_cast<int>(nscr), 0);
+                nscr += n2;
+                W += Hv * n2;
+                longest_split = max(longest_split, n1);
+                ++ns;
+            }
+        }
+        s_nsplit = ns;
+        a.plan->ntask = num_seqs + 2 * ns;
+        a.plan->nsplit = ns;
+        a.plan->nscr = nscr;
+    }
+    __syncthreads();
+    const int ns = s_nsplit;
+    for (int i = tid; i < num_seqs; i += kPfOffThreads) {
+        int k = -1, below = 0;
+        for (int j = 0; j < ns; ++j) {
+            if (s_seq[j] == i) k = j;
+            if (s_seq[j] < i) ++below;
+        }
+        if (k >= 0) {
+            a.tasks[3 * k] = make_int4(i, kPfFirst, k, 0);
+            a.tasks[3 * k + 1] = make_int4(i, kPfZero, k, 0);
+            a.tasks[3 * k + 2] = make_int4(i, kPfOper, k, 0);
+        } else {
+            a.tasks[3 * ns + i - below] = make_int4(i, kPfWhole, 0, 0);
+        }
+    }
+    for (int j = 0; j < ns; ++j) {  // the scratch chunks: the second parts' chunks
+        const int n = s_seq[j];
+        const long long bos = a.cu_seqlens[n], len = a.cu_seqlens[n + 1] - bos;
+        const long long n1 = s_n1[j], cnt = (len + pf::C - 1) / pf::C;
+        for (long long c = n1 + tid; c < cnt; c += kPfOffThreads) {
+            const long long L = len - c * pf::C < pf::C ? len - c * pf::C : pf::C;
+            a.scr_tab[s_base[j] + c - n1] = make_longlong2(bos + c * pf::C, (static_cast<long long>(j) << 32) | L);
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -711,8 +846,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     __shared__ __align__(8) uint64_t bars[NBAR];
     __shared__ volatile int abort_flag;
 
-    const int n = blockIdx.x / a.Hv;
-    const int h = blockIdx.x - n * a.Hv;
+    const int task = blockIdx.x / a.Hv;
+    const int h = blockIdx.x - task * a.Hv;
+    if (task >= a.plan->ntask) return;
+    const int4 tk = a.tasks[task];
+    const int n = tk.x, kind = tk.y, split = tk.z;
     const int hk = h / (a.Hv / a.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == NW;
@@ -721,7 +859,8 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     const int qt = tid >> 7;     // workers: which quarter of the columns
 
     // ---- sequence bounds, pool slot and records (uniform over the CTA; bad ones are flagged and skipped)
-    const long long bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
+    long long bos = a.cu_seqlens[n];
+    const long long eos = a.cu_seqlens[n + 1];
     if (bos < 0 || eos < bos || eos > a.T || a.chunk_off[n + 1] > a.cap) {
         if (tid == 0) atomicOr(a.status, 2);
         return;
@@ -731,10 +870,28 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         if (tid == 0) atomicOr(a.status, 1);
         return;
     }
-    const long long Tn = eos - bos;
+    long long Tn = eos - bos;
+    long long chunk0 = a.chunk_off[n];
+    // a split sequence: the first part's n1 chunks, or the second part's chunks from a zero state
+    // (outputs O'^T and end state to the scratch) or from the identity with v = 0 (outputs F as bf16
+    // high / low tiles, end state P); sc = the second part's first scratch chunk
+    long long sc = 0;
+    float* Sdst = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * D * D;  // end state
+    if (kind != kPfWhole) {
+        const int4 sp = a.splits[split];
+        const long long n1 = sp.y;
+        sc = sp.z;
+        if (kind == kPfFirst) {
+            Tn = n1 * C;
+        } else {
+            bos += n1 * C;
+            Tn -= n1 * C;
+            chunk0 += n1;
+        }
+        Sdst = a.scr_state + ((static_cast<size_t>(split) * 3 + (kind - 1)) * a.Hv + h) * D * D;
+    }
     if (Tn == 0) return;
     const long long nch = (Tn + C - 1) / C;
-    const long long chunk0 = a.chunk_off[n];
     auto chunk_len = [&](long long c) -> int { return static_cast<int>(Tn - c * C < C ? Tn - c * C : C); };
     const bool short_last = chunk_len(nch - 1) < C;
 
@@ -829,12 +986,16 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     // outputs of chunk c from O (TMEM), tokens 16*qt .. (lane v)
     // Lane v holds tokens 16*qt .. 16*qt+15 of its column; an 8 x 8 transpose inside each group of
     // 8 lanes (three xor-shuffle stages) gives lane 8b + j the columns 8b .. 8b+7 (of the warp's
-    // 32) of token 8s + j, stored as one 16-byte vector per set s of 8 tokens.
+    // 32) of token 8s + j, stored as one 16-byte vector per set s of 8 tokens.  The second part of
+    // a split sequence writes its chunk's scratch row instead: O' in fp32 (rows t, 128 columns), or
+    // F as bf16 high and low K-major tiles (rows t, 128 columns), the B operand image of the fix-up
+    // kernel.
     auto outputs = [&](long long c) {
         const int L = chunk_len(c);
         float o16[16];
         tc::ld16(trow + TM_O + (c & 1) * 64 + 16 * qt, o16);
         tc::wait_ld();
+        uint8_t* scr = a.scr_rows + ((sc + c) * a.Hv + h) * kPfScratchRowBytes;
         const int j8 = lane & 7;
         uint16_t* o = a.out + static_cast<size_t>(bos + c * C) * vo_stride + h * D + (row - j8);
 #pragma unroll
@@ -854,7 +1015,18 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 }
             }
             const int t = 16 * qt + 8 * set + j8;
-            if (t < L) *reinterpret_cast<uint4*>(o + static_cast<size_t>(t) * vo_stride) = pack_in_x8<F16>(r);
+            if (kind == kPfZero) {
+                float4* d = reinterpret_cast<float4*>(scr + (static_cast<size_t>(t) * D + row - j8) * 4);
+                d[0] = make_float4(r[0], r[1], r[2], r[3]);
+                d[1] = make_float4(r[4], r[5], r[6], r[7]);
+            } else if (kind == kPfOper) {
+                uint4 hi, lo;
+                split_bf16x8(r, hi, lo);
+                *reinterpret_cast<uint4*>(scr + 32768 + tc::sw_chunk(t, (row - j8) >> 3, 64)) = hi;
+                *reinterpret_cast<uint4*>(scr + 49152 + tc::sw_chunk(t, (row - j8) >> 3, 64)) = lo;
+            } else if (t < L) {
+                *reinterpret_cast<uint4*>(o + static_cast<size_t>(t) * vo_stride) = pack_in_x8<F16>(r);
+            }
         }
     };
     // Delta^T (hi / lo) and Delta~^T = Delta^T diag(D_L rk) (hi / lo), lane v, 16 s each (over W,
@@ -1041,10 +1213,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 inflight |= 1u << i;
                 lastpar = (lastpar & ~(1u << i)) | (parity << i);
             };
-            // k or v rows by TMA (128-byte swizzled operand layout; rows past T arrive as zeros)
-            auto fetch_rows = [&](const CUtensorMap* map, int head, long long c, uint32_t dst, int bar,
+            // k or v rows from token z on by TMA (128-byte swizzled operand layout; rows past T arrive
+            // as zeros)
+            auto fetch_rows = [&](const CUtensorMap* map, int head, long long z64, uint32_t dst, int bar,
                                   uint32_t parity) {
-                const int z = static_cast<int>(bos + c * C);
+                const int z = static_cast<int>(z64);
                 tc::mbar_expect_tx(&bars[bar], 2 * 8192);
                 tc::tma_load_3d(sb + dst, map, 0, head, z, &bars[bar]);
                 tc::tma_load_3d(sb + dst + 8192, map, 64, head, z, &bars[bar]);
@@ -1058,9 +1231,13 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 mark(bar, parity);
             };
             auto fetch_k = [&](long long c) {
-                fetch_rows(&maps.k, hk, c, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
+                fetch_rows(&maps.k, hk, bos + c * C, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1),
+                           (c >> 1) & 1);
             };
-            auto fetch_v = [&](long long c) { fetch_rows(&maps.v, h, c, OFF_V, B_V, c & 1); };
+            // v = 0 for the identity-start chain: a box wholly past the last token reads as zeros
+            auto fetch_v = [&](long long c) {
+                fetch_rows(&maps.v, h, kind == kPfOper ? a.T : bos + c * C, OFF_V, B_V, c & 1);
+            };
             auto fetch_r1 = [&](long long c) { fetch_rec(c, REC_T4, REC_QT - REC_T4, OFF_T4, B_R1, c & 1); };
             auto fetch_qt = [&](long long c) { fetch_rec(c, REC_QT, REC_M - REC_QT, OFF_QT, B_QT, c & 1); };
             auto fetch_rm = [&](long long c) { fetch_rec(c, REC_M, REC_VEC - REC_M, OFF_M, B_RM, c & 1); };
@@ -1109,18 +1286,25 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     } else {
         // ---- workers
         do {
-            // gather the state from its pool slot: row v, columns 32*qt .. -> TMEM and S0 (bf16
-            // high parts in shared memory, low parts in TMEM)
+            // gather the state from its pool slot (or the zero / identity start of a split
+            // sequence's second part): row v, columns 32*qt .. -> TMEM and S0 (bf16 high parts in
+            // shared memory, low parts in TMEM)
             {
                 const float4* src = reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
                 float lo16[16];
 #pragma unroll
                 for (int c16 = 0; c16 < 2; ++c16) {
                     float v[16];
+                    if (kind <= kPfFirst) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float4 f = src[c16 * 4 + j];
-                        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 f = src[c16 * 4 + j];
+                            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+                        }
+                    } else {  // zero state, or the identity
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = (kind == kPfOper && row == 32 * qt + 16 * c16 + j) ? 1.f : 0.f;
                     }
                     tc::st16(trow + TM_S + 32 * qt + c16 * 16, v);
                     const int c8 = 4 * qt + 2 * c16;
@@ -1185,7 +1369,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         if (tid == 0) atomicOr(a.status, 4);
     } else if (warp < NW) {
         // ---- workers: scatter the final state back to its pool slot (row v, columns 32*qt ..)
-        float4* dst = reinterpret_cast<float4*>(Sg + static_cast<size_t>(row) * D + 32 * qt);
+        float4* dst = reinterpret_cast<float4*>(Sdst + static_cast<size_t>(row) * D + 32 * qt);
         float s32[32];
         ld32(trow + TM_S + 32 * qt, s32);
 #pragma unroll
@@ -1195,6 +1379,313 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
+}
+
+// ------------------------------------------------------------------------------------------------
+// The fix-up of split sequences (the rule and the algebra are described at the offsets kernel).
+// State jobs (the first max_splits CTAs of each head's column): for a split and a value head, the
+// end state S_a P + B' written to the pool slot (two 128 x 64 x 128 products, P read MN-major).
+// Chunk jobs: G consecutive scratch chunks of one split and value head, out[t] = O'[t] + S_a F[t]
+// for the chunks' tokens, one 128 x 64 x 128 product per chunk with S_a and F as bf16 high + low
+// parts (hi hi + hi lo + lo hi: about 16 bits, so the one rounding that counts is the output's).
+// G is the smallest chunk count (at least 2) whose jobs, with the state jobs, fit one per CTA of
+// a grid of one CTA per SM (each holds 226 KB of shared memory), which loops over the jobs if they
+// do not fit.  A chunk job streams: its control lane keeps F three chunks ahead in a ring of four shared-memory
+// buffers (bulk copies) and issues each chunk's products into one of two TMEM buffers as soon as
+// that buffer has been read; eight output warps (TMEM lane = row v, two column halves) copy the
+// product tile into shared memory as [t][v], then add O' (token-major, read one chunk ahead) and
+// store the outputs row by row, coalesced, so the copies, the products and the stores of
+// different chunks overlap.
+namespace pf {
+constexpr int FX_NW = 8;                       // output warps; the control warp is warp FX_NW
+constexpr int FX_NT = 32 * (FX_NW + 1);
+constexpr int FX_RING = 4;
+constexpr uint32_t FX_A = 0;                   // S_a hi, lo: 128 rows v x 128 columns, K-major, 32 KB each
+constexpr uint32_t FX_B = 65536;               // ring of B buffers (hi, lo: 16 KB each)
+constexpr uint32_t FX_STG = FX_B + FX_RING * 32768;  // the product tile, fp32 [64 t][128 v]
+constexpr uint32_t FX_USED = FX_STG + 32768;
+constexpr uint32_t FX_SMEM = FX_USED + 1024;   // + alignment slack
+constexpr uint32_t FX_COLS = 128;              // two 64-column product buffers
+}  // namespace pf
+
+template <bool F16>
+__global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const __grid_constant__ PrefillArgs a) {
+    using namespace pf;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    // F_FULL + s: F in ring buffer s; MMA_DONE + b: products in TMEM buffer b done; D_FREE + b:
+    // TMEM buffer b read by the output warps
+    enum { F_FULL = 0, MMA_DONE = FX_RING, D_FREE = FX_RING + 2, FX_NBAR = FX_RING + 4 };
+    __shared__ __align__(8) uint64_t bars[FX_NBAR];
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & 127, half = (tid >> 7) & 1;  // output warps
+    const bool control = warp == FX_NW;
+    const int nsplit = a.plan->nsplit;
+    const long long nscr = a.plan->nscr;
+    if (nsplit == 0) return;
+
+    // jobs per value head: nsplit state jobs, then the chunk jobs of every split, G chunks each;
+    // G is the smallest (at least 2) whose jobs fit one per CTA of the grid, else the longest part
+    long long G = (nscr * a.Hv + gridDim.x - 1) / gridDim.x, longest = 0, J = 0;
+    G = G < 2 ? 2 : G;
+    for (int sp = 0; sp < nsplit; ++sp) {
+        const long long n2 = (sp + 1 < nsplit ? a.splits[sp + 1].z : nscr) - a.splits[sp].z;
+        longest = n2 > longest ? n2 : longest;
+    }
+    for (;; ++G) {
+        J = nsplit;
+        for (int sp = 0; sp < nsplit; ++sp)
+            J += ((sp + 1 < nsplit ? a.splits[sp + 1].z : nscr) - a.splits[sp].z + G - 1) / G;
+        if (J * a.Hv <= gridDim.x || G >= longest) break;
+    }
+    const long long total = J * a.Hv;
+    if (static_cast<long long>(blockIdx.x) >= total) return;
+
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = tc::smem_u32(sm);
+    if (warp == 0) tc::tmem_alloc(&tmem_slot, FX_COLS);
+    if (tid == 0) abort_flag = 0;
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = tmem_slot;
+    int h = 0, split = -1;
+    bool state_job = false;
+    long long c0 = 0, c1 = 0;
+    const uint32_t trow = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint64_t dAh = tc::sdesc(sb + FX_A, 16, 1024), dAl = tc::sdesc(sb + FX_A + 32768, 16, 1024);
+    const size_t DD = static_cast<size_t>(D) * D;
+    auto state_of = [&](int which) -> const float* {
+        return a.scr_state + (static_cast<size_t>(split) * 3 + which) * a.Hv * DD + static_cast<size_t>(h) * DD;
+    };
+    // output warps: 128 rows of fp32, nc columns from col0 per thread, to bf16 high / low 128-byte
+    // swizzled tiles of 128 rows; the thread's first 16-byte chunk is c8_0
+    auto convert_rows = [&](const float* src, int col0, int c8_0, uint32_t dst_hi, uint32_t dst_lo, int nc) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(row) * D + col0);
+#pragma unroll 4
+        for (int cc = 0; cc < nc / 8; ++cc) {
+            const float4 x0 = s4[2 * cc], x1 = s4[2 * cc + 1];
+            const float v8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint4 hi, lo;
+            split_bf16x8(v8, hi, lo);
+            *reinterpret_cast<uint4*>(sm + dst_hi + tc::sw_chunk(row, c8_0 + cc, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + dst_lo + tc::sw_chunk(row, c8_0 + cc, 128)) = lo;
+        }
+    };
+    // control: TMEM buffer b = S_a times ring buffer s, as hi hi + hi lo + lo hi; B K-major (F: 64
+    // rows t, 128 columns) or MN-major (P: 128 rows k', 64 columns, one swizzle span: no leading
+    // offset), committed to MMA_DONE + b
+    auto products = [&](int b, int s, bool b_mn) {
+        const uint32_t base = sb + FX_B + 32768u * s;
+        const uint64_t Bh = b_mn ? tc::sdesc(base, 16384, 1024) : tc::sdesc(base, 16, 1024);
+        const uint64_t Bl = b_mn ? tc::sdesc(base + 16384, 16384, 1024) : tc::sdesc(base + 16384, 16, 1024);
+        const uint32_t id = tc::idesc_bf16(128, 64, 0, b_mn ? 1 : 0, 0);
+        const uint64_t A[3] = {dAh, dAh, dAl};
+        const uint64_t B[3] = {Bh, Bl, Bh};
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint32_t bo = b_mn ? ks * 2048 : (ks >> 2) * 8192 + (ks & 3) * 32;
+                tc::mma_bf16(tm + 64 * b, dadd(A[p], ao), dadd(B[p], bo), id, (p | ks) != 0);
+            }
+        tc::commit(&bars[MMA_DONE + b]);
+    };
+    auto ctl_wait = [&](int i, uint32_t parity) -> bool {
+        if (tc::mbar_wait_or_abort(&bars[i], parity, kWaitLimit, &abort_flag)) return true;
+        abort_flag = 1;
+        return false;
+    };
+    auto warp_wait = [&](int i, uint32_t parity) -> bool {
+        bool ok = tc::mbar_sleep_wait(&bars[i], parity, kSleepWaitLimit, 1000u, &abort_flag);
+        ok = __all_sync(kFullMask, ok ? 1 : 0) != 0;
+        if (!ok && lane == 0) abort_flag = 1;
+        tc::fence_after();
+        return ok;
+    };
+    // output warps: TMEM buffer b, this thread's 32 columns; then hand the buffer back
+    auto ld_d = [&](int b, float (&d)[32], bool release) {
+        float x[16], y[16];
+        tc::ld16(trow + 64 * b + 32 * half, x);
+        tc::ld16(trow + 64 * b + 32 * half + 16, y);
+        tc::wait_ld();
+        if (release) {
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[D_FREE + b]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            d[i] = x[i];
+            d[16 + i] = y[i];
+        }
+    };
+
+    for (long long job = blockIdx.x; job < total && !abort_flag; job += gridDim.x) {
+    h = static_cast<int>(job / J);
+    {
+        long long r = job - static_cast<long long>(h) * J;
+        state_job = r < nsplit;
+        split = -1;
+        if (state_job) {
+            split = static_cast<int>(r);
+        } else {
+            r -= nsplit;
+            for (int sp = 0; sp < nsplit; ++sp) {
+                const long long base = a.splits[sp].z;
+                const long long top = sp + 1 < nsplit ? a.splits[sp + 1].z : nscr;
+                const long long ng = (top - base + G - 1) / G;
+                if (r < ng) {
+                    split = sp;
+                    c0 = base + r * G;
+                    c1 = c0 + G < top ? c0 + G : top;
+                    break;
+                }
+                r -= ng;
+            }
+        }
+    }
+    const long long slot = split < 0 ? -1 : a.cache_indices[a.splits[split].x];
+    if (slot < 0 || slot >= a.pool_size) continue;  // the sequential kernel flagged and skipped it
+    const int n = static_cast<int>(c1 - c0);
+    // fresh barriers for every job (everything of the previous job has completed)
+    if (tid == 0)
+        for (int i = 0; i < FX_NBAR; ++i) {
+            if (job != blockIdx.x)
+                asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(&bars[i])) : "memory");
+            tc::mbar_init(&bars[i], i >= D_FREE ? FX_NW : 1);
+        }
+    __syncthreads();
+
+    if (!control) convert_rows(state_of(0), 64 * half, 8 * half, FX_A, FX_A + 32768, 64);  // S_a -> A
+    if (state_job) {
+        // P's columns 64j .. 64j+63 -> MN-major B in ring buffer j (rows k', 64 columns; 32 per
+        // thread), both products at once
+        if (!control)
+            for (int j = 0; j < 2; ++j)
+                convert_rows(state_of(2), 64 * j + 32 * half, 4 * half, FX_B + 32768u * j, FX_B + 32768u * j + 16384, 32);
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncthreads();
+        if (control) {
+            if (lane == 0) {
+                tc::fence_after();
+                products(0, 0, true);
+                products(1, 1, true);
+            }
+            __syncwarp();
+        } else {
+            float4* Sdst4 = reinterpret_cast<float4*>(a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * DD);
+            const float4* Bz4 = reinterpret_cast<const float4*>(state_of(1));
+            for (int j = 0; j < 2; ++j) {
+                if (!warp_wait(MMA_DONE + j, 0)) break;
+                float d[32];
+                ld_d(j, d, false);
+                const size_t o4 = (static_cast<size_t>(row) * D + 64 * j + 32 * half) / 4;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 b0 = Bz4[o4 + i];
+                    Sdst4[o4 + i] = make_float4(d[4 * i] + b0.x, d[4 * i + 1] + b0.y, d[4 * i + 2] + b0.z,
+                                                d[4 * i + 3] + b0.w);
+                }
+            }
+        }
+    } else if (control) {
+        if (lane == 0) {
+            uint32_t inflight = 0;  // ring buffers with a copy in flight (for the drain after an abort)
+            auto fetch_f = [&](int i) {  // F of chunk c0 + i -> ring buffer i % FX_RING
+                const int s = i % FX_RING;
+                const uint8_t* src = a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes + 32768;
+                tc::mbar_expect_tx(&bars[F_FULL + s], 32768);
+                tc::bulk_load(sb + FX_B + 32768u * s, src, 32768, &bars[F_FULL + s]);
+                inflight |= 1u << s;
+            };
+            for (int i = 0; i < n && i < FX_RING; ++i) fetch_f(i);
+        }
+        __syncwarp();
+        tc::fence_before();
+        __syncthreads();  // A is in place
+        if (lane == 0) {
+            for (int i = 0; i < n; ++i) {
+                const int s = i % FX_RING, b = i & 1;
+                if (!ctl_wait(F_FULL + s, (i / FX_RING) & 1)) break;
+                if (i >= 2 && !ctl_wait(D_FREE + b, ((i - 2) >> 1) & 1)) break;
+                tc::fence_after();
+                products(b, s, false);
+                // refill the buffer of chunk i - 1 once its products are done
+                if (i >= 1 && i - 1 + FX_RING < n) {
+                    if (!ctl_wait(MMA_DONE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
+                    const int i4 = i - 1 + FX_RING, s4 = i4 % FX_RING;
+                    const uint8_t* src = a.scr_rows + ((c0 + i4) * a.Hv + h) * kPfScratchRowBytes + 32768;
+                    tc::mbar_expect_tx(&bars[F_FULL + s4], 32768);
+                    tc::bulk_load(sb + FX_B + 32768u * s4, src, 32768, &bars[F_FULL + s4]);
+                }
+            }
+            if (abort_flag) {  // one more bounded wait on every copy and product that may be in flight
+                for (int s = 0; s < FX_RING; ++s) tc::mbar_wait(&bars[F_FULL + s], 0, 1u << 20);
+                for (int b = 0; b < 2; ++b) tc::mbar_wait(&bars[MMA_DONE + b], 0, 1u << 20);
+            }
+        }
+        __syncwarp();
+    } else {
+        tc::fence_proxy_async();  // A (generic-proxy writes) before the tensor core reads it
+        tc::fence_before();
+        __syncthreads();
+        // unit u = tid + 256 k (k < 8) of a chunk: token u >> 5, columns 4 (u & 31) .. + 3
+        auto load_o = [&](int i, float4 (&o4)[8]) {
+            const float4* op = reinterpret_cast<const float4*>(a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o4[k] = op[tid + 256 * k];
+        };
+        float* stg = reinterpret_cast<float*>(sm + FX_STG);
+        float4 ocur[8], onext[8];
+        longlong2 ecur = a.scr_tab[c0], enext = ecur;  // (first token, split << 32 | length)
+        load_o(0, ocur);
+        if (n > 1) {
+            load_o(1, onext);
+            enext = a.scr_tab[c0 + 1];
+        }
+        for (int i = 0; i < n; ++i) {
+            const int b = i & 1;
+            if (!warp_wait(MMA_DONE + b, (i >> 1) & 1)) break;
+            float d[32];
+            ld_d(b, d, true);
+            // the product tile to shared memory as [t][v] (lanes: consecutive v, no bank conflict)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) stg[(32 * half + k) * D + row] = d[k];
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * FX_NW) : "memory");
+            const longlong2 e = ecur;
+            const int L = static_cast<int>(e.y & 0xffffffffLL);
+            uint16_t* o = a.out + static_cast<size_t>(e.x) * a.Hv * D + static_cast<size_t>(h) * D;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int u = tid + 256 * k, t = u >> 5, c4 = u & 31;
+                const float4 p = *reinterpret_cast<const float4*>(stg + t * D + 4 * c4);
+                const float x[4] = {p.x + ocur[k].x, p.y + ocur[k].y, p.z + ocur[k].z, p.w + ocur[k].w};
+                if (t < L)
+                    *reinterpret_cast<uint2*>(o + static_cast<size_t>(t) * a.Hv * D + 4 * c4) =
+                        make_uint2(pack_in_x2<F16>(x[0], x[1]), pack_in_x2<F16>(x[2], x[3]));
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * FX_NW) : "memory");  // the tile is read
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ocur[k] = onext[k];
+            ecur = enext;
+            if (i + 2 < n) {
+                load_o(i + 2, onext);
+                enext = a.scr_tab[c0 + i + 2];
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();  // the job is done: its copies, products and TMEM reads have completed
+    tc::fence_after();
+    }
+    if (abort_flag && tid == 0) atomicOr(a.status, 4);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, FX_COLS);
 }
 
 }  // namespace gdn

@@ -171,11 +171,21 @@ gdn_status comba_forward(float* state, const void* q, const void* k, const void*
 
 /*
  * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_chunked needs for these
- * sizes: the first chunk of every sequence (8 bytes each, num_seqs + 1 of them, padded to 1 KB)
- * and one 66,560-byte record per (chunk, value head) for up to ceil(T / 64) + num_seqs chunks
- * (what a chunk contributes independently of the carried state: Tw, Tu and the output-scaled M
- * split into bf16 high / low parts, the output-scaled q rows, and per-token scales).  Pure host function; returns 0 when num_seqs is 0 and
- * for sizes gdn_prefill_chunked does not support.
+ * sizes, with cap = ceil(T / 64) + num_seqs chunks and cap2 = floor(cap / 2):
+ *   - a header padded to 1 KB: the first chunk of every sequence (8 bytes each, num_seqs + 1 of
+ *     them, padded to 16 bytes), a 16-byte entry per chunk, and the schedule of the sequential
+ *     kernel (16 bytes, 16 per task for num_seqs + 16 tasks, 16 per split for 8 splits, 16 per
+ *     scratch chunk for cap2 of them);
+ *   - one 66,560-byte record per (chunk, value head) (what a chunk contributes independently of
+ *     the carried state: Tw, Tu and the output-scaled M split into bf16 high / low parts, the
+ *     output-scaled q rows, and per-token scales);
+ *   - the scratch of sequences split in two (a long sequence's second half runs next to its first
+ *     half and is corrected afterwards): 3 x 65,536 bytes per split (at most 8) and value head,
+ *     and 65,536 bytes per scratch chunk (cap2) and value head.
+ * A workspace holding the header and the records but not the split scratch is also accepted;
+ * then no sequence is split (same results up to rounding, slower when one sequence dominates).
+ * Pure host function; returns 0 when num_seqs is 0 and for sizes gdn_prefill_chunked does not
+ * support.
  */
 size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K, int V,
                                   int chunk_size);
@@ -203,8 +213,9 @@ size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, int Hv, int K
  *   cache_indices  int64 [num_seqs]   distinct slots; duplicates give an undefined result
  *   cu_seqlens     int64 [num_seqs + 1]
  *   out            bf16 [T, Hv, V]    16-byte aligned; tokens of skipped sequences are not written
- *   workspace      device buffer of at least gdn_prefill_workspace_size(...) bytes, 256-byte
- *                  aligned, overlapping neither out nor state_pool (NULL only when num_seqs is 0);
+ *   workspace      device buffer of gdn_prefill_workspace_size(...) bytes (or at least its header
+ *                  and records, see there; workspace_bytes tells which), 256-byte aligned,
+ *                  overlapping neither out nor state_pool (NULL only when num_seqs is 0);
  *                  contents need not be initialised and are scratch after the call; calls that
  *                  share a workspace must not overlap on the GPU
  *   dev_status     device int32, zeroed by the caller; the kernels OR in GDN_STATUS_* bits for a
@@ -247,10 +258,11 @@ gdn_status gdn_prefill_chunked_f16(const void* q, const void* k, const void* v, 
  * The workspace is a 64 MiB array of the library's own device memory (a static device variable,
  * which every GPU that loads the library holds until the process exits).  The call allocates and
  * frees nothing:
- *   - Sizes whose gdn_prefill_workspace_size(...) exceeds 64 MiB are rejected with
- *     GDN_ERR_UNSUPPORTED before anything runs (use gdn_prefill_chunked then).  About 1,000
- *     (chunk, value head) records fit: for instance T = 3,000 tokens over a few sequences with
- *     Hv = 16.
+ *   - Sizes whose header and records (gdn_prefill_workspace_size without the split scratch)
+ *     exceed 64 MiB are rejected with GDN_ERR_UNSUPPORTED before anything runs (use
+ *     gdn_prefill_chunked then).  About 1,000 (chunk, value head) records fit: for instance
+ *     T = 3,000 tokens over a few sequences with Hv = 16.  Long sequences are split only when the
+ *     whole gdn_prefill_workspace_size(...) fits.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *     that device current) and keeps it; make that first call before any stream capture.
  *   - Every call on a device shares the one array.  Nothing in it has to start at zero: each call

@@ -87,14 +87,20 @@ def test_window_validation(lib):
 
 
 def test_prefill_workspace_size(lib):
-    # chunk offsets (8 bytes per sequence + 1, padded to 16) and the chunk table (16 bytes per chunk),
-    # padded to 1 KB, + one 66,560-byte record per (chunk, value head), for up to
-    # cap = ceil(T / 64) + num_seqs chunks
-    def header(n, cap):
-        return ((8 * (n + 1) + 15) // 16 * 16 + 16 * cap + 1023) // 1024 * 1024
-    assert header(4, 244) == 4096 and header(200, 202) == 5120
-    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == 4096 + (240 + 4) * 32 * 66560
-    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == 5120 + (2 + 200) * 2 * 66560
+    # header: chunk offsets (8 bytes per sequence + 1, padded to 16), the chunk table (16 bytes per
+    # chunk), the schedule (16 bytes, then 16 per task for num_seqs + 16 tasks, 16 per split for 8
+    # splits, 16 per scratch chunk), padded to 1 KB; one 66,560-byte record per (chunk, value head)
+    # for up to cap = ceil(T / 64) + num_seqs chunks; then the split scratch: 3 states of 64 KB per
+    # split (8) and value head, one 64 KB row per scratch chunk (cap // 2) and value head
+    def size(n, T, Hv):
+        cap = (T + 63) // 64 + n
+        cap2 = cap // 2
+        head = (8 * (n + 1) + 15) // 16 * 16 + 16 * cap + 16 + 16 * (n + 16) + 16 * 8 + 16 * cap2
+        head = (head + 1023) // 1024 * 1024
+        return head + cap * Hv * 66560 + 8 * 3 * Hv * 65536 + cap2 * Hv * 65536
+    assert size(4, 15360, 32) == 7168 + 244 * 32 * 66560 + 24 * 32 * 65536 + 122 * 32 * 65536
+    assert gdn.gdn_prefill_workspace_size(4, 15360, 16, 32, 128, 128, 64) == size(4, 15360, 32)
+    assert gdn.gdn_prefill_workspace_size(200, 65, 1, 2, 128, 128, 64) == size(200, 65, 2)
     assert gdn.gdn_prefill_workspace_size(0, 100, 1, 1, 128, 128, 64) == 0
     assert gdn.gdn_prefill_workspace_size(1, 100, 1, 1, 64, 128, 64) == 0    # unsupported K
     assert gdn.gdn_prefill_workspace_size(1, 100, 2, 3, 128, 128, 64) == 0   # Hv % Hk != 0
@@ -115,7 +121,11 @@ def test_prefill_validation(lib, name):
                  ws, ws_bytes, P, N)
     ws = ctypes.c_void_p(1 << 44)
     assert call(N, 0) == gdn.GDN_ERR_INVALID_ARG and "workspace" in gdn.last_error()
-    assert call(ws, need - 1) == gdn.GDN_ERR_INVALID_ARG and "needed" in gdn.last_error()
+    # the header and the records are required; the split scratch (3 states per split for 8 splits,
+    # one row per scratch chunk, cap // 2 = 2 of them, 64 KB each per value head) is optional
+    need_min = need - (8 * 3 * 2 + 2 * 2) * 65536
+    assert call(ws, need_min - 1) == gdn.GDN_ERR_INVALID_ARG and "needed" in gdn.last_error()
+    assert str(need_min) in gdn.last_error()
     assert gdn.last_error().startswith(name + ":")
     assert call(ctypes.c_void_p((1 << 44) + 16), need) == gdn.GDN_ERR_INVALID_ARG   # misaligned
     assert call(ctypes.c_void_p((1 << 40) - 256), need) == gdn.GDN_ERR_INVALID_ARG  # overlaps out

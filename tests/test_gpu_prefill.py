@@ -170,20 +170,70 @@ def test_zero_key_and_query_rows():
     assert not host(out)[[1, 64, 72]].any()
 
 
-@pytest.mark.parametrize("case", ["no_update", "no_decay"])
-def test_gate_extremes(case):
+@pytest.mark.parametrize("seqlens", [[150, 64], [700]])
+@pytest.mark.parametrize("case", ["no_update", "no_decay", "full_decay"])
+def test_gate_extremes(case, seqlens):
     # b -> -inf: beta = 0, the state only decays; a -> -inf: the log-gate is 0 (no decay), so the
-    # state carries unchanged in scale over 3 chunks and gamma_L = 1 on every chunk
-    x = gi.gdn_prefill_inputs(gi.rng(41), [150, 64], 1, 2, 128, 128, pool=2, mild_gates=True)
+    # state carries unchanged in scale and gamma_L = 1 on every chunk; a -> +inf: the chunk decay
+    # gamma_L underflows to 0 in fp32 and the update overwrites the state.  700 tokens (11 chunks)
+    # with Hv = 2 is a sequence the schedule cuts in two.
+    x = gi.gdn_prefill_inputs(gi.rng(41), seqlens, 1, 2, 128, 128, pool=2, mild_gates=True)
     if case == "no_update":
         x["b"][:] = -60.0
-    else:
+    elif case == "no_decay":
         x["a"][:] = -60.0
+    else:
+        x["a"][:] = 40.0
     d = _to_dev(x)
     scale = 128 ** -0.5
     out, st = _gpu(d, scale)
     assert st == 0
     _check_all(x, d, out, scale)
+
+
+def _split_scratch_bytes(N, T, Hv):
+    # the optional tail of the workspace: 3 states per split (8 splits) and one row per scratch
+    # chunk (cap // 2), 64 KB each per value head
+    cap = (T + 63) // 64 + N
+    return (8 * 3 * Hv + (cap // 2) * Hv) * 65536
+
+
+def _gpu_ws(d, scale, ws_bytes):
+    T, Hv = d["v"].shape[0], d["v"].shape[1]
+    out = torch.full((T, Hv, 128), SENTINEL, dtype=d["v"].dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                            d["state_pool"], d["cache_indices"], d["cu_seqlens"], 64, scale=scale,
+                            out=out, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    return out, int(status.item())
+
+
+@pytest.mark.parametrize("mild", [False, True])
+@pytest.mark.parametrize("seqlens", [[1300 + 20, 900, 700, 40], [2000, 3], [64 * 8]])
+def test_long_sequences_split_in_two(seqlens, mild):
+    # Sequences of 8 or more chunks that set the call's length are cut in two: the second half runs
+    # from a zero state and from the identity (v = 0) next to the first half, and the fix-up kernel
+    # combines them with the first half's end state.  The first case splits two sequences (21 and 15
+    # chunks; 11 chunks would not shorten the call), the second one, the third exactly 8 chunks.
+    # With a workspace that lacks the split scratch nothing is split.  Both match the oracle, and
+    # each other within the output tolerance.
+    N = len(seqlens)
+    x = gi.gdn_prefill_inputs(gi.rng(600 + sum(seqlens) + mild), seqlens, 1, 2, 128, 128, pool=N + 2,
+                              mild_gates=mild)
+    scale = 128 ** -0.5
+    full = gdn.gdn_prefill_workspace_size(N, x["T"], 1, 2, 128, 128, 64)
+    outs, pools = [], []
+    for ws_bytes in (full, full - _split_scratch_bytes(N, x["T"], 2)):
+        d = _to_dev(x)
+        out, st = _gpu_ws(d, scale, ws_bytes)
+        assert st == 0
+        _check_all(x, d, out, scale)
+        outs.append(host(out))
+        pools.append(host(d["state_pool"]))
+    assert max_rel_err(outs[0], outs[1]) <= OUT_TOL
+    assert max_rel_err(pools[0], pools[1]) <= STATE_TOL
 
 
 def test_all_sequences_empty():
