@@ -277,7 +277,11 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
     __shared__ int top_seq[kPfMaxSplits + 1];
     __shared__ long long top_cnt[kPfMaxSplits + 1];
     __shared__ int s_nsplit, s_seq[kPfMaxSplits], s_n1[kPfMaxSplits], s_base[kPfMaxSplits];
+    // up to kPfOffThreads sequences (one tile): each sequence's first chunk, first token and length
+    __shared__ long long s_off[kPfOffThreads + 1], s_bos[kPfOffThreads], s_len[kPfOffThreads];
     const int num_seqs = a.num_seqs;
+    const bool one_tile = num_seqs <= kPfOffThreads;
+    long long my_cnt = 0;  // one tile: this thread's sequence's chunks
     const long long T = a.T, cap = a.cap;
     long long* chunk_off = a.chunk_off;
     longlong2* chunk_tab = a.chunk_tab;
@@ -316,9 +320,16 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
         const long long before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - cnt;
         if (i < num_seqs) {
             chunk_off[i] = before;
-            for (long long j = 0; j < cnt && before + j < cap; ++j) {
-                const long long L = len - j * pf::C < pf::C ? len - j * pf::C : pf::C;
-                chunk_tab[before + j] = make_longlong2(bos + j * pf::C, (static_cast<long long>(i) << 32) | L);
+            if (one_tile) {  // the table is filled in parallel below
+                s_off[i] = before;
+                s_bos[i] = bos;
+                s_len[i] = len;
+                my_cnt = cnt;
+            } else {
+                for (long long j = 0; j < cnt && before + j < cap; ++j) {
+                    const long long L = len - j * pf::C < pf::C ? len - j * pf::C : pf::C;
+                    chunk_tab[before + j] = make_longlong2(bos + j * pf::C, (static_cast<long long>(i) << 32) | L);
+                }
             }
         }
         __syncthreads();
@@ -326,6 +337,22 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
         __syncthreads();
     }
     if (tid == 0) chunk_off[num_seqs] = carry;
+    if (one_tile) {
+        // chunk f belongs to the last sequence whose first chunk is <= f (empty sequences share
+        // their successor's first chunk and come before it)
+        const long long nch = carry < cap ? carry : cap;
+        for (long long f = tid; f < nch; f += kPfOffThreads) {
+            int lo = 0, hi = num_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= f) lo = mid;
+                else hi = mid - 1;
+            }
+            const long long j = f - s_off[lo], len = s_len[lo];
+            const long long L = len - j * pf::C < pf::C ? len - j * pf::C : pf::C;
+            chunk_tab[f] = make_longlong2(s_bos[lo] + j * pf::C, (static_cast<long long>(lo) << 32) | L);
+        }
+    }
 
     // ---- the schedule: the ms + 1 longest sequences (keys chunks << 16 | 0xffff - index, unique):
     //      each warp takes its own top ms + 1 by rounds of a warp maximum, then warp 0 merges the
@@ -333,32 +360,32 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
     const int ms = (a.max_splits > 0 && num_seqs <= kPfOffThreads)
                        ? (a.max_splits < kPfMaxSplits ? a.max_splits : kPfMaxSplits) : 0;
     if (ms > 0) {
+        // (sequences of fewer than kPfMinSplitChunks chunks are never split: key 0)
         unsigned long long key = 0;
-        if (tid < num_seqs) {
-            const long long b0 = a.cu_seqlens[tid], e0 = a.cu_seqlens[tid + 1];
-            if (b0 >= 0 && e0 >= b0 && e0 <= T && e0 > b0)
-                key = (static_cast<unsigned long long>((e0 - b0 + pf::C - 1) / pf::C) << 16) |
-                      static_cast<unsigned>(0xffff - tid);
-        }
-        const bool any = __syncthreads_or(key != 0) != 0;
-        if (any && warp * 32 < num_seqs) {
-            for (int r = 0; r <= ms; ++r) {
-                unsigned long long m = key;
+        if (tid < num_seqs && my_cnt >= kPfMinSplitChunks)
+            key = (static_cast<unsigned long long>(my_cnt) << 16) | static_cast<unsigned>(0xffff - tid);
+        {
+            int r = 0;
+            if (__any_sync(kFullMask, key != 0)) {
+                for (; r <= ms; ++r) {
+                    unsigned long long m = key;
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) {
-                    const unsigned long long y = __shfl_xor_sync(kFullMask, m, o);
-                    m = y > m ? y : m;
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        const unsigned long long y = __shfl_xor_sync(kFullMask, m, o);
+                        m = y > m ? y : m;
+                    }
+                    if (m == 0) break;      // the rest of the warp's list is empty
+                    if (key == m) key = 0;  // taken (keys are unique)
+                    if (lane == 0) cand[warp][r] = m;
                 }
-                if (key == m) key = 0;  // taken (keys are unique; 0 stays 0)
-                if (lane == 0) cand[warp][r] = m;
             }
-        } else if (lane == 0) {
-            for (int r = 0; r <= ms; ++r) cand[warp][r] = 0;
+            if (lane == 0)
+                for (; r <= ms; ++r) cand[warp][r] = 0;
         }
         __syncthreads();
         if (warp == 0) {
-            int ptr = 0;
-            for (int r = 0; r <= ms; ++r) {
+            int ptr = 0, r = 0;
+            for (; r <= ms; ++r) {
                 const unsigned long long mine = ptr <= ms ? cand[lane][ptr] : 0ull;
                 unsigned long long m = mine;
 #pragma unroll
@@ -366,12 +393,18 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
                     const unsigned long long y = __shfl_xor_sync(kFullMask, m, o);
                     m = y > m ? y : m;
                 }
-                if (m != 0 && mine == m) ++ptr;
+                if (m == 0) break;
+                if (mine == m) ++ptr;
                 if (lane == 0) {
-                    top_seq[r] = m ? 0xffff - static_cast<int>(m & 0xffffu) : -1;
+                    top_seq[r] = 0xffff - static_cast<int>(m & 0xffffu);
                     top_cnt[r] = static_cast<long long>(m >> 16);
                 }
             }
+            if (lane == 0)
+                for (; r <= ms; ++r) {
+                    top_seq[r] = -1;
+                    top_cnt[r] = 0;
+                }
         }
         __syncthreads();
     }
@@ -422,9 +455,9 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
             a.tasks[3 * ns + i - below] = make_int4(i, kPfWhole, 0, 0);
         }
     }
-    for (int j = 0; j < ns; ++j) {  // the scratch chunks: the second parts' chunks
+    for (int j = 0; j < ns; ++j) {  // the scratch chunks: the second parts' chunks (one tile)
         const int n = s_seq[j];
-        const long long bos = a.cu_seqlens[n], len = a.cu_seqlens[n + 1] - bos;
+        const long long bos = s_bos[n], len = s_len[n];
         const long long n1 = s_n1[j], cnt = (len + pf::C - 1) / pf::C;
         for (long long c = n1 + tid; c < cnt; c += kPfOffThreads) {
             const long long L = len - c * pf::C < pf::C ? len - c * pf::C : pf::C;
@@ -1399,11 +1432,11 @@ __global__ void __launch_bounds__(pf::NTS, 1)
 namespace pf {
 constexpr int FX_NW = 8;                       // output warps; the control warp is warp FX_NW
 constexpr int FX_NT = 32 * (FX_NW + 1);
-constexpr int FX_RING = 4;
+constexpr int FX_RING = 3;                     // F buffers
 constexpr uint32_t FX_A = 0;                   // S_a hi, lo: 128 rows v x 128 columns, K-major, 32 KB each
 constexpr uint32_t FX_B = 65536;               // ring of B buffers (hi, lo: 16 KB each)
-constexpr uint32_t FX_STG = FX_B + FX_RING * 32768;  // the product tile, fp32 [64 t][128 v]
-constexpr uint32_t FX_USED = FX_STG + 32768;
+constexpr uint32_t FX_O = FX_B + FX_RING * 32768;  // two O' buffers, fp32 [64 t][128 v]
+constexpr uint32_t FX_USED = FX_O + 2 * 32768;
 constexpr uint32_t FX_SMEM = FX_USED + 1024;   // + alignment slack
 constexpr uint32_t FX_COLS = 128;              // two 64-column product buffers
 }  // namespace pf
@@ -1414,8 +1447,10 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     // F_FULL + s: F in ring buffer s; MMA_DONE + b: products in TMEM buffer b done; D_FREE + b:
-    // TMEM buffer b read by the output warps
-    enum { F_FULL = 0, MMA_DONE = FX_RING, D_FREE = FX_RING + 2, FX_NBAR = FX_RING + 4 };
+    // TMEM buffer b read by the output warps; O_FULL + b: O' in buffer b; O_FREE + b: O' buffer b
+    // read by the output warps
+    enum { F_FULL = 0, MMA_DONE = FX_RING, D_FREE = FX_RING + 2, O_FULL = FX_RING + 4, O_FREE = FX_RING + 6,
+           FX_NBAR = FX_RING + 8 };
     __shared__ __align__(8) uint64_t bars[FX_NBAR];
     __shared__ volatile int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1555,7 +1590,7 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
         for (int i = 0; i < FX_NBAR; ++i) {
             if (job != blockIdx.x)
                 asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(&bars[i])) : "memory");
-            tc::mbar_init(&bars[i], i >= D_FREE ? FX_NW : 1);
+            tc::mbar_init(&bars[i], ((i >= D_FREE && i < O_FULL) || i >= O_FREE) ? FX_NW : 1);
         }
     __syncthreads();
 
@@ -1593,16 +1628,22 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
             }
         }
     } else if (control) {
+        // F of chunk c0 + i -> ring buffer i % FX_RING; O' of chunk c0 + i -> O' buffer i % 2
+        auto fetch_f = [&](int i) {
+            const int s = i % FX_RING;
+            const uint8_t* src = a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes + 32768;
+            tc::mbar_expect_tx(&bars[F_FULL + s], 32768);
+            tc::bulk_load(sb + FX_B + 32768u * s, src, 32768, &bars[F_FULL + s]);
+        };
+        auto fetch_o = [&](int i) {
+            const int s = i & 1;
+            const uint8_t* src = a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes;
+            tc::mbar_expect_tx(&bars[O_FULL + s], 32768);
+            tc::bulk_load(sb + FX_O + 32768u * s, src, 32768, &bars[O_FULL + s]);
+        };
         if (lane == 0) {
-            uint32_t inflight = 0;  // ring buffers with a copy in flight (for the drain after an abort)
-            auto fetch_f = [&](int i) {  // F of chunk c0 + i -> ring buffer i % FX_RING
-                const int s = i % FX_RING;
-                const uint8_t* src = a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes + 32768;
-                tc::mbar_expect_tx(&bars[F_FULL + s], 32768);
-                tc::bulk_load(sb + FX_B + 32768u * s, src, 32768, &bars[F_FULL + s]);
-                inflight |= 1u << s;
-            };
             for (int i = 0; i < n && i < FX_RING; ++i) fetch_f(i);
+            for (int i = 0; i < n && i < 2; ++i) fetch_o(i);
         }
         __syncwarp();
         tc::fence_before();
@@ -1614,18 +1655,25 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
                 if (i >= 2 && !ctl_wait(D_FREE + b, ((i - 2) >> 1) & 1)) break;
                 tc::fence_after();
                 products(b, s, false);
-                // refill the buffer of chunk i - 1 once its products are done
-                if (i >= 1 && i - 1 + FX_RING < n) {
-                    if (!ctl_wait(MMA_DONE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
-                    const int i4 = i - 1 + FX_RING, s4 = i4 % FX_RING;
-                    const uint8_t* src = a.scr_rows + ((c0 + i4) * a.Hv + h) * kPfScratchRowBytes + 32768;
-                    tc::mbar_expect_tx(&bars[F_FULL + s4], 32768);
-                    tc::bulk_load(sb + FX_B + 32768u * s4, src, 32768, &bars[F_FULL + s4]);
+                if (i >= 1) {
+                    // the F buffer of chunk i - 1 once its products are done, and the O' buffer of
+                    // chunk i - 1 once the output warps have read it
+                    if (i - 1 + FX_RING < n) {
+                        if (!ctl_wait(MMA_DONE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
+                        fetch_f(i - 1 + FX_RING);
+                    }
+                    if (i + 1 < n) {
+                        if (!ctl_wait(O_FREE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
+                        fetch_o(i + 1);
+                    }
                 }
             }
             if (abort_flag) {  // one more bounded wait on every copy and product that may be in flight
                 for (int s = 0; s < FX_RING; ++s) tc::mbar_wait(&bars[F_FULL + s], 0, 1u << 20);
-                for (int b = 0; b < 2; ++b) tc::mbar_wait(&bars[MMA_DONE + b], 0, 1u << 20);
+                for (int b = 0; b < 2; ++b) {
+                    tc::mbar_wait(&bars[MMA_DONE + b], 0, 1u << 20);
+                    tc::mbar_wait(&bars[O_FULL + b], 0, 1u << 20);
+                }
             }
         }
         __syncwarp();
@@ -1633,49 +1681,38 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
         tc::fence_proxy_async();  // A (generic-proxy writes) before the tensor core reads it
         tc::fence_before();
         __syncthreads();
-        // unit u = tid + 256 k (k < 8) of a chunk: token u >> 5, columns 4 (u & 31) .. + 3
-        auto load_o = [&](int i, float4 (&o4)[8]) {
-            const float4* op = reinterpret_cast<const float4*>(a.scr_rows + ((c0 + i) * a.Hv + h) * kPfScratchRowBytes);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o4[k] = op[tid + 256 * k];
-        };
-        float* stg = reinterpret_cast<float*>(sm + FX_STG);
-        float4 ocur[8], onext[8];
-        longlong2 ecur = a.scr_tab[c0], enext = ecur;  // (first token, split << 32 | length)
-        load_o(0, ocur);
-        if (n > 1) {
-            load_o(1, onext);
-            enext = a.scr_tab[c0 + 1];
-        }
+        // every output warp runs every iteration (the named barrier needs all eight); after a
+        // failed wait a warp only keeps the barrier count
+        bool good = true;
         for (int i = 0; i < n; ++i) {
             const int b = i & 1;
-            if (!warp_wait(MMA_DONE + b, (i >> 1) & 1)) break;
+            good = good && warp_wait(MMA_DONE + b, (i >> 1) & 1);
             float d[32];
-            ld_d(b, d, true);
-            // the product tile to shared memory as [t][v] (lanes: consecutive v, no bank conflict)
+            if (good) ld_d(b, d, true);
+            good = good && warp_wait(O_FULL + b, (i >> 1) & 1);
+            // the products added into O' (buffer b, [t][v]: lanes are consecutive v, no bank conflict)
+            float* ob = reinterpret_cast<float*>(sm + FX_O + 32768u * b);
+            if (good) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) stg[(32 * half + k) * D + row] = d[k];
+                for (int k = 0; k < 32; ++k) ob[(32 * half + k) * D + row] += d[k];
+            }
             asm volatile("bar.sync 1, %0;" ::"n"(32 * FX_NW) : "memory");
-            const longlong2 e = ecur;
+            if (!good) continue;
+            // unit u = tid + 256 k (k < 8): token u >> 5, columns 4 (u & 31) .. + 3, stored coalesced
+            const longlong2 e = a.scr_tab[c0 + i];
             const int L = static_cast<int>(e.y & 0xffffffffLL);
             uint16_t* o = a.out + static_cast<size_t>(e.x) * a.Hv * D + static_cast<size_t>(h) * D;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int u = tid + 256 * k, t = u >> 5, c4 = u & 31;
-                const float4 p = *reinterpret_cast<const float4*>(stg + t * D + 4 * c4);
-                const float x[4] = {p.x + ocur[k].x, p.y + ocur[k].y, p.z + ocur[k].z, p.w + ocur[k].w};
+                const float4 p = *reinterpret_cast<const float4*>(ob + t * D + 4 * c4);
                 if (t < L)
                     *reinterpret_cast<uint2*>(o + static_cast<size_t>(t) * a.Hv * D + 4 * c4) =
-                        make_uint2(pack_in_x2<F16>(x[0], x[1]), pack_in_x2<F16>(x[2], x[3]));
+                        make_uint2(pack_in_x2<F16>(p.x, p.y), pack_in_x2<F16>(p.z, p.w));
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * FX_NW) : "memory");  // the tile is read
-#pragma unroll
-            for (int k = 0; k < 8; ++k) ocur[k] = onext[k];
-            ecur = enext;
-            if (i + 2 < n) {
-                load_o(i + 2, onext);
-                enext = a.scr_tab[c0 + i + 2];
-            }
+            tc::fence_proxy_async();  // the buffer is refilled by a bulk copy next
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[O_FREE + b]);
         }
     }
     tc::fence_before();
