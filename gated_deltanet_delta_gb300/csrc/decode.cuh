@@ -128,10 +128,19 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeArgs a) {
     }
 }
 
-// T consecutive decode steps ([gated_delta.rs] mt_gated_delta_chunk).  The same row split as the
-// single step; the state rows stay in registers for all T tokens.  Tokens are staged in blocks of
-// TB: q and k of the key head (fp32), v of this CTA's rows, g and beta go to shared memory, then the
-// block's tokens run with warp shuffles only, so a block costs two barriers.
+// T consecutive decode steps ([gated_delta.rs] mt_gated_delta_chunk).  The single step's row split;
+// the state rows stay in registers for all T tokens, held as c * R with one scalar c per head: the
+// gate multiplies c instead of every element, the rank-1 update is R += k (delta / c), and c is
+// folded back into R when |c| leaves [2^-40, 2^40] (uniform over the CTA: every thread sees the
+// same gates).  Per token one pass over a thread's rows forms R k and R q (and the lane's share of
+// k q), one reduction round inside the row group sums all of them, and
+//     kv = c (R k),  delta = (v - kv) beta,  y = scale (c (R q) + delta (k q))
+// -- the readout of the updated state, S_new q = g S q + delta (k q), regrouped -- before a second
+// pass applies the update.  Arithmetic on column pairs with packed f32x2 FMAs.  Tokens are staged
+// in blocks of TB: q and k of the key head (fp32), v of this CTA's rows, g and beta go to shared
+// memory, then the block's tokens run with warp shuffles only, so a block costs two barriers.
+constexpr float kMultiLo = 9.094947e-13f;  // 2^-40
+constexpr float kMultiHi = 1.0995116e12f;  // 2^40
 template <int DK, int TPR, int RPT, int NT, int TB>
 __global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int NV = DK / (4 * TPR);
@@ -165,14 +174,15 @@ __global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiA
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
+    float c = 1.f;  // the state is c * s
     for (int t0 = 0; t0 < a.T; t0 += TB) {
         const int nb = a.T - t0 < TB ? a.T - t0 : TB;
         __syncthreads();  // the previous block's shared inputs are no longer read
         for (int i = threadIdx.x; i < nb * (DK / 4); i += NT) {
-            const int tt = i / (DK / 4), c = i - tt * (DK / 4);
-            const size_t off = ((size_t(b) * a.T + t0 + tt) * a.Hk + hk) * DK + 4 * c;
-            ks[tt][c] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.k + off));
-            qs[tt][c] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.q + off));
+            const int tt = i / (DK / 4), cc = i - tt * (DK / 4);
+            const size_t off = ((size_t(b) * a.T + t0 + tt) * a.Hk + hk) * DK + 4 * cc;
+            ks[tt][cc] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.k + off));
+            qs[tt][cc] = bf16x4_to_f32x4(*reinterpret_cast<const uint2*>(a.q + off));
         }
         for (int i = threadIdx.x; i < nb * ROWS; i += NT) {
             const int tt = i / ROWS, r = i - tt * ROWS;
@@ -186,40 +196,74 @@ __global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiA
         }
         __syncthreads();
         for (int tt = 0; tt < nb; ++tt) {
-            const float gate = gs[tt], beta = bs[tt];
+            const float beta = bs[tt];
+            c *= gs[tt];
+            if (!(fabsf(c) >= kMultiLo && fabsf(c) <= kMultiHi)) {  // fold c into the rows
+                const float2 c2 = make_float2(c, c);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                    for (int m = 0; m < NV; ++m) {
+                        float4& x = s[r][m];
+                        const float2 x01 = __fmul2_rn(make_float2(x.x, x.y), c2);
+                        const float2 x23 = __fmul2_rn(make_float2(x.z, x.w), c2);
+                        x = make_float4(x01.x, x01.y, x23.x, x23.y);
+                    }
+                c = 1.f;
+            }
+            // pass 1: R k, R q per row and this lane's share of k q
+            float2 kq2 = make_float2(0.f, 0.f);
+            float2 rk2[RPT], rq2[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) rk2[r] = rq2[r] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int m = 0; m < NV; ++m) {
+                const float4 kk = ks[tt][lr + TPR * m];
+                const float4 qq = qs[tt][lr + TPR * m];
+                const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+                const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
+                kq2 = __ffma2_rn(k01, q01, kq2);
+                kq2 = __ffma2_rn(k23, q23, kq2);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const float2 x01 = make_float2(s[r][m].x, s[r][m].y), x23 = make_float2(s[r][m].z, s[r][m].w);
+                    rk2[r] = __ffma2_rn(x01, k01, rk2[r]);
+                    rk2[r] = __ffma2_rn(x23, k23, rk2[r]);
+                    rq2[r] = __ffma2_rn(x01, q01, rq2[r]);
+                    rq2[r] = __ffma2_rn(x23, q23, rq2[r]);
+                }
+            }
+            float kq = kq2.x + kq2.y, rk[RPT], rq[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                float kv = 0.f;
+                rk[r] = rk2[r].x + rk2[r].y;
+                rq[r] = rq2[r].x + rq2[r].y;
+            }
+#pragma unroll
+            for (int o = TPR / 2; o > 0; o >>= 1) {
+                kq += __shfl_xor_sync(kFullMask, kq, o);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    rk[r] += __shfl_xor_sync(kFullMask, rk[r], o);
+                    rq[r] += __shfl_xor_sync(kFullMask, rq[r], o);
+                }
+            }
+            // pass 2: delta, the readout, the rank-1 update
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float delta = (vs[tt][r * RPP + rw] - c * rk[r]) * beta;
+                const float yv = a.scale * fmaf(delta, kq, c * rq[r]);
+                const float dc = delta / c;
+                const float2 d2 = make_float2(dc, dc);
 #pragma unroll
                 for (int m = 0; m < NV; ++m) {
                     const float4 kk = ks[tt][lr + TPR * m];
                     float4& x = s[r][m];
-                    x.x *= gate; x.y *= gate; x.z *= gate; x.w *= gate;
-                    kv = fmaf(x.x, kk.x, kv);
-                    kv = fmaf(x.y, kk.y, kv);
-                    kv = fmaf(x.z, kk.z, kv);
-                    kv = fmaf(x.w, kk.w, kv);
+                    const float2 x01 = __ffma2_rn(make_float2(kk.x, kk.y), d2, make_float2(x.x, x.y));
+                    const float2 x23 = __ffma2_rn(make_float2(kk.z, kk.w), d2, make_float2(x.z, x.w));
+                    x = make_float4(x01.x, x01.y, x23.x, x23.y);
                 }
-                kv = group_sum<TPR>(kv);
-                const float delta = (vs[tt][r * RPP + rw] - kv) * beta;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < NV; ++m) {
-                    const float4 kk = ks[tt][lr + TPR * m];
-                    const float4 qq = qs[tt][lr + TPR * m];
-                    float4& x = s[r][m];
-                    x.x = fmaf(delta, kk.x, x.x);
-                    x.y = fmaf(delta, kk.y, x.y);
-                    x.z = fmaf(delta, kk.z, x.z);
-                    x.w = fmaf(delta, kk.w, x.w);
-                    acc = fmaf(x.x, qq.x, acc);
-                    acc = fmaf(x.y, qq.y, acc);
-                    acc = fmaf(x.z, qq.z, acc);
-                    acc = fmaf(x.w, qq.w, acc);
-                }
-                acc = group_sum<TPR>(acc);
                 if (row[r] < a.Dv && lr == 0) {
-                    const float yv = a.scale * acc;
                     const size_t yi = ((size_t(b) * a.T + t0 + tt) * a.Hv + hv) * a.Dv + row[r];
                     if (a.y_f32)
                         static_cast<float*>(a.y)[yi] = yv;
@@ -229,11 +273,17 @@ __global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiA
             }
         }
     }
+    const float2 c2 = make_float2(c, c);
 #pragma unroll
     for (int r = 0; r < RPT; ++r)
         if (row[r] < a.Dv)
 #pragma unroll
-            for (int m = 0; m < NV; ++m) st_stream(dst + size_t(row[r]) * (DK / 4) + lr + TPR * m, s[r][m]);
+            for (int m = 0; m < NV; ++m) {
+                const float4 x = s[r][m];
+                const float2 x01 = __fmul2_rn(make_float2(x.x, x.y), c2);
+                const float2 x23 = __fmul2_rn(make_float2(x.z, x.w), c2);
+                st_stream(dst + size_t(row[r]) * (DK / 4) + lr + TPR * m, make_float4(x01.x, x01.y, x23.x, x23.y));
+            }
 }
 
 // Rows covered by one CTA of a configuration.
