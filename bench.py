@@ -74,6 +74,14 @@ def prefill_bytes(seqlens, Hk, Hv, K, V):
             + 2 * n * Hv * V * K * 4 + n * 8 + (n + 1) * 8 + 2 * Hv * 4)
 
 
+def comba_prefill_bytes(seqlens, H, K, V):
+    """q, k, p, v, beta (bf16) and g (f32) read once, out (bf16) written once, the sequences'
+    pool slots gathered and scattered."""
+    T, n = sum(seqlens), len(seqlens)
+    return (3 * T * H * K * 2 + T * H * V * 2 + T * H * (2 + 4) + T * H * V * 2
+            + 2 * n * H * K * V * 4 + n * 8 + (n + 1) * 8)
+
+
 def prefill_flops(seqlens, Hv, K, V, C):
     chunks = sum((s + C - 1) // C for s in seqlens)
     T = sum(seqlens)
@@ -527,6 +535,34 @@ class OracleDecodeSample:
         return state_bytes / secs / 1e9, self.threads, desc, secs
 
 
+def bench_comba_prefill(torch, gdn, dist, steps, warmup, seed):
+    """The Comba chunked prefill on the GDN prefill's token layout: lengths 4096+2048+1024+8192,
+    H=32 heads (each with its own q, k, p), K=V=128, chunk 64, a 16-slot pool."""
+    c = gi.GDN_PREFILL
+    H, K, V, C = c["Hv"], c["K"], c["V"], c["chunk"]
+    x = gi.comba_prefill_inputs(gi.rng(seed + 5), c["seqlens"], H, K, V, c["pool"])
+    dev = torch.device("cuda")
+    bf, f32 = torch.bfloat16, torch.float32
+    d = {n: torch.from_numpy(x[n]).to(dt).to(dev) for n, dt in
+         (("q", bf), ("k", bf), ("v", bf), ("p", bf), ("beta", bf), ("g_log", f32), ("state_pool", f32),
+          ("cache_indices", torch.int64), ("cu_seqlens", torch.int64))}
+    T = x["T"]
+    out = torch.empty((T, H, V), dtype=bf, device=dev)
+    ws = torch.empty(max(1, gdn.gdn_prefill_workspace_size(len(c["seqlens"]), T, H, H, K, V, C)),
+                     dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        gdn.comba_prefill_chunked(d["q"], d["k"], d["v"], d["p"], d["beta"], d["g_log"], d["state_pool"],
+                                  d["cache_indices"], d["cu_seqlens"], C, out=out, workspace=ws, dev_status=status)
+
+    for i in range(warmup):
+        step(i)
+    secs = _timed(torch, dist, steps, step)
+    return dict(secs=secs, T=T, alg_bytes=comba_prefill_bytes(c["seqlens"], H, K, V),
+                flops=prefill_flops(c["seqlens"], H, K, V, C))
+
+
 # ------------------------------------------------------------------------------------------------
 def main_single_op(args, torch, gdn, dist, seed):
     """One operation alone, args.steps timed calls after args.warmup: a small, repeatable command to
@@ -537,6 +573,7 @@ def main_single_op(args, torch, gdn, dist, seed):
         "comba_forward": lambda: bench_comba_forward(torch, gdn, dist, args.steps, args.warmup, seed),
         "prefill": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed),
         "prefill_f16": lambda: bench_prefill(torch, gdn, dist, args.steps, args.warmup, seed, "f16"),
+        "comba_prefill": lambda: bench_comba_prefill(torch, gdn, dist, args.steps, args.warmup, seed),
         "window_verify": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, False),
         "window_commit": lambda: bench_window(torch, gdn, dist, args.steps, args.warmup, seed, True),
         "decode_multi": lambda: bench_decode_multi(torch, gdn, dist, args.steps, args.warmup, seed),
@@ -558,7 +595,8 @@ def main():
     ap.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline (rank 0, N=1)")
-    ap.add_argument("--op", choices=("decode", "comba", "comba_forward", "prefill", "prefill_f16", "window_verify", "window_commit",
+    ap.add_argument("--op", choices=("decode", "comba", "comba_forward", "prefill", "prefill_f16", "comba_prefill",
+                                     "window_verify", "window_commit",
                                      "decode_multi", "decode_pooled"),
                     help="time only this operation on its workload and print its time per call "
                          "(for profiling; not the benchmark line)")
@@ -595,6 +633,9 @@ def main():
                          ("prefill_f16", lambda: bench_prefill(torch, gdn, dist,
                                                                max(3, args.steps // 10),
                                                                args.warmup, seed, "f16")),
+                         ("comba_prefill", lambda: bench_comba_prefill(torch, gdn, dist,
+                                                                       max(3, args.steps // 10),
+                                                                       args.warmup, seed)),
                          ("window_verify", lambda: bench_window(torch, gdn, dist, args.steps,
                                                                 args.warmup, seed, False)),
                          ("window_commit", lambda: bench_window(torch, gdn, dist, args.steps,
@@ -638,7 +679,9 @@ def main():
     elif "comba" in extra:
         ops["comba_decode"] = extra["comba"]
     for key, op_name, dt_note in (("prefill", "prefill_chunked", ""),
-                                  ("prefill_f16", "prefill_chunked_f16", ", fp16 token arrays")):
+                                  ("prefill_f16", "prefill_chunked_f16", ", fp16 token arrays"),
+                                  ("comba_prefill", "comba_prefill_chunked",
+                                   ", Comba recurrence, H=32 (own q, k, p per head)")):
         pf = extra.get(key, {})
         if "secs" not in pf:
             if key in extra:

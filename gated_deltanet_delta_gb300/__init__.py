@@ -25,7 +25,8 @@ STATUS_BAD_SEQLENS = 2
 # Every symbol that include/gdn.h declares.
 ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "comba_forward",
                "gdn_prefill_workspace_size",
-               "gdn_prefill_chunked", "gdn_prefill_chunked_f16", "gdn_prefill_chunked_noalloc", "gdn_window_fused",
+               "gdn_prefill_chunked", "gdn_prefill_chunked_f16", "gdn_prefill_chunked_noalloc",
+               "comba_prefill_chunked", "gdn_window_fused",
                "gdn_status_string", "gdn_last_error")
 
 
@@ -70,6 +71,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_chunked.restype = I
         lib.gdn_prefill_chunked_f16.argtypes = lib.gdn_prefill_chunked.argtypes
         lib.gdn_prefill_chunked_f16.restype = I
+        lib.comba_prefill_chunked.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I, I, F, P, P, SZ,
+                                              P, P]
+        lib.comba_prefill_chunked.restype = I
         lib.gdn_prefill_chunked_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I64, I, I, I,
                                                     I, I, F, P, P, P]
         lib.gdn_prefill_chunked_noalloc.restype = I
@@ -319,6 +323,46 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices
                                  _ptr(cache_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
                                  int(chunk_size), scale, _ptr(out), _ptr(workspace), wsz,
                                  _ptr(dev_status), _stream(q.device)), name)
+    return out
+
+
+def comba_prefill_chunked(q, k, v, p, beta, g, state_pool, cache_indices, cu_seqlens, chunk_size: int = 64,
+                          scale=None, out=None, workspace=None, dev_status=None):
+    """Varlen chunkwise prefill of the Comba recurrence.  q, k, p [T,H,K] and v [T,H,V] bf16; beta
+    bf16 [T,H]; g f32 [T,H] (log decay); state_pool f32 [pool,H,K,V] (updated in place);
+    cache_indices int64 [N]; cu_seqlens int64 [N+1].  Returns out bf16 [T,H,V]; scale defaults to
+    K^-0.5."""
+    torch = _torch()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cache_indices.shape[0]
+    bf = torch.bfloat16
+    _want(q, "q", bf)
+    _want(k, "k", bf, (T, H, K))
+    _want(p, "p", bf, (T, H, K))
+    _want(v, "v", bf, (T, H, V))
+    _want(beta, "beta", bf, (T, H))
+    _want(g, "g", torch.float32, (T, H))
+    _want(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, K, V):
+        raise ValueError(f"state_pool must be [pool,{H},{K},{V}], got {tuple(state_pool.shape)}")
+    _want(cache_indices, "cache_indices", torch.int64, (N,))
+    _want(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,))
+    if out is None:
+        out = torch.empty((T, H, V), dtype=bf, device=q.device)
+    _want(out, "out", bf, (T, H, V))
+    ws_bytes = gdn_prefill_workspace_size(N, T, H, H, K, V, chunk_size)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    _want(dev_status, "dev_status", torch.int32, (1,))
+    scale = K ** -0.5 if scale is None else float(scale)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().comba_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(p), _ptr(beta), _ptr(g), _ptr(state_pool),
+                                        state_pool.shape[0], _ptr(cache_indices), _ptr(cu_seqlens), N, T, H, K, V,
+                                        int(chunk_size), scale, _ptr(out), _ptr(workspace), wsz, _ptr(dev_status),
+                                        _stream(q.device)), "comba_prefill_chunked")
     return out
 
 

@@ -319,14 +319,21 @@ extern "C" size_t gdn_prefill_workspace_size(int num_seqs, int64_t T, int Hk, in
     return gdn::prefill_workspace_bytes(T, num_seqs, Hv);
 }
 
-// gdn_prefill_chunked and gdn_prefill_chunked_f16: the same checks and launch, the token arrays
-// (q, k, v, a, b, out) in bf16 or in IEEE binary16.
+// gdn_prefill_chunked, gdn_prefill_chunked_f16 and comba_prefill_chunked: the same checks and
+// launch, the token arrays (q, k, v, a, b, out) in bf16 or in IEEE binary16; for Comba (a, b, A_log,
+// dt_bias unused) the read keys, log decays and betas of CombaIn instead.
+struct CombaIn {
+    const void* p;
+    const void* beta;
+    const float* g;
+};
 static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const void* k, const void* v,
                                 const void* a, const void* b, const float* A_log, const float* dt_bias,
                                 float* state_pool, int pool_size, const int64_t* cache_indices,
                                 const int64_t* cu_seqlens, int num_seqs, int64_t T, int Hk, int Hv, int K,
                                 int V, int chunk_size, float scale, void* out, void* workspace,
-                                size_t workspace_bytes, int32_t* dev_status, gdn_stream_t stream) {
+                                size_t workspace_bytes, int32_t* dev_status, gdn_stream_t stream,
+                                const CombaIn* cb = nullptr) {
     REQUIRE(num_seqs >= 0 && T >= 0 && pool_size >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1,
             GDN_ERR_INVALID_ARG, "%s: sizes must be num_seqs, T, pool_size >= 0 and Hk, Hv, K, V >= 1", fn);
     REQUIRE(Hv % Hk == 0, GDN_ERR_INVALID_ARG, "%s: Hv (%d) must be a multiple of Hk (%d)", fn, Hv, Hk);
@@ -334,14 +341,21 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     REQUIRE(prefill_chunk_size_ok(chunk_size), GDN_ERR_UNSUPPORTED, "%s: chunk_size must be 64 or 128 (got %d)",
             fn, chunk_size);
     if (num_seqs == 0) return GDN_OK;
-    REQUIRE(cache_indices && cu_seqlens && dev_status && A_log && dt_bias && state_pool,
+    REQUIRE(cache_indices && cu_seqlens && dev_status && state_pool && (cb || (A_log && dt_bias)),
             GDN_ERR_INVALID_ARG, "%s: null pointer", fn);
-    REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG, "%s: null token pointer", fn);
+    if (cb) {
+        REQUIRE(T == 0 || (q && k && v && cb->p && cb->beta && cb->g && out), GDN_ERR_INVALID_ARG,
+                "%s: null token pointer", fn);
+        REQUIRE(aligned(cb->p, 16) && aligned(cb->beta, 2) && aligned(cb->g, 4), GDN_ERR_INVALID_ARG,
+                "%s: misaligned argument (p 16 bytes, beta 2, g 4)", fn);
+    } else {
+        REQUIRE(T == 0 || (q && k && v && a && b && out), GDN_ERR_INVALID_ARG, "%s: null token pointer", fn);
+        REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(A_log, 4) && aligned(dt_bias, 4), GDN_ERR_INVALID_ARG,
+                "%s: misaligned argument", fn);
+    }
     REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) && aligned(state_pool, 16),
             GDN_ERR_INVALID_ARG, "%s: q, k, v, out and state_pool must be 16-byte aligned", fn);
-    REQUIRE(aligned(a, 2) && aligned(b, 2) && aligned(A_log, 4) &&
-                aligned(dt_bias, 4) && aligned(dev_status, 4) && aligned(cache_indices, 8) &&
-                aligned(cu_seqlens, 8),
+    REQUIRE(aligned(dev_status, 4) && aligned(cache_indices, 8) && aligned(cu_seqlens, 8),
             GDN_ERR_INVALID_ARG, "%s: misaligned argument", fn);
     const size_t obytes = size_t(T) * Hv * V * 2, pbytes = size_t(pool_size) * Hv * V * K * 4;
     REQUIRE(!any_overlap(out, obytes, state_pool, pbytes), GDN_ERR_INVALID_ARG, "%s: out overlaps state_pool",
@@ -365,6 +379,9 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     p.b = static_cast<const uint16_t*>(b);
     p.A_log = A_log;
     p.dt_bias = dt_bias;
+    p.p = cb ? static_cast<const uint16_t*>(cb->p) : nullptr;
+    p.g_log = cb ? cb->g : nullptr;
+    p.beta_in = cb ? static_cast<const uint16_t*>(cb->beta) : nullptr;
     p.state_pool = state_pool;
     p.cache_indices = cache_indices;
     p.cu_seqlens = cu_seqlens;
@@ -377,7 +394,8 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     p.Hv = Hv;
     p.scale = scale;
     p.eps = 1e-6f;
-    const cudaError_t e = gdn::launch_prefill(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), f16);
+    const cudaError_t e =
+        gdn::launch_prefill(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), f16, cb != nullptr);
     if (e != cudaSuccess)
         return fail(GDN_ERR_CUDA, "%s: launch failed (TMA descriptors or kernel): %s", fn, cudaGetErrorString(e));
     g_last_error[0] = '\0';
@@ -408,6 +426,18 @@ extern "C" gdn_status gdn_prefill_chunked_f16(const void* q, const void* k, cons
     return prefill_entry("gdn_prefill_chunked_f16", true, q, k, v, a, b, A_log, dt_bias, state_pool, pool_size,
                          cache_indices, cu_seqlens, num_seqs, T, Hk, Hv, K, V, chunk_size, scale, out,
                          workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" gdn_status comba_prefill_chunked(const void* q, const void* k, const void* v, const void* p,
+                                            const void* beta, const float* g, float* state_pool, int pool_size,
+                                            const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                            int num_seqs, int64_t T, int H, int K, int V, int chunk_size,
+                                            float scale, void* out, void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, gdn_stream_t stream) {
+    const CombaIn cb{p, beta, g};
+    return prefill_entry("comba_prefill_chunked", false, q, k, v, nullptr, nullptr, nullptr, nullptr, state_pool,
+                         pool_size, cache_indices, cu_seqlens, num_seqs, T, H, H, K, V, chunk_size, scale, out,
+                         workspace, workspace_bytes, dev_status, stream, &cb);
 }
 
 

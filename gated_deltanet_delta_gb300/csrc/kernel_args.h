@@ -111,7 +111,10 @@ struct PrefillArgs {
     const uint16_t* b;
     const float* A_log;
     const float* dt_bias;
-    float* state_pool;
+    const uint16_t* p;        // Comba: read keys [T, H, K] (q, k, v as above; a, b, A_log, dt_bias unused)
+    const float* g_log;       // Comba: log decay per token and head [T, H] (gate = exp(g_log))
+    const uint16_t* beta_in;  // Comba: beta per token and head [T, H] (the value itself)
+    float* state_pool;        // GDN: [pool, Hv, V, K]; Comba: [pool, H, K, V]
     const int64_t* cache_indices;
     const int64_t* cu_seqlens;
     uint16_t* out;
@@ -149,6 +152,7 @@ constexpr long long kPfRecordVec = 65536;
 // 64 features x 1 head x 64 tokens with the 128-byte swizzle.
 struct PrefillMaps {
     CUtensorMap q, k, v;
+    CUtensorMap p;  // Comba: the read keys [T, H, 128]
 };
 
 constexpr int kWinD = 128;       // head dim

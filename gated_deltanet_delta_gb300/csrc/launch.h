@@ -36,7 +36,8 @@ size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv);
 // Raises the kernels' shared-memory limits once per device, then launches; returns the launch
 // error.  Sequences are split only when workspace_bytes holds the scratch.
 // f16: q, k, v, a, b and out are IEEE binary16 (else bf16).
+// comba: the Comba variant (read keys p, given log decays and betas, [K][V] state pool; bf16).
 cudaError_t launch_prefill(const PrefillArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                           bool f16);
+                           bool f16, bool comba = false);
 
 }  // namespace gdn

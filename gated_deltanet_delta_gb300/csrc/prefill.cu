@@ -72,29 +72,49 @@ size_t prefill_workspace_bytes(long long T, int num_seqs, int Hv) { return prefi
 namespace {
 std::atomic<int> g_nsm[kMaxDevices];  // per device: multiprocessor count (0: not read yet)
 
-template <bool F16>
+template <bool F16, bool CB>
 cudaError_t set_smem_limits() {
-    cudaError_t e = cudaFuncSetAttribute(gdn_prefill_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gdn_prefill_kernel<F16, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gdn_prefill_fixup_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gdn_prefill_fixup_kernel<F16, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(pf::FX_SMEM));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gdn_prefill_prep_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(pf::P_SMEM));
+    return cudaFuncSetAttribute(gdn_prefill_prep_kernel<F16, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(CB ? pf::P_SMEM_CB : pf::P_SMEM));
+}
+
+// the three kernels of one variant
+template <bool F16, bool CB>
+void launch_variant(const PrefillArgs& a, const PrefillMaps& maps, bool split, cudaStream_t stream) {
+    if (a.T > 0) {  // one CTA per (chunk, key head, pair of value heads) of the capacity; the ones past
+                    // the last chunk exit
+        const int ngrp = (a.Hv / a.Hk + pf::PH - 1) / pf::PH;
+        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hk) * static_cast<unsigned>(ngrp);
+        gdn_prefill_prep_kernel<F16, CB><<<pgrid, pf::PNT, CB ? pf::P_SMEM_CB : pf::P_SMEM, stream>>>(a, maps);
+    }
+    // one CTA per (task, value head); tasks past the schedule's count exit
+    const unsigned grid = static_cast<unsigned>(a.num_seqs + 2 * a.max_splits) * static_cast<unsigned>(a.Hv);
+    gdn_prefill_kernel<F16, CB><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
+    if (split && a.T > 0) {  // one CTA per SM, looping over the jobs (none when nothing was split)
+        const unsigned fgrid = static_cast<unsigned>(a.nsm > 0 ? a.nsm : 1);
+        gdn_prefill_fixup_kernel<F16, CB><<<fgrid, pf::FX_NT, pf::FX_SMEM, stream>>>(a);
+    }
 }
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                           bool f16) {
+                           bool f16, bool comba) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!g_smem_set[dev].load(std::memory_order_acquire)) {
-        e = set_smem_limits<false>();
+        e = set_smem_limits<false, false>();
         if (e != cudaSuccess) return e;
-        e = set_smem_limits<true>();
+        e = set_smem_limits<true, false>();
+        if (e != cudaSuccess) return e;
+        e = set_smem_limits<false, true>();
         if (e != cudaSuccess) return e;
         int nsm = 0;
         e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -123,26 +143,13 @@ cudaError_t launch_prefill(const PrefillArgs& args, void* workspace, size_t work
     std::memset(&maps, 0, sizeof(maps));
     if (a.T > 0) {  // with T = 0 every sequence is empty and no kernel reads the maps
         if (!encode_rows(&maps.q, a.q, a.T, a.Hk, f16) || !encode_rows(&maps.k, a.k, a.T, a.Hk, f16) ||
-            !encode_rows(&maps.v, a.v, a.T, a.Hv, f16))
+            !encode_rows(&maps.v, a.v, a.T, a.Hv, f16) || (comba && !encode_rows(&maps.p, a.p, a.T, a.Hk, false)))
             return cudaErrorInvalidValue;
     }
     gdn_prefill_offsets_kernel<<<1, kPfOffThreads, 0, stream>>>(a);
-    if (a.T > 0) {  // one CTA per (chunk, key head, pair of value heads) of the capacity; the ones past
-                    // the last chunk exit
-        const int ngrp = (a.Hv / a.Hk + pf::PH - 1) / pf::PH;
-        const unsigned pgrid = static_cast<unsigned>(a.cap) * static_cast<unsigned>(a.Hk) * static_cast<unsigned>(ngrp);
-        if (f16) gdn_prefill_prep_kernel<true><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
-        else gdn_prefill_prep_kernel<false><<<pgrid, pf::PNT, pf::P_SMEM, stream>>>(a, maps);
-    }
-    // one CTA per (task, value head); tasks past the schedule's count exit
-    const unsigned grid = static_cast<unsigned>(a.num_seqs + 2 * a.max_splits) * static_cast<unsigned>(a.Hv);
-    if (f16) gdn_prefill_kernel<true><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
-    else gdn_prefill_kernel<false><<<grid, pf::NTS, pf::SMEM_BYTES, stream>>>(a, maps);
-    if (split && a.T > 0) {  // one CTA per SM, looping over the jobs (none when nothing was split)
-        const unsigned fgrid = static_cast<unsigned>(a.nsm > 0 ? a.nsm : 1);
-        if (f16) gdn_prefill_fixup_kernel<true><<<fgrid, pf::FX_NT, pf::FX_SMEM, stream>>>(a);
-        else gdn_prefill_fixup_kernel<false><<<fgrid, pf::FX_NT, pf::FX_SMEM, stream>>>(a);
-    }
+    if (comba) launch_variant<false, true>(a, maps, split, stream);
+    else if (f16) launch_variant<true, false>(a, maps, split, stream);
+    else launch_variant<false, false>(a, maps, split, stream);
     return cudaGetLastError();
 }
 

@@ -87,6 +87,9 @@ constexpr uint32_t P_X = P_L + 64 * LST * 4;  // fp32 [32][ZST] scratch of the b
                                                // it, M~ hi / lo staged in the record's layout (16 KB)
 constexpr uint32_t P_USED = P_X + 16384;
 constexpr uint32_t P_SMEM = P_USED + 1024;
+// Comba: the write keys' rows (the B operand of G = [P; Q] K^T) in a tile of their own
+constexpr uint32_t P_K2 = (P_USED + 1023) / 1024 * 1024;
+constexpr uint32_t P_SMEM_CB = P_K2 + 16384 + 1024;
 constexpr uint32_t P_TM_G = 0, P_TM_COLS = 64;
 static_assert(P_X + 32 * ZST * 4 <= P_USED && P_X % 16 == 0, "Lm, T, the M~ staging and the scratch fit");
 
@@ -475,7 +478,10 @@ __global__ void __launch_bounds__(kPfOffThreads) gdn_prefill_offsets_kernel(cons
 // CTAs of 256 threads, five per SM: the latency-bound phases of one CTA (the inverse runs 64, 128
 // and 256 threads wide) overlap with those of four others.  Every part of a record is written to
 // the workspace directly.
-template <bool F16>
+// CB (Comba, read key p != write key k; inputs pre-normalised, gates given): the rows of G are
+// [P; Q] K^T (Lm from P K^T, M~ from Q K^T), the norms are 1, the log decay and beta are read as
+// they are; everything after G is the same.
+template <bool F16, bool CB>
 __global__ void __launch_bounds__(pf::PNT, 5)
     gdn_prefill_prep_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
@@ -515,24 +521,36 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         tc::mbar_init(&mbar, 1);
         tc::mbar_init(&bar_kq, 1);
         const int z = static_cast<int>(tok0);
-        tc::mbar_expect_tx(&bar_kq, 4 * 8192);
-        tc::tma_load_3d(sb + P_KQ, &maps.k, 0, hk, z, &bar_kq);
-        tc::tma_load_3d(sb + P_KQ + 16384, &maps.k, 64, hk, z, &bar_kq);
+        tc::mbar_expect_tx(&bar_kq, (CB ? 6 : 4) * 8192);
+        const CUtensorMap* top = CB ? &maps.p : &maps.k;  // the rows above Q in the tile
+        tc::tma_load_3d(sb + P_KQ, top, 0, hk, z, &bar_kq);
+        tc::tma_load_3d(sb + P_KQ + 16384, top, 64, hk, z, &bar_kq);
         tc::tma_load_3d(sb + P_KQ + 8192, &maps.q, 0, hk, z, &bar_kq);
         tc::tma_load_3d(sb + P_KQ + 16384 + 8192, &maps.q, 64, hk, z, &bar_kq);
+        if constexpr (CB) {
+            tc::tma_load_3d(sb + P_K2, &maps.k, 0, hk, z, &bar_kq);
+            tc::tma_load_3d(sb + P_K2 + 8192, &maps.k, 64, hk, z, &bar_kq);
+        }
     }
     // gate inputs: thread jg * 64 + t takes token t of value head h0 + jg
     const int jg = tid >> 6, tg = tid & (C - 1);
     uint16_t a_raw = 0, b_raw = 0;
-    float a_mul = 0.f, dtb = 0.f;
+    float a_mul = 0.f, dtb = 0.f, g_in = 0.f;
     if (jg < nh) {
         if (tg < L) {
             const size_t gi = static_cast<size_t>(tok0 + tg) * a.Hv + h0 + jg;
-            a_raw = a.a[gi];
-            b_raw = a.b[gi];
+            if constexpr (CB) {
+                g_in = a.g_log[gi];
+                b_raw = a.beta_in[gi];
+            } else {
+                a_raw = a.a[gi];
+                b_raw = a.b[gi];
+            }
         }
-        a_mul = expf(a.A_log[h0 + jg]);
-        dtb = a.dt_bias[h0 + jg];
+        if constexpr (!CB) {
+            a_mul = expf(a.A_log[h0 + jg]);
+            dtb = a.dt_bias[h0 + jg];
+        }
     }
     tc::fence_before();
     __syncthreads();
@@ -557,10 +575,16 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sm + P_KQ + tc::sw_chunk(s, c, 128)) = z;
                 *reinterpret_cast<uint4*>(sm + P_KQ + tc::sw_chunk(64 + s, c, 128)) = z;
+                if constexpr (CB) *reinterpret_cast<uint4*>(sm + P_K2 + tc::sw_chunk(s, c, 64)) = z;
             }
             __syncthreads();
         }
-        {
+        if constexpr (CB) {  // the keys and queries come normalised
+            if (tid < C) {
+                rks[tid] = 1.f;
+                rqs[tid] = 1.f;
+            }
+        } else {
             const int rp = tid >> 4, ch = tid & 15;  // 16 threads per row, rows rp + 16 p
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
@@ -584,14 +608,16 @@ __global__ void __launch_bounds__(pf::PNT, 5)
         __syncthreads();
         tc::fence_after();
 
-        // ---- 2. G = [K; Q] K^T
+        // ---- 2. G = [K; Q] K^T (Comba: [P; Q] K^T, K in its own tile)
         if (tid == 0) {
             const uint64_t dKQ = tc::sdesc(sb + P_KQ, 16, 1024);
+            const uint64_t dK2 = tc::sdesc(sb + P_K2, 16, 1024);
             const uint32_t id = idesc_in<F16>(128, 64, 0, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t d = dadd(dKQ, (ks >> 2) * 16384 + (ks & 3) * 32);
-                tc::mma_bf16(tm + P_TM_G, d, d, id, ks > 0);
+                const uint64_t bk = CB ? dadd(dK2, (ks >> 2) * 8192 + (ks & 3) * 32) : d;
+                tc::mma_bf16(tm + P_TM_G, d, bk, id, ks > 0);
             }
             tc::commit(&mbar);
         }
@@ -601,10 +627,15 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             const int t = tg;
             float ell = 0.f, be = 0.f;
             if (t < L) {
-                const float x = in_to_f32<F16>(a_raw) + dtb;
-                const float sp = x > 20.f ? x : log1pf(__expf(x));
-                ell = -a_mul * sp;
-                be = __frcp_rn(1.f + __expf(-in_to_f32<F16>(b_raw)));
+                if constexpr (CB) {
+                    ell = g_in;
+                    be = bf16_to_f32(b_raw);
+                } else {
+                    const float x = in_to_f32<F16>(a_raw) + dtb;
+                    const float sp = x > 20.f ? x : log1pf(__expf(x));
+                    ell = -a_mul * sp;
+                    be = __frcp_rn(1.f + __expf(-in_to_f32<F16>(b_raw)));
+                }
             }
             float g = ell;
 #pragma unroll
@@ -870,7 +901,10 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 // transpose and one 16-byte store per 8 columns.  The control lane issues each MMA batch as soon as
 // the workers' hand-off arrives; the producer lane issues each copy as soon as its buffer's last
 // reader is done.
-template <bool F16>
+// CB (Comba): W from the read keys' rows (one p tile), the state update from the write keys' rows
+// (one k tile: the GDN path double-buffers k because W and the update share it), and the pool
+// holds each head's state as [K][V].
+template <bool F16, bool CB>
 __global__ void __launch_bounds__(pf::NTS, 1)
     gdn_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
     using namespace pf;
@@ -980,15 +1014,31 @@ __global__ void __launch_bounds__(pf::NTS, 1)
 
     // ---- workers' pieces
     // zero the k and v rows of chunk c past the sequence end (before its W and U)
+    // (Comba: the p and v rows, which W and U read; the k rows, which only the update reads and
+    // which land a chunk later, are zeroed by zero_tail_k before the update)
     auto zero_tail = [&](long long c) {
         const int L = chunk_len(c);
-        uint8_t* kt = sm + OFF_K + (c & 1) * 16384;
+        uint8_t* kt = sm + OFF_K + (CB ? 16384 : (c & 1) * 16384);
         for (int e = tid; e < (C - L) * 16; e += NW * 32) {
             const int s = L + (e >> 4), cc = e & 15;
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(kt + tc::sw_chunk(s, cc, 64)) = z;
             *reinterpret_cast<uint4*>(sm + OFF_V + tc::sw_chunk(s, cc, 64)) = z;
         }
+    };
+    auto zero_tail_k = [&](long long c) {  // Comba
+        const int L = chunk_len(c);
+        for (int e = tid; e < (C - L) * 16; e += NW * 32) {
+            const int s = L + (e >> 4), cc = e & 15;
+            *reinterpret_cast<uint4*>(sm + OFF_K + tc::sw_chunk(s, cc, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // workers: the tiles W and U read of chunk c have landed (before zero_tail)
+    auto wait_tiles = [&](long long c) -> bool {
+        if constexpr (CB)
+            return warp_wait(B_K1, c & 1) && warp_wait(B_V, c & 1);
+        else
+            return warp_wait(B_K0 + static_cast<int>(c & 1), (c >> 1) & 1) && warp_wait(B_V, c & 1);
     };
     // W (W^T in TMEM) -> bf16 MN-major B operand: lane f holds W[t][f], t = 16*qt ..
     auto convert_w = [&]() {
@@ -1119,7 +1169,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             };
             // W^T = K^T Tw^T and U^T = V^T Tu^T of chunk c (A MN-major from the token tiles)
             auto issue_wu = [&](long long c) {
-                const uint64_t dK = dadd(dK0, (c & 1) * 16384);
+                const uint64_t dK = dadd(dK0, CB ? 16384u : static_cast<uint32_t>(c & 1) * 16384u);  // Comba: p
                 const uint32_t tu = tm + TM_U + (c & 1) * 64;
                 const uint32_t idw = idesc_in<F16>(128, 64, 1, 0, 0);
 #pragma unroll
@@ -1138,12 +1188,14 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             // its tail)
             auto wu_inputs = [&](long long c) -> bool {
                 if (c == nch - 1 && short_last) return wait_bar(R_Z, 0) && wait_bar(B_R1, c & 1);
-                return wait_bar(B_K0 + static_cast<int>(c & 1), (c >> 1) & 1) && wait_bar(B_V, c & 1) &&
-                       wait_bar(B_R1, c & 1);
+                const bool tile = CB ? wait_bar(B_K1, c & 1) : wait_bar(B_K0 + static_cast<int>(c & 1), (c >> 1) & 1);
+                return tile && wait_bar(B_V, c & 1) && wait_bar(B_R1, c & 1);
             };
             auto wu_ready_now = [&](long long c) -> bool {
-                return !(c == nch - 1 && short_last) && tc::mbar_test(&bars[B_K0 + static_cast<int>(c & 1)], (c >> 1) & 1) &&
-                       tc::mbar_test(&bars[B_V], c & 1) && tc::mbar_test(&bars[B_R1], c & 1);
+                const bool tile = CB ? tc::mbar_test(&bars[B_K1], c & 1)
+                                     : tc::mbar_test(&bars[B_K0 + static_cast<int>(c & 1)], (c >> 1) & 1);
+                return !(c == nch - 1 && short_last) && tile && tc::mbar_test(&bars[B_V], c & 1) &&
+                       tc::mbar_test(&bars[B_R1], c & 1);
             };
 
             do {
@@ -1153,7 +1205,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 for (long long c = 0; c < nch; ++c) {
                     const bool more = c + 1 < nch;
                     const uint32_t par = c & 1;
-                    const uint64_t dK = dadd(dK0, (c & 1) * 16384);
+                    const uint64_t dK = dadd(dK0, CB ? 0u : static_cast<uint32_t>(c & 1) * 16384u);
                     // ---- A. P~^T = S0 Q~^T once S0 is in place, as S0's high parts (shared memory)
                     //      times Q~ plus its low parts (TMEM) times Q~; then, once W is in place,
                     //      Delta^T = U^T - S0 W^T (high parts; accumulated onto U^T, B negated)
@@ -1178,6 +1230,14 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         for (int ks = 0; ks < 8; ++ks)
                             tc::mma_bf16(tm + TM_U + (c & 1) * 64, dadd(dS0, (ks >> 2) * 16384 + (ks & 3) * 32),
                                          dadd(dWmn, ks * 2048), idd, 1u);
+                        // Comba: with p != k the chunk transition is not a contraction and the
+                        // rounding of S0 grows from chunk to chunk: its low parts (TMEM) too
+                        if constexpr (CB) {
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks)
+                                tc::mma_bf16_ts(tm + TM_U + (c & 1) * 64, tm + TM_SL + 8 * ks, dadd(dWmn, ks * 2048),
+                                                idd, 1u);
+                        }
                         tc::commit(&bars[B_A]);
                         mark(B_A, par);
                     }
@@ -1191,6 +1251,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     // ---- C. S += Delta~^T K, which the workers wait for, then O^T = P~^T + Delta^T M~^T
                     //      (three hi / lo products), stored by the workers while they wait for Delta
                     if (!wait_bar(R_B, par) || !wait_bar(B_RM, par)) break;
+                    if (CB && !wait_bar(B_K0, par)) break;  // Comba: the update's own k tile
                     if (!wu_done && wu_ready_now(c + 1)) {
                         tc::fence_after();
                         issue_wu(c + 1);
@@ -1263,9 +1324,15 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 tc::bulk_load(sb + dst, rec + from, bytes, &bars[bar]);
                 mark(bar, parity);
             };
-            auto fetch_k = [&](long long c) {
-                fetch_rows(&maps.k, hk, bos + c * C, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1),
-                           (c >> 1) & 1);
+            auto fetch_k = [&](long long c) {  // Comba: one k tile, for the update
+                if constexpr (CB)
+                    fetch_rows(&maps.k, hk, bos + c * C, OFF_K, B_K0, c & 1);
+                else
+                    fetch_rows(&maps.k, hk, bos + c * C, OFF_K + (c & 1) * 16384, B_K0 + static_cast<int>(c & 1),
+                               (c >> 1) & 1);
+            };
+            auto fetch_p = [&](long long c) {  // Comba: one p tile, for W
+                fetch_rows(&maps.p, hk, bos + c * C, OFF_K + 16384, B_K1, c & 1);
             };
             // v = 0 for the identity-start chain: a box wholly past the last token reads as zeros
             auto fetch_v = [&](long long c) {
@@ -1279,17 +1346,19 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                           (c >> 1) & 1);
             };
             fetch_k(0);
+            if constexpr (CB) fetch_p(0);
             fetch_v(0);
             fetch_r1(0);
             fetch_qt(0);
             fetch_rm(0);
             fetch_rv(0);
-            if (nch > 1) fetch_k(1);
+            if (!CB && nch > 1) fetch_k(1);
             do {
                 if (!wait_bar(B_WU, 0)) break;
-                if (nch > 1) {  // U read the v tile, W and U the record part
+                if (nch > 1) {  // U read the v tile, W and U the record part (and Comba's W the p tile)
                     fetch_v(1);
                     fetch_r1(1);
+                    if constexpr (CB) fetch_p(1);
                 }
                 for (long long c = 0; c < nch; ++c) {
                     const bool more = c + 1 < nch;
@@ -1299,13 +1368,14 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                         fetch_qt(c + 1);
                         fetch_rv(c + 1);  // its buffer's last reader, chunk c - 1's Delta conversion, is done
                         if (!wait_bar(B_WU, (c + 1) & 1)) break;
-                        if (c + 2 < nch) {  // U read the v tile, W and U the record part
+                        if (c + 2 < nch) {  // U read the v tile, W and U the record part (Comba: W the p tile)
                             fetch_v(c + 2);
                             fetch_r1(c + 2);
+                            if constexpr (CB) fetch_p(c + 2);
                         }
                     }
                     if (!wait_bar(B_C, par)) break;
-                    if (c + 2 < nch) fetch_k(c + 2);   // the update read this k tile
+                    if (CB ? more : c + 2 < nch) fetch_k(CB ? c + 1 : c + 2);  // the update read this k tile
                     if (!wait_bar(B_O, par)) break;
                     if (more) fetch_rm(c + 1);         // M~ Delta read M~
                 }
@@ -1328,7 +1398,10 @@ __global__ void __launch_bounds__(pf::NTS, 1)
 #pragma unroll
                 for (int c16 = 0; c16 < 2; ++c16) {
                     float v[16];
-                    if (kind <= kPfFirst) {
+                    if (kind <= kPfFirst && CB) {  // Comba's pool holds [K][V]: lanes read consecutive v
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = Sg[static_cast<size_t>(32 * qt + 16 * c16 + j) * D + row];
+                    } else if (kind <= kPfFirst) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float4 f = src[c16 * 4 + j];
@@ -1356,7 +1429,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
             }
             warp_arrive(R_S);  // S0 of chunk 0 in place
             if (nch == 1 && short_last) {
-                if (!warp_wait(B_K0, 0) || !warp_wait(B_V, 0)) break;
+                if (!wait_tiles(0)) break;
                 zero_tail(0);
                 warp_arrive(R_Z);
             }
@@ -1369,6 +1442,10 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                 const uint32_t par = c & 1;
                 if (!warp_wait(B_A, par) || !warp_wait(B_RV0 + static_cast<int>(c & 1), (c >> 1) & 1)) { ok = false; break; }
                 convert_delta(c);
+                if (CB && c == nch - 1 && short_last) {  // the update's k rows past the end
+                    if (!warp_wait(B_K0, c & 1)) { ok = false; break; }
+                    zero_tail_k(c);
+                }
                 warp_arrive(R_B);
                 if (!warp_wait(B_C, par)) { ok = false; break; }
                 if (more) {
@@ -1376,7 +1453,7 @@ __global__ void __launch_bounds__(pf::NTS, 1)
                     warp_arrive(R_S);
                     const long long c1 = c + 1;
                     if (c1 == nch - 1 && short_last) {
-                        if (!warp_wait(B_K0 + static_cast<int>(c1 & 1), (c1 >> 1) & 1) || !warp_wait(B_V, c1 & 1)) {
+                        if (!wait_tiles(c1)) {
                             ok = false;
                             break;
                         }
@@ -1405,9 +1482,14 @@ __global__ void __launch_bounds__(pf::NTS, 1)
         float4* dst = reinterpret_cast<float4*>(Sdst + static_cast<size_t>(row) * D + 32 * qt);
         float s32[32];
         ld32(trow + TM_S + 32 * qt, s32);
+        if (CB && kind == kPfWhole) {  // Comba's pool holds [K][V]
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(s32[4 * i], s32[4 * i + 1], s32[4 * i + 2], s32[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) Sdst[static_cast<size_t>(32 * qt + i) * D + row] = s32[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(s32[4 * i], s32[4 * i + 1], s32[4 * i + 2], s32[4 * i + 3]);
+        }
     }
     tc::fence_before();
     __syncthreads();
@@ -1441,7 +1523,7 @@ constexpr uint32_t FX_SMEM = FX_USED + 1024;   // + alignment slack
 constexpr uint32_t FX_COLS = 128;              // two 64-column product buffers
 }  // namespace pf
 
-template <bool F16>
+template <bool F16, bool CB>
 __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const __grid_constant__ PrefillArgs a) {
     using namespace pf;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1612,7 +1694,8 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
             }
             __syncwarp();
         } else {
-            float4* Sdst4 = reinterpret_cast<float4*>(a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * DD);
+            float* Sdst = a.state_pool + (static_cast<size_t>(slot) * a.Hv + h) * DD;
+            float4* Sdst4 = reinterpret_cast<float4*>(Sdst);
             const float4* Bz4 = reinterpret_cast<const float4*>(state_of(1));
             for (int j = 0; j < 2; ++j) {
                 if (!warp_wait(MMA_DONE + j, 0)) break;
@@ -1622,8 +1705,17 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 b0 = Bz4[o4 + i];
-                    Sdst4[o4 + i] = make_float4(d[4 * i] + b0.x, d[4 * i + 1] + b0.y, d[4 * i + 2] + b0.z,
-                                                d[4 * i + 3] + b0.w);
+                    const float4 r = make_float4(d[4 * i] + b0.x, d[4 * i + 1] + b0.y, d[4 * i + 2] + b0.z,
+                                                 d[4 * i + 3] + b0.w);
+                    if constexpr (CB) {  // Comba's pool holds [K][V]: column k of row v
+                        const size_t k0 = 64 * j + 32 * half + 4 * i;
+                        Sdst[(k0 + 0) * D + row] = r.x;
+                        Sdst[(k0 + 1) * D + row] = r.y;
+                        Sdst[(k0 + 2) * D + row] = r.z;
+                        Sdst[(k0 + 3) * D + row] = r.w;
+                    } else {
+                        Sdst4[o4 + i] = r;
+                    }
                 }
             }
         }

@@ -113,6 +113,26 @@ def comba_forward_inputs(g: np.random.Generator, B: int, T: int, H: int, K: int,
 # ------------------------------------------------------------------------------------------------
 # Prefill
 # ------------------------------------------------------------------------------------------------
+def comba_prefill_inputs(g: np.random.Generator, seqlens, H: int, K: int, V: int, pool: int,
+                         mild: bool = False) -> dict:
+    """Varlen Comba prefill inputs, every token drawn as comba_decode_token draws one: q, k, p
+    [T,H,K] bf16; v [T,H,V] bf16; beta bf16, g_log fp32 [T,H]; state_pool [pool,H,K,V] fp32 =
+    0.05 randn; distinct cache_indices.  mild divides the log decays by 25, so that the state
+    carried from chunk to chunk is not wiped out."""
+    seqlens = [int(s) for s in seqlens]
+    T = int(sum(seqlens))
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(seqlens)
+    x = comba_decode_token(g, T, H, K, V)
+    if mild:
+        x["g_log"] = (x["g_log"] / np.float32(25.0)).astype(np.float32)
+    x["state_pool"] = (_randn(g, (pool, H, K, V)) * np.float32(0.05)).astype(np.float32)
+    x["cache_indices"] = g.choice(pool, size=len(seqlens), replace=False).astype(np.int64)
+    x["cu_seqlens"] = cu
+    x["T"] = T
+    return x
+
+
 def gdn_prefill_inputs(g: np.random.Generator, seqlens, Hk: int, Hv: int, K: int, V: int,
                        pool: int, mild_gates: bool = False, dtype: str = "bf16") -> dict:
     """Varlen prefill inputs.  mild_gates draws A_log = log(U(0.01, 0.1)) instead of

@@ -11,6 +11,7 @@
  *   gdn_prefill_chunked  varlen chunkwise-WY prefill over a pooled state, gates derived in-kernel
  *   gdn_prefill_chunked_f16  the same with IEEE binary16 token arrays
  *   gdn_prefill_chunked_noalloc  the same with the library's own fixed-size workspace
+ *   comba_prefill_chunked  varlen chunkwise-WY prefill of the Comba recurrence over a pooled state
  *   gdn_window_fused     fused decode window: conv + SiLU, L2 norm, gates, recurrence over ntok
  *                        tokens, gated RMSNorm, with verify / commit / partial commit
  *
@@ -247,6 +248,33 @@ gdn_status gdn_prefill_chunked_f16(const void* q, const void* k, const void* v, 
                                    int K, int V, int chunk_size, float scale, void* out,
                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                    gdn_stream_t stream);
+
+/*
+ * comba_prefill_chunked -- varlen prefill of the Comba recurrence ([comba spec] spec_md: the decode
+ * step is the comba-forward recurrence for one token; here over every token of num_seqs sequences),
+ * computed chunk by chunk with the same WY representation as gdn_prefill_chunked ([gdn_chunkwise]
+ * steps 1-3), the read key p taking k's place where the state is read (the in-chunk triangular
+ * system and W) and k kept where it is written.  Per sequence n and head h:
+ *     S <- state_pool[cache_indices[n], h]  (K x V, V contiguous);  per token t:
+ *     S <- exp(g_t) S;  u = beta_t (v_t - S^T p_t);  S <- S + k_t u^T;  out_t = S^T (scale q_t);
+ *     state_pool[cache_indices[n], h] <- S.
+ *   q, k, p        bf16 [T, H, K]     used as given (the spec passes them L2-normalised)
+ *   v              bf16 [T, H, V]
+ *   beta           bf16 [T, H]        the value itself
+ *   g              f32  [T, H]        log decay (the gate is exp(g))
+ *   state_pool     f32  [pool_size, H, K, V]  updated IN PLACE at the referenced slots only
+ *   out            bf16 [T, H, V]     16-byte aligned
+ *   q, k, p, v     16-byte aligned; beta 2-byte, g 4-byte aligned
+ * cache_indices, cu_seqlens, workspace (gdn_prefill_workspace_size(num_seqs, T, H, H, K, V,
+ * chunk_size)), dev_status, chunk_size and the checks are those of gdn_prefill_chunked.
+ * Supported: K = V = 128, chunk_size 64 or 128.
+ */
+gdn_status comba_prefill_chunked(const void* q, const void* k, const void* v, const void* p,
+                                 const void* beta, const float* g, float* state_pool, int pool_size,
+                                 const int64_t* cache_indices, const int64_t* cu_seqlens, int num_seqs,
+                                 int64_t T, int H, int K, int V, int chunk_size, float scale, void* out,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 gdn_stream_t stream);
 
 /*
  * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot allocate device memory

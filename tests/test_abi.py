@@ -134,6 +134,26 @@ def test_prefill_validation(lib, name):
     assert call(N, 0, num_seqs=0) == gdn.GDN_OK
 
 
+def test_comba_prefill_validation(lib):
+    f = lib.comba_prefill_chunked
+    pool, out = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 40)
+    need = gdn.gdn_prefill_workspace_size(2, 100, 2, 2, 128, 128, 64)
+    ws = ctypes.c_void_p(1 << 44)
+
+    def call(ws=ws, ws_bytes=need, chunk=64, num_seqs=2, K=128, p=P, g=P, beta=P):
+        # (q, k, v, p, beta, g, state_pool, pool_size, cache_indices, cu_seqlens, num_seqs, T, H, K, V,
+        #  chunk_size, scale, out, workspace, workspace_bytes, dev_status, stream)
+        return f(P, P, P, p, beta, g, pool, 4, P, P, num_seqs, 100, 2, K, 128, chunk, 1.0, out, ws, ws_bytes, P, N)
+    assert call(ws=N, ws_bytes=0) == gdn.GDN_ERR_INVALID_ARG and "workspace" in gdn.last_error()
+    assert gdn.last_error().startswith("comba_prefill_chunked:")
+    assert call(p=N) == gdn.GDN_ERR_INVALID_ARG and "null token pointer" in gdn.last_error()
+    assert call(p=ctypes.c_void_p(24)) == gdn.GDN_ERR_INVALID_ARG   # p must be 16-byte aligned
+    assert call(g=ctypes.c_void_p(18)) == gdn.GDN_ERR_INVALID_ARG   # g must be 4-byte aligned
+    assert call(chunk=32) == gdn.GDN_ERR_UNSUPPORTED and "64 or 128" in gdn.last_error()
+    assert call(K=64) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(ws=N, ws_bytes=0, num_seqs=0) == gdn.GDN_OK
+
+
 def test_comba_forward_validation(lib):
     f = lib.comba_forward
     st, o = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 40)
