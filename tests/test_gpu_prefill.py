@@ -328,3 +328,51 @@ def test_rejections():
         gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
                                 d["state_pool"], d["cache_indices"], d["cu_seqlens"], 96)
     assert e.value.status == gdn.GDN_ERR_UNSUPPORTED  # chunk sizes other than 64 and 128
+
+
+def _plan(ws, N, T):
+    # the schedule in the workspace header (layout in gdn.h): after the chunk offsets (8 bytes per
+    # sequence + 1, padded to 16) and the chunk table (16 bytes per chunk of cap), the plan
+    # (int ntask, int nsplit, int64 nscr), num_seqs + 16 tasks (int4) and 8 splits (int4:
+    # sequence, first-part chunks, first scratch chunk)
+    cap = (T + 63) // 64 + N
+    off = (8 * (N + 1) + 15) // 16 * 16 + 16 * cap
+    raw = ws.cpu().numpy()
+    ntask, nsplit = (int(v) for v in raw[off:off + 8].view(np.int32))
+    nscr = int(raw[off + 8:off + 16].view(np.int64)[0])
+    tasks = raw[off + 16:off + 16 + 16 * (N + 16)].view(np.int32).reshape(-1, 4)[:ntask, :3]
+    so = off + 16 + 16 * (N + 16)
+    splits = raw[so:so + 16 * 8].view(np.int32).reshape(-1, 4)[:nsplit, :3]
+    return ntask, nsplit, nscr, tasks.tolist(), splits.tolist()
+
+
+@pytest.mark.parametrize("seqlens,Hv,expect", [
+    # 21, 15, 11 and 1 chunks, 2 value heads: cut 21 -> 11 + 10 and 15 -> 8 + 7; cutting 11 would
+    # not shorten the longest chain (11) by 10 %
+    ([1300 + 20, 900, 700, 40], 2, [[0, 11, 0], [1, 8, 10]]),
+    # the benchmark's lengths with 32 value heads: only the 8192-token sequence (128 chunks) is cut
+    ([4096, 2048, 1024, 8192], 32, [[3, 64, 0]]),
+    # 7 chunks: below the 8-chunk minimum
+    ([448], 2, []),
+])
+def test_split_schedule(seqlens, Hv, expect):
+    N = len(seqlens)
+    x = gi.gdn_prefill_inputs(gi.rng(3), seqlens, 1, Hv, 128, 128, pool=N + 1, mild_gates=True)
+    d = _to_dev(x)
+    T = x["T"]
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(N, T, 1, Hv, 128, 128, 64), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["state_pool"],
+                            d["cache_indices"], d["cu_seqlens"], 64, out=None, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ntask, nsplit, nscr, tasks, splits = _plan(ws, N, T)
+    assert splits == expect
+    assert nsplit == len(expect) and ntask == N + 2 * nsplit
+    assert nscr == sum((seqlens[s] + 63) // 64 - n1 for s, n1, _ in expect)
+    # tasks: the split sequences' three chains first (first part, zero start, identity start), then
+    # the other sequences in order; every sequence appears
+    split_seqs = [s for s, _, _ in expect]
+    want = [[s, kind, j] for j, s in enumerate(split_seqs) for kind in (1, 2, 3)]
+    want += [[n, 0, 0] for n in range(N) if n not in split_seqs]
+    assert tasks == want
