@@ -279,7 +279,7 @@ gdn_status comba_prefill_chunked(const void* q, const void* k, const void* v, co
 /*
  * gdn_prefill_chunked_noalloc -- gdn_prefill_chunked for callers that cannot allocate device memory
  * themselves, for instance code running under a host framework whose allocator owns all device
- * memory, or in a place where calling cudaMalloc is not allowed.  The paper has no counterpart: this
+ * memory, or in a place where calling cudaMalloc is not allowed.  No page has a counterpart: this
  * is a deployment variant, not a different computation.  Same arguments, layouts and results as
  * gdn_prefill_chunked, without the workspace arguments.
  *
