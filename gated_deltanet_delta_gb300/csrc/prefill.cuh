@@ -787,7 +787,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p}
                 const float* Lr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB;
                 const float* Tc = Ls + (32 * pB) * LST + 32 * pB + cB;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
                     const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
@@ -795,17 +795,18 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
-                        acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
-                        acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
+                        const float2 l2 = make_float2(lk[w], lk[w]);
+                        a01 = __ffma2_rn(l2, make_float2(t4.x, t4.y), a01);
+                        a23 = __ffma2_rn(l2, make_float2(t4.z, t4.w), a23);
                     }
                 }
-                *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = acc;
+                *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = make_float4(a01.x, a01.y, a23.x, a23.y);
             }
             __syncthreads();
             if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p}
                 const float* Tr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
                 const float* Xc = Zs + (16 * pB) * ZST + cB;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
                     const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
@@ -813,19 +814,20 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 x4 = *reinterpret_cast<const float4*>(Xc + (4 * k4 + w) * ZST);
-                        acc.x = fmaf(tk[w], x4.x, acc.x); acc.y = fmaf(tk[w], x4.y, acc.y);
-                        acc.z = fmaf(tk[w], x4.z, acc.z); acc.w = fmaf(tk[w], x4.w, acc.w);
+                        const float2 l2 = make_float2(tk[w], tk[w]);
+                        a01 = __ffma2_rn(l2, make_float2(x4.x, x4.y), a01);
+                        a23 = __ffma2_rn(l2, make_float2(x4.z, x4.w), a23);
                     }
                 }
                 *reinterpret_cast<float4*>(Ls + (32 * pB + 16 + rB) * LST + 32 * pB + cB) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                    make_float4(-a01.x, -a01.y, -a23.x, -a23.y);
             }
             __syncthreads();
             const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
             {  // Z = Lm_bl T_tl (all 256 threads)
                 const float* Lr = Ls + (32 + rC) * LST;
                 const float* Tc = Ls + cC;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
                     const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
@@ -833,17 +835,18 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 t4 = *reinterpret_cast<const float4*>(Tc + (4 * k4 + w) * LST);
-                        acc.x = fmaf(lk[w], t4.x, acc.x); acc.y = fmaf(lk[w], t4.y, acc.y);
-                        acc.z = fmaf(lk[w], t4.z, acc.z); acc.w = fmaf(lk[w], t4.w, acc.w);
+                        const float2 l2 = make_float2(lk[w], lk[w]);
+                        a01 = __ffma2_rn(l2, make_float2(t4.x, t4.y), a01);
+                        a23 = __ffma2_rn(l2, make_float2(t4.z, t4.w), a23);
                     }
                 }
-                *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = acc;
+                *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = make_float4(a01.x, a01.y, a23.x, a23.y);
             }
             __syncthreads();
             {  // T_bl = -T_br Z, over Lm_bl
                 const float* Tr = Ls + (32 + rC) * LST + 32;
                 const float* Zc = Zs + cC;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
                     const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
@@ -851,11 +854,12 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 z4 = *reinterpret_cast<const float4*>(Zc + (4 * k4 + w) * ZST);
-                        acc.x = fmaf(tk[w], z4.x, acc.x); acc.y = fmaf(tk[w], z4.y, acc.y);
-                        acc.z = fmaf(tk[w], z4.z, acc.z); acc.w = fmaf(tk[w], z4.w, acc.w);
+                        const float2 l2 = make_float2(tk[w], tk[w]);
+                        a01 = __ffma2_rn(l2, make_float2(z4.x, z4.y), a01);
+                        a23 = __ffma2_rn(l2, make_float2(z4.z, z4.w), a23);
                     }
                 }
-                *reinterpret_cast<float4*>(Ls + (32 + rC) * LST + cC) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                *reinterpret_cast<float4*>(Ls + (32 + rC) * LST + cC) = make_float4(-a01.x, -a01.y, -a23.x, -a23.y);
             }
             __syncthreads();
 
