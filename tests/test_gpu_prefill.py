@@ -376,3 +376,33 @@ def test_split_schedule(seqlens, Hv, expect):
     want = [[s, kind, j] for j, s in enumerate(split_seqs) for kind in (1, 2, 3)]
     want += [[n, 0, 0] for n in range(N) if n not in split_seqs]
     assert tasks == want
+
+
+def test_split_with_more_fixup_jobs_than_sms():
+    # One 200-chunk sequence over 80 value heads: the schedule splits it 100 + 100, and the fix-up's
+    # jobs (a state job and a chunk job per head, 160) outnumber its one-CTA-per-SM grid, so some
+    # CTAs run two jobs (fresh barriers for the second).  The oracle runs on sampled heads.
+    Hk, Hv = 8, 80
+    seqlens = [200 * 64 - 5]
+    x = gi.gdn_prefill_inputs(gi.rng(77), seqlens, Hk, Hv, 128, 128, pool=2, mild_gates=True)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    T = x["T"]
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(1, T, Hk, Hv, 128, 128, 64), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                  d["state_pool"], d["cache_indices"], d["cu_seqlens"], 64, scale=scale,
+                                  workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ntask, nsplit, nscr, tasks, splits = _plan(ws, 1, T)
+    assert splits == [[0, 100, 0]] and nscr == 100
+    o, pool = host(out), host(d["state_pool"])
+    slot = int(x["cache_indices"][0])
+    for h in (0, 41, 79):  # the unit oracle on the one key head and value head involved
+        hk = h // (Hv // Hk)
+        S, o_ref = oracle.gdn_prefill_unit(x["q"][:, hk:hk + 1], x["k"][:, hk:hk + 1], x["v"][:, h:h + 1],
+                                           x["a"][:, h:h + 1], x["b"][:, h:h + 1], x["A_log"][h], x["dt_bias"][h],
+                                           x["state_pool"][slot, h], 0, scale)
+        assert max_rel_err(o[:, h], o_ref) <= OUT_TOL, h
+        assert max_rel_err(pool[slot, h], S) <= STATE_TOL, h
