@@ -248,12 +248,13 @@ __global__ void __launch_bounds__(NT) gdn_decode_multi_kernel(const DecodeMultiA
                     rq[r] += __shfl_xor_sync(kFullMask, rq[r], o);
                 }
             }
-            // pass 2: delta, the readout, the rank-1 update
+            // pass 2: delta, the readout, the rank-1 update (one reciprocal of c per token)
+            const float ic = 1.f / c;
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const float delta = (vs[tt][r * RPP + rw] - c * rk[r]) * beta;
                 const float yv = a.scale * fmaf(delta, kq, c * rq[r]);
-                const float dc = delta / c;
+                const float dc = delta * ic;
                 const float2 d2 = make_float2(dc, dc);
 #pragma unroll
                 for (int m = 0; m < NV; ++m) {
