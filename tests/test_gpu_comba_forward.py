@@ -89,3 +89,25 @@ def test_benchmark_workload_sampled_heads():
                                             x["v"][sl], x["p"][sl], x["beta"][sl], x["g_log"][sl], scale)
         assert max_rel_err(S[b, h], ref_S[0, 0]) <= TOL, (b, h)
         assert max_rel_err(o[b, :, h], ref_o[0, :, 0]) <= TOL, (b, h)
+
+
+def test_gate_extremes():
+    # g = -inf (the state wiped at that token), g = 0 (no decay), beta = 0 and beta = 1, over three
+    # chunks of tokens with a ragged tail
+    B, T, H, K, V = 2, 19, 3, 128, 128
+    x = gi.comba_forward_inputs(gi.rng(11), B, T, H, K, V)
+    x["g_log"][:, 3, 0] = -np.inf
+    x["g_log"][:, 9:12, 1] = -np.inf
+    x["g_log"][:, :, 2] = 0.0
+    x["beta"][0, 5:9, :] = 0.0
+    x["beta"][1, 12:, :] = 1.0
+    scale = K ** -0.5
+    ref_S, ref_o = oracle.comba_forward(x["state"], x["q"], x["k"], x["v"], x["p"], x["beta"],
+                                        x["g_log"], scale)
+    assert np.isfinite(ref_S).all() and np.isfinite(ref_o).all()
+    S, o = _run(_dev(x), scale, torch.float32)
+    assert np.isfinite(S).all() and np.isfinite(o).all()
+    for b in range(B):
+        for h in range(H):
+            assert max_rel_err(S[b, h], ref_S[b, h]) <= TOL, (b, h)
+            assert max_rel_err(o[b, :, h], ref_o[b, :, h]) <= TOL, (b, h)
