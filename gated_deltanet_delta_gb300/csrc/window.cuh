@@ -12,18 +12,23 @@
 // 0x100|k: token k; 0: never).
 //
 // GB300 mapping.  A CTA of 128 threads owns one (n, h) head: lane (column group cg, row block rb)
-// of warp w holds the 4 columns 32w + 4cg .. of the 32 rows 32rb .. 32rb+31 in registers for the
-// whole window, so the 64 KB head state is read from HBM once and written at most once.  Both
-// reductions over the 128 rows (kv and o) are a register sum plus two xor-shuffles inside the warp,
-// so a token needs one barrier (after the conv outputs are written; the per-token buffers are
-// double-buffered by token parity).  The kernel is bound by instruction issue and latency, not
-// memory, so the per-element work is three packed f32x2 FMAs per two elements and token, and the
-// per-token scalar work (conv, norms, gates) is shared by 128 state elements per thread: the state
-// is held as c * R with a per-head scalar c (the gate multiplies c; R += k (rk delta / c) is the
-// rank-1 update; c is folded back into R when it drops below 2^-40), and the q/k norms are applied
-// to reduced sums.  Each thread convolves q and k channel t of key head hk and v channel t of its
-// value head, with histories and taps in registers, a token ahead of their use; the gated RMSNorm
-// reads the head's outputs of every token from shared memory after the last token.
+// of warp w holds the 4 columns 32w + 4cg .. of the 32 rows 32rb .. 32rb+31 in registers, so the
+// 64 KB head state is read from HBM once and written at most once.  The window's tokens are not
+// stepped one by one: their conv outputs, gates and Gram entries do not depend on the state, so the
+// window runs as one chunk of the WY form (with k^_t = rk_t k_t, w_s = rk_s u_s, D_ts the product of
+// the gates of tokens s+1 .. t and gamma_t that of tokens 0 .. t):
+//     u_t = beta_t (v_t - rk_t (gamma_t S0^T k_t + sum_{s<t} D_ts (k_t . k_s) w_s))
+//     o_t = rq_t / sqrt(128) (gamma_t S0^T q_t + sum_{s<=t} D_ts (q_t . k_s) w_s)
+//     S after m tokens = gamma_{m-1} S0 + sum_{s<m} D_{m-1,s} k_s w_s^T
+// -- the single steps regrouped (u_t is token t's delta, w_t = rk_t delta_t).  So the kernel is a
+// conv prologue for every token, one pass over the slab forming S0^T k_t and S0^T q_t for all tokens
+// (the reductions over the rows are register sums plus two xor-shuffles inside the warp), a
+// per-column triangular solve (thread t owns column t, which its own warp holds), and, when the
+// window commits, one pass applying the rank-m write: three CTA barriers per window.  The q and k
+// L2 norms are scalars folded into the solve (|k_t|^2 and |q_t|^2 come with the Gram entries);
+// every decay is the exponential of a sum of log gates over its own segment.  Each thread
+// convolves q and k channel t of key head hk and v channel t of its value head for every token;
+// the gated RMSNorm of each token's 128 outputs follows the last barrier.
 #pragma once
 
 #include "common.cuh"
@@ -35,10 +40,6 @@ __device__ __forceinline__ float silu_f32(float s) { return __fdividef(s, 1.0f +
 __device__ __forceinline__ float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float softplus_f32(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 
-// The state of a head half is kept as c * R (c a per-head scalar, R in registers): the gate then
-// scales c, not every element, and the rank-1 update becomes R += k (rk delta / c).  When c drops
-// below kWinRenorm it is folded back into R.
-constexpr float kWinRenorm = 9.094947e-13f;  // 2^-40
 
 // Asynchronous 4-byte global -> shared copy (completes at cp_async_wait_all of the same thread).
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
@@ -50,21 +51,22 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const WindowArgs a) {
-    constexpr int D = kWinD, NR = 32;  // rows per lane
-    static_assert(kWinThreads == 128 && D == 128, "window tile");
-
-    // per-token buffers, double-buffered by token parity: one barrier per token.  q and k of a
-    // token by row block of 32, padded to a stride of 36 floats so that the four row blocks a warp
-    // reads at once fall in different banks
-    constexpr int RBS = 36;
-    __shared__ __align__(16) float qraw[2][4 * RBS];
-    __shared__ __align__(16) float kraw[2][4 * RBS];
-    __shared__ __align__(16) float vraw[2][D];
-    __shared__ float gates[kWinMaxTok][2];  // gate and beta of every token, computed up front
-    __shared__ __align__(16) float osm[kWinMaxTok][D];
-    __shared__ float ssw[kWinMaxTok][4];  // per-warp sums of o^2
-    __shared__ float ss[kWinMaxTok];
-    __shared__ float zs[kWinMaxTok * D];  // the epilogue's z and gamma, fetched up front
+    constexpr int D = kWinD, NR = 32, TK = kWinMaxTok;  // rows per lane, tokens per window at most
+    static_assert(kWinThreads == 128 && D == 128 && TK == 8, "window tile");
+    // conv outputs of q and k by token, channels by row block of 32 padded to a stride of 36 floats
+    // so that the four row blocks a warp reads at once fall in different banks
+    // (and by token at a stride of 148 floats, so that the Gram's eight keys fall in different banks)
+    constexpr int RBS = 36, TSTR = 4 * RBS + 4;
+    __shared__ __align__(16) float qc[TK][TSTR];
+    __shared__ __align__(16) float kc[TK][TSTR];
+    __shared__ __align__(16) float kvp[TK][D];  // S0^T k_t (raw k)
+    __shared__ __align__(16) float qrp[TK][D];  // S0^T q_t (raw q)
+    __shared__ __align__(16) float wsm[TK][D];  // w_t = rk_t delta_t
+    __shared__ float kkd[TK][TK], qkd[TK][TK];  // D_ts (k_t . k_s), s < t; D_ts (q_t . k_s), s <= t
+    __shared__ float kk2[TK], qq2[TK];          // |k_t|^2, |q_t|^2
+    __shared__ float lg[TK], bet[TK], gam[TK], gtl[TK];  // log gate, beta, gamma_t, D_{m-1,t}
+    __shared__ float ssw[TK][4];                // per-warp sums of o^2
+    __shared__ float zs[TK * D];                // the epilogue's z and gamma, fetched up front
     __shared__ float gs[D];
 
     const int unit = blockIdx.x;  // n * h_v + h
@@ -76,13 +78,12 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
     const int rb = lane >> 3;             // block of 32 rows
     const int col = 32 * warp + 4 * cg;   // first of this lane's 4 columns
     const int C = (2 * a.h_k + a.h_v) * D;
-    const int ntok = a.ntok;
+    const int ntok = a.ntok, m = a.commit_at;
 
-    // ---- the state: rows 32rb .. 32rb+31, columns col .. col+3, held as cs * R
+    // ---- the state: rows 32rb .. 32rb+31, columns col .. col+3, packed along rows:
+    // R[p][j] = (S[32rb + 2p][col + j], S[32rb + 2p + 1][col + j])
     const size_t row_stride = size_t(a.h_v) * D;
     float* sbase = a.state + size_t(n) * D * row_stride + size_t(h) * D + col;
-    // packed along rows: R[p][j] = (S[2p][j], S[2p+1][j]) of this lane's rows and 4 columns, so that
-    // the per-row k and q pairs come straight from float4 loads
     float2 R[NR / 2][4];
 #pragma unroll
     for (int p = 0; p < NR / 2; ++p) {
@@ -93,185 +94,258 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
         R[p][2] = make_float2(x.z, y.z);
         R[p][3] = make_float2(x.w, y.w);
     }
-    float cs = 1.0f;
 
-    // ---- this thread's conv channels: q, k of key head hk and v of value head h, channel tid
+    // ---- conv + SiLU of this thread's channels (q, k of key head hk; v of value head h; channel
+    // tid) for every token; the committed history; tokens past ntok read as zero
     const int ch_q = hk * D + tid;
     const int ch_k = (a.h_k + hk) * D + tid;
     const int ch_v = (2 * a.h_k + h) * D + tid;
     const float* hist_n = a.hist + size_t(n) * C * 3;
-    float hq[3], hk3[3], hv[3];
+    const float* x_n = a.qkv + size_t(n) * ntok * C;
+    // the sequence h0 h1 h2 x0 .. x_{ntok-1} of each channel
+    float sq[TK + 3], sk[TK + 3], sv[TK + 3];
 #pragma unroll
     for (int e = 0; e < 3; ++e) {
-        hq[e] = hist_n[size_t(ch_q) * 3 + e];
-        hk3[e] = hist_n[size_t(ch_k) * 3 + e];
-        hv[e] = hist_n[size_t(ch_v) * 3 + e];
+        sq[e] = hist_n[size_t(ch_q) * 3 + e];
+        sk[e] = hist_n[size_t(ch_k) * 3 + e];
+        sv[e] = hist_n[size_t(ch_v) * 3 + e];
+    }
+#pragma unroll
+    for (int t = 0; t < TK; ++t) {
+        const bool on = t < ntok;
+        sq[t + 3] = on ? x_n[size_t(t) * C + ch_q] : 0.f;
+        sk[t + 3] = on ? x_n[size_t(t) * C + ch_k] : 0.f;
+        sv[t + 3] = on ? x_n[size_t(t) * C + ch_v] : 0.f;
     }
     const float4 wq = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_q) * 4);
     const float4 wk = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_k) * 4);
     const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + size_t(ch_v) * 4);
-    const bool own_qk = h < a.h_k;  // the q/k history of key head hk is written by head h == hk
-    const float dth = a.dt[h], ssm = a.ssm_a[h];
-    const float* x_n = a.qkv + size_t(n) * ntok * C;
-    float xq = x_n[ch_q], xk = x_n[ch_k], xv = x_n[ch_v];
-    // every token's gate and beta (thread t), read after the first token's barrier
-    if (tid < ntok) {
-        const size_t gi = (size_t(n) * ntok + tid) * a.h_v + h;
-        gates[tid][0] = expf(softplus_f32(a.alpha[gi] + dth) * ssm);
-        gates[tid][1] = sigmoid_f32(a.beta[gi]);
-    }
     // the epilogue's z (token i, column tid) and gamma, copied asynchronously now
 #pragma unroll
-    for (int i = 0; i < kWinMaxTok; ++i)
+    for (int i = 0; i < TK; ++i)
         if (i < ntok) cp_async4(&zs[i * D + tid], a.z + ((size_t(n) * ntok + i) * a.h_v + h) * D + tid);
     cp_async4(&gs[tid], a.gamma + tid);
 
-    for (int t = 0; t < ntok; ++t) {
-        const int b = t & 1;
-        float nq = 0.f, nk = 0.f, nv = 0.f;
-        if (t + 1 < ntok) {
-            const float* xn = x_n + size_t(t + 1) * C;
-            nq = xn[ch_q];
-            nk = xn[ch_k];
-            nv = xn[ch_v];
-        }
-        // conv + SiLU, history shift, committed history
-        const float cq = silu_f32(fmaf(xq, wq.w, fmaf(hq[2], wq.z, fmaf(hq[1], wq.y, hq[0] * wq.x))));
-        const float ck = silu_f32(fmaf(xk, wk.w, fmaf(hk3[2], wk.z, fmaf(hk3[1], wk.y, hk3[0] * wk.x))));
-        const float cv = silu_f32(fmaf(xv, wv.w, fmaf(hv[2], wv.z, fmaf(hv[1], wv.y, hv[0] * wv.x))));
-        hq[0] = hq[1]; hq[1] = hq[2]; hq[2] = xq;
-        hk3[0] = hk3[1]; hk3[1] = hk3[2]; hk3[2] = xk;
-        hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
-        if (t + 1 == a.commit_at) {
-            float* ho = a.hist_out + size_t(n) * C * 3;
-            if (own_qk) {
+    float vt[TK];  // v conv outputs of column tid
+    const int cidx = (tid >> 5) * RBS + (tid & 31);
 #pragma unroll
-                for (int e = 0; e < 3; ++e) {
-                    ho[size_t(ch_q) * 3 + e] = hq[e];
-                    ho[size_t(ch_k) * 3 + e] = hk3[e];
+    for (int t = 0; t < TK; ++t) {
+        const bool on = t < ntok;
+        const float cq = silu_f32(fmaf(sq[t + 3], wq.w, fmaf(sq[t + 2], wq.z, fmaf(sq[t + 1], wq.y, sq[t] * wq.x))));
+        const float ck = silu_f32(fmaf(sk[t + 3], wk.w, fmaf(sk[t + 2], wk.z, fmaf(sk[t + 1], wk.y, sk[t] * wk.x))));
+        const float cv = silu_f32(fmaf(sv[t + 3], wv.w, fmaf(sv[t + 2], wv.z, fmaf(sv[t + 1], wv.y, sv[t] * wv.x))));
+        qc[t][cidx] = on ? cq : 0.f;
+        kc[t][cidx] = on ? ck : 0.f;
+        vt[t] = on ? cv : 0.f;
+    }
+    if (m > 0) {  // history after m tokens: elements m, m+1, m+2 of the sequence
+        float* ho = a.hist_out + size_t(n) * C * 3;
+#pragma unroll
+        for (int e = 0; e < 3; ++e) {
+            float hq = sq[e], hkv = sk[e], hv = sv[e];
+#pragma unroll
+            for (int r = 1; r <= TK; ++r)
+                if (r == m) { hq = sq[r + e]; hkv = sk[r + e]; hv = sv[r + e]; }
+            if (h < a.h_k) {  // the q/k history of key head hk is written by head h == hk
+                ho[size_t(ch_q) * 3 + e] = hq;
+                ho[size_t(ch_k) * 3 + e] = hkv;
+            }
+            ho[size_t(ch_v) * 3 + e] = hv;
+        }
+    }
+    // the gates: log gate and beta of token lane, gamma_t, and the decay from t to token m-1
+    if (warp == 0) {
+        float l = 0.f, be = 0.f;
+        if (lane < ntok) {
+            const size_t gi = (size_t(n) * ntok + lane) * a.h_v + h;
+            l = softplus_f32(a.alpha[gi] + a.dt[h]) * a.ssm_a[h];
+            be = sigmoid_f32(a.beta[gi]);
+        }
+        float pre = l, suf = __shfl_down_sync(kFullMask, lane < m ? l : 0.f, 1);  // suf: sum over t < r < m
+#pragma unroll
+        for (int o = 1; o < TK; o <<= 1) {
+            const float y = __shfl_up_sync(kFullMask, pre, o);
+            if (lane >= o) pre += y;
+            const float z = __shfl_down_sync(kFullMask, suf, o);
+            if (lane + o < 32) suf += z;
+        }
+        if (lane < TK) {
+            lg[lane] = l;
+            bet[lane] = be;
+            gam[lane] = expf(pre);
+            gtl[lane] = lane < m ? expf(suf) : 0.f;
+        }
+    }
+    __syncthreads();
+
+    // ---- the Gram entries, one thread per entry of the 8 x 8 blocks K K^T and Q K^T (four
+    // accumulators over the 128 channels); the thread of Q K^T's diagonal entry t also forms |q_t|^2
+    {
+        const int which = tid >> 6, t = (tid >> 3) & 7, s = tid & 7;
+        const float* x = which ? qc[t] : kc[t];
+        const float* y = kc[s];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), aq = acc;
+#pragma unroll 8
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const int off = (c4 >> 3) * RBS + 4 * (c4 & 7);
+            const float4 xv = *reinterpret_cast<const float4*>(x + off);
+            const float4 yv = *reinterpret_cast<const float4*>(y + off);
+            acc.x = fmaf(xv.x, yv.x, acc.x); acc.y = fmaf(xv.y, yv.y, acc.y);
+            acc.z = fmaf(xv.z, yv.z, acc.z); acc.w = fmaf(xv.w, yv.w, acc.w);
+            aq.x = fmaf(xv.x, xv.x, aq.x); aq.y = fmaf(xv.y, xv.y, aq.y);
+            aq.z = fmaf(xv.z, xv.z, aq.z); aq.w = fmaf(xv.w, xv.w, aq.w);
+        }
+        const float d = (acc.x + acc.y) + (acc.z + acc.w);
+        float seg = 0.f;  // log gates of tokens s+1 .. t
+        for (int r = s + 1; r <= t; ++r) seg += lg[r];
+        if (which == 0) {
+            if (s == t) kk2[t] = d;
+            else if (s < t) kkd[t][s] = expf(seg) * d;
+        } else if (s <= t) {
+            qkd[t][s] = expf(seg) * d;
+            if (s == t) qq2[t] = (aq.x + aq.y) + (aq.z + aq.w);
+        }
+    }
+
+    // ---- S0^T k_t and S0^T q_t of this warp's 32 columns, a token pair at a time
+    {
+        const float4* k4 = reinterpret_cast<const float4*>(&kc[0][0] + rb * RBS);
+        const float4* q4 = reinterpret_cast<const float4*>(&qc[0][0] + rb * RBS);
+        constexpr int TS = TSTR / 4;  // float4 stride between tokens
+#pragma unroll 1  // a rolled loop: the body is reused from the instruction cache
+        for (int tp = 0; tp < TK / 2; ++tp) {
+            if (2 * tp >= ntok) break;
+            float2 ak[2][4], aq[2][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ak[0][j] = ak[1][j] = aq[0][j] = aq[1][j] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int m4 = 0; m4 < NR / 4; ++m4) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float4 kk = k4[(2 * tp + u) * TS + m4];
+                    const float4 qq = q4[(2 * tp + u) * TS + m4];
+                    const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+                    const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ak[u][j] = __ffma2_rn(R[2 * m4][j], k01, ak[u][j]);
+                        ak[u][j] = __ffma2_rn(R[2 * m4 + 1][j], k23, ak[u][j]);
+                        aq[u][j] = __ffma2_rn(R[2 * m4][j], q01, aq[u][j]);
+                        aq[u][j] = __ffma2_rn(R[2 * m4 + 1][j], q23, aq[u][j]);
+                    }
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 3; ++e) ho[size_t(ch_v) * 3 + e] = hv[e];
-        }
-        xq = nq; xk = nk; xv = nv;
-        qraw[b][(tid >> 5) * RBS + (tid & 31)] = cq;
-        kraw[b][(tid >> 5) * RBS + (tid & 31)] = ck;
-        vraw[b][tid] = cv;
-        __syncthreads();
-
-        // everything below is warp-local: the warp owns 32 whole columns
-        const float gate = gates[t][0], beta = gates[t][1];
-        const float4* k4 = reinterpret_cast<const float4*>(kraw[b] + rb * RBS);
-        const float4* q4 = reinterpret_cast<const float4*>(qraw[b] + rb * RBS);
-
-        // kv = cs rk sum_i R_ij k_i: 32 rows in registers (as 16 row pairs), then the 4 row blocks
-        // by two shuffles; |k|^2 and |q|^2 (the L2 norms) ride along: each lane sums its row
-        // block's 32 squares and the same two shuffles add the 4 blocks
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        float2 nk2 = make_float2(0.f, 0.f), nq2 = make_float2(0.f, 0.f);
+            for (int u = 0; u < 2; ++u) {
+                float kv[4], qr[4];
 #pragma unroll
-        for (int m4 = 0; m4 < NR / 4; ++m4) {
-            const float4 kk = k4[m4];
-            const float4 qq = q4[m4];
-            const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
-            const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
-            nk2 = __ffma2_rn(k01, k01, __ffma2_rn(k23, k23, nk2));
-            nq2 = __ffma2_rn(q01, q01, __ffma2_rn(q23, q23, nq2));
+                for (int j = 0; j < 4; ++j) {
+                    kv[j] = ak[u][j].x + ak[u][j].y;
+                    qr[j] = aq[u][j].x + aq[u][j].y;
+                }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[j] = __ffma2_rn(R[2 * m4][j], k01, acc[j]);
-                acc[j] = __ffma2_rn(R[2 * m4 + 1][j], k23, acc[j]);
+                for (int o = 8; o < 32; o <<= 1)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        kv[j] += __shfl_xor_sync(kFullMask, kv[j], o);
+                        qr[j] += __shfl_xor_sync(kFullMask, qr[j], o);
+                    }
+                if (rb == 0) {
+                    *reinterpret_cast<float4*>(&kvp[2 * tp + u][col]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    *reinterpret_cast<float4*>(&qrp[2 * tp + u][col]) = make_float4(qr[0], qr[1], qr[2], qr[3]);
+                }
             }
         }
-        float kvs[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) kvs[j] = acc[j].x + acc[j].y;
-        float ksq = nk2.x + nk2.y, qsq = nq2.x + nq2.y;
-#pragma unroll
-        for (int o = 8; o < 32; o <<= 1) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) kvs[j] += __shfl_xor_sync(kFullMask, kvs[j], o);
-            ksq += __shfl_xor_sync(kFullMask, ksq, o);
-            qsq += __shfl_xor_sync(kFullMask, qsq, o);
-        }
-        const float rk = rsqrtf(ksq + a.eps);
-        const float rq = rsqrtf(qsq + a.eps);
-        const float4 vv = *reinterpret_cast<const float4*>(vraw[b] + col);
-        const float gk = gate * cs * rk;
-        float cn = gate * cs;
-        if (cn < kWinRenorm) {  // uniform over the CTA: fold cs' into R
-#pragma unroll
-            for (int p = 0; p < NR / 2; ++p)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) R[p][j] = __fmul2_rn(R[p][j], make_float2(cn, cn));
-            cn = 1.0f;
-        }
-        const float ek = beta * rk * __frcp_rn(cn);
-        const float vj[4] = {vv.x, vv.y, vv.z, vv.w};
-        float2 e2[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float e = (vj[j] - gk * kvs[j]) * ek;
-            e2[j] = make_float2(e, e);
-        }
-        cs = cn;
-
-        // rank-1 update and readout
-        float2 oacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int m4 = 0; m4 < NR / 4; ++m4) {
-            const float4 kk = k4[m4];
-            const float4 qq = q4[m4];
-            const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
-            const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                R[2 * m4][j] = __ffma2_rn(k01, e2[j], R[2 * m4][j]);
-                R[2 * m4 + 1][j] = __ffma2_rn(k23, e2[j], R[2 * m4 + 1][j]);
-                oacc[j] = __ffma2_rn(R[2 * m4][j], q01, oacc[j]);
-                oacc[j] = __ffma2_rn(R[2 * m4 + 1][j], q23, oacc[j]);
-            }
-        }
-        if (t + 1 == a.commit_at) {
-#pragma unroll
-            for (int p = 0; p < NR / 2; ++p) {
-                st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p) * row_stride),
-                          make_float4(cs * R[p][0].x, cs * R[p][1].x, cs * R[p][2].x, cs * R[p][3].x));
-                st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p + 1) * row_stride),
-                          make_float4(cs * R[p][0].y, cs * R[p][1].y, cs * R[p][2].y, cs * R[p][3].y));
-            }
-        }
-        float os[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) os[j] = oacc[j].x + oacc[j].y;
-#pragma unroll
-        for (int o = 8; o < 32; o <<= 1)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) os[j] += __shfl_xor_sync(kFullMask, os[j], o);
-        const float sc = cs * rq * 0.08838834764831845f;  // cs rq / sqrt(128)
-        const float4 ot = make_float4(os[0] * sc, os[1] * sc, os[2] * sc, os[3] * sc);
-        // lanes 0 .. 7 (row block 0) hold the warp's 32 outputs
-        float e = rb == 0 ? ot.x * ot.x + ot.y * ot.y + ot.z * ot.z + ot.w * ot.w : 0.f;
-        if (rb == 0) *reinterpret_cast<float4*>(&osm[t][col]) = ot;
-        e += __shfl_xor_sync(kFullMask, e, 1);
-        e += __shfl_xor_sync(kFullMask, e, 2);
-        e += __shfl_xor_sync(kFullMask, e, 4);
-        if (lane == 0) ssw[t][warp] = e;
     }
-    cp_async_wait_all();  // this thread's z and gamma (read only by this thread)
     __syncthreads();
-    if (tid < ntok) ss[tid] = (ssw[tid][0] + ssw[tid][1]) + (ssw[tid][2] + ssw[tid][3]);
+
+    // ---- the triangular solve and the outputs of column tid (held by this thread's own warp)
+    float ov[TK];
+    {
+        float w[TK];
+#pragma unroll
+        for (int t = 0; t < TK; ++t) {
+            const float rk = rsqrtf(kk2[t] + a.eps);
+            const float rq = rsqrtf(qq2[t] + a.eps) * 0.08838834764831845f;  // rq / sqrt(128)
+            const float g = gam[t];
+            float acc = g * kvp[t][tid];
+#pragma unroll
+            for (int s = 0; s < t; ++s) acc = fmaf(kkd[t][s], w[s], acc);
+            w[t] = t < ntok ? rk * (bet[t] * (vt[t] - rk * acc)) : 0.f;  // tokens past ntok: no S0^T k_t
+            float o = g * qrp[t][tid];
+#pragma unroll
+            for (int s = 0; s <= t; ++s) o = fmaf(qkd[t][s], w[s], o);
+            ov[t] = o * rq;
+            wsm[t][tid] = w[t];
+        }
+        // the sums of o^2 over this warp's 32 columns, per token
+#pragma unroll
+        for (int t = 0; t < TK; ++t) {
+            float e = ov[t] * ov[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(kFullMask, e, o);
+            if (lane == 0) ssw[t][warp] = e;
+        }
+    }
+    __syncwarp();
+
+    // ---- commit: S = gamma_{m-1} S0 + sum_{s<m} k_s (D_{m-1,s} w_s)^T, four tokens at a time
+    if (m > 0) {
+        const float gm = gam[m - 1];
+        const float2 g2 = make_float2(gm, gm);
+#pragma unroll
+        for (int p = 0; p < NR / 2; ++p)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) R[p][j] = __fmul2_rn(R[p][j], g2);
+        const float4* k4 = reinterpret_cast<const float4*>(&kc[0][0] + rb * RBS);
+        constexpr int TS = TSTR / 4;
+#pragma unroll 1
+        for (int hf = 0; hf < TK / 4; ++hf) {
+            if (4 * hf >= m) break;
+            float2 d2[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s = 4 * hf + u;
+                const float f = gtl[s];
+                const float4 ww = s < m ? *reinterpret_cast<const float4*>(&wsm[s][col]) : make_float4(0.f, 0.f, 0.f, 0.f);
+                d2[u][0] = make_float2(f * ww.x, f * ww.x);
+                d2[u][1] = make_float2(f * ww.y, f * ww.y);
+                d2[u][2] = make_float2(f * ww.z, f * ww.z);
+                d2[u][3] = make_float2(f * ww.w, f * ww.w);
+            }
+#pragma unroll
+            for (int m4 = 0; m4 < NR / 4; ++m4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 kk = k4[(4 * hf + u) * TS + m4];
+                    const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        R[2 * m4][j] = __ffma2_rn(k01, d2[u][j], R[2 * m4][j]);
+                        R[2 * m4 + 1][j] = __ffma2_rn(k23, d2[u][j], R[2 * m4 + 1][j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < NR / 2; ++p) {
+            st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p) * row_stride),
+                      make_float4(R[p][0].x, R[p][1].x, R[p][2].x, R[p][3].x));
+            st_stream(reinterpret_cast<float4*>(sbase + size_t(rb * NR + 2 * p + 1) * row_stride),
+                      make_float4(R[p][0].y, R[p][1].y, R[p][2].y, R[p][3].y));
+        }
+    }
+
+    cp_async_wait_all();  // this thread's z and gamma (read only by this thread)
     __syncthreads();
     // the gated RMSNorm over the head's 128 outputs of each token
 #pragma unroll
-    for (int i = 0; i < kWinMaxTok; ++i) {
+    for (int i = 0; i < TK; ++i) {
         if (i < ntok) {
-            const float rs = rsqrtf(ss[i] / float(D) + a.eps);
+            const float ss = (ssw[i][0] + ssw[i][1]) + (ssw[i][2] + ssw[i][3]);
+            const float rs = rsqrtf(ss / float(D) + a.eps);
             const size_t yi = ((size_t(n) * ntok + i) * a.h_v + h) * D + tid;
-            a.y[yi] = osm[i][tid] * rs * gs[tid] * sigmoid_f32(zs[i * D + tid]);
+            a.y[yi] = ov[i] * rs * gs[tid] * sigmoid_f32(zs[i * D + tid]);
         }
     }
 }
