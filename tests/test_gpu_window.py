@@ -128,3 +128,22 @@ def test_rejections_write_nothing():
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
     assert bool(torch.all(y == 3.0))
     assert np.array_equal(host(d["state"]), x["state"].astype(np.float64))
+
+
+@pytest.mark.parametrize("commit", [1, 0x105])
+def test_gate_extremes(commit):
+    # gates that saturate: alpha = +60 drives the decay to exp(-60 * |ssm_a|) = 0 (the state wiped at
+    # that token), alpha = -60 to exp(0) = 1 (no decay); beta_raw = -60 / +60 give beta = 0 / 1
+    N, h_k, h_v, ntok = 2, 2, 4, 8
+    x = gi.gdn_window_inputs(gi.rng(31), N, h_k, h_v, 128, ntok)
+    x["alpha"][:, 2, 0] = 60.0
+    x["alpha"][:, 5:7, 1] = 60.0
+    x["alpha"][:, :, 2] = -60.0
+    x["beta"][0, 3:6, :] = -60.0
+    x["beta"][1, :, 3] = 60.0
+    S, ho, y = _gpu(_dev(x), h_k, commit)
+    rS, rho, ry = _oracle(x, h_k, commit)
+    assert np.isfinite(ry).all() and np.isfinite(rS).all()
+    assert max_rel_err(host(y), ry) <= TOL
+    assert max_rel_err(host(S), rS) <= TOL
+    assert np.array_equal(host(ho), rho)
