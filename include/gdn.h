@@ -150,8 +150,9 @@ gdn_status comba_decode_step(const float* state, float* state_new, const void* q
 /*
  * comba_forward -- the Comba recurrence over T consecutive tokens of each of B sequences.
  * [comba spec] spec_md: the decode step is the comba-forward task's recurrence run for one token,
- * and running it T times reproduces that task.  Per (b, h) head and token t, exactly the
- * comba_decode_step arithmetic on the state carried from token t - 1:
+ * and running it T times reproduces that task.  Per (b, h) head and token t, the comba_decode_step
+ * function on the state carried from token t - 1 (evaluated 8 tokens at a time in the equivalent
+ * WY-regrouped form, so results match T single steps up to rounding order):
  *     S = exp(g_t) S;  u_j = beta_t (v_j - sum_i p_i S_ij);  S_ij += k_i u_j;
  *     o_t,j = sum_i (scale q_i) S_ij.
  *
@@ -313,7 +314,9 @@ gdn_status gdn_prefill_chunked_noalloc(const void* q, const void* k, const void*
  *     gate = exp(softplus(alpha + dt) ssm_a) (softplus threshold 20);  beta = sigmoid(beta_raw);
  *     kv_j = sum_i S[i][j] k_i;  delta_j = (v_j - gate kv_j) beta;  S[i][j] = gate S[i][j] + k_i delta_j;
  *     o_j = (sum_i S[i][j] q_i) / sqrt(128);  y_j = o_j rsqrt(mean(o^2) + eps) gamma_j sigmoid(z_j).
- * Value head h reads key head h % h_k.  Head dim is 128; C = (2 h_k + h_v) * 128 channels.
+ * Value head h reads key head h % h_k.  Head dim is 128; C = (2 h_k + h_v) * 128 channels.  The
+ * window is evaluated as one WY-regrouped chunk (the same function up to rounding order); a commit
+ * after token k gives bit for bit what a k-token window gives.
  *
  *   state     f32 [N, 128, h_v, 128]  (key row i, head h, value column j)  read; written in place
  *                                     only when committing
