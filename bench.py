@@ -232,15 +232,21 @@ def _cuda_ok():
 # ------------------------------------------------------------------------------------------------
 # GPU measurements
 # ------------------------------------------------------------------------------------------------
-def _timed(torch, dist, steps, fn):
+E2E_GRAPH = 8  # decode steps per captured graph of the end-to-end loop
+
+
+def _timed(torch, dist, steps, fn, finish=None):
     """Run fn(i) for i in range(steps) between barriers and synchronises; return seconds (max over
-    ranks) measured with CUDA events on the current stream."""
+    ranks) measured with CUDA events on the current stream.  finish() (if given) runs before the
+    end event, to join work that fn put on other streams into the current one."""
     dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for i in range(steps):
         fn(i)
+    if finish is not None:
+        finish()
     end.record()
     torch.cuda.synchronize()
     dist.barrier()
@@ -280,7 +286,9 @@ def bench_decode(torch, gdn, dist, steps, warmup, seed):
 
     # end to end through the public API: per step, the token inputs come from pinned host memory
     # (packed in one buffer, one copy) and y goes back to pinned host memory; the state stays
-    # resident in HBM (a serving cache)
+    # resident in HBM (a serving cache).  The two chains are two independent request batches served
+    # alternately: a chain's copies run on copy streams and overlap the other chain's kernel, and a
+    # chain's next inputs are sent only after its previous result has arrived on the host side.
     parts = [x.contiguous().view(torch.uint8).reshape(-1) for x in t]
     offs, total = [], 0
     for p_ in parts:
@@ -289,24 +297,74 @@ def bench_decode(torch, gdn, dist, steps, warmup, seed):
     host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
     for p_, o_ in zip(parts, offs):
         host_in[o_:o_ + p_.numel()].copy_(p_.cpu())
-    dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = [dev_in[o_:o_ + p_.numel()].view(x.dtype).view(x.shape)
-             for p_, o_, x in zip(parts, offs, t)]
-    host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    dev_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = [[dev_in[ch][o_:o_ + p_.numel()].view(x.dtype).view(x.shape)
+              for p_, o_, x in zip(parts, offs, t)] for ch in range(2)]
+    ys = [torch.empty_like(y) for _ in range(2)]
+    host_y = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in, ev_k, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
-    def e2e_step(i):
-        dev_in.copy_(host_in, non_blocking=True)
-        chain, parity = (i % 2) * 2, (i // 2) % 2
-        gdn.gdn_decode_step(states[chain + parity], *views, state_out=states[chain + 1 - parity],
-                            y=y)
-        host_y.copy_(y, non_blocking=True)
+    def e2e_step(i, base):
+        """Step i of a sequence of steps starting at step base, on the current stream."""
+        comp = torch.cuda.current_stream()
+        ch, parity = i % 2, (i // 2) % 2
+        if i == base:  # the copy streams follow the current stream from here on
+            s_in.wait_stream(comp)
+            s_out.wait_stream(comp)
+        if i - base >= 2:
+            s_in.wait_event(ev_out[ch])  # this chain's previous result is on the host
+            s_in.wait_event(ev_k[ch])    # and its previous kernel no longer reads dev_in[ch]
+        with torch.cuda.stream(s_in):
+            dev_in[ch].copy_(host_in, non_blocking=True)
+        ev_in[ch].record(s_in)
+        comp.wait_event(ev_in[ch])
+        gdn.gdn_decode_step(states[2 * ch + parity], *views[ch], state_out=states[2 * ch + 1 - parity],
+                            y=ys[ch])
+        ev_k[ch].record(comp)
+        s_out.wait_event(ev_k[ch])
+        with torch.cuda.stream(s_out):
+            host_y[ch].copy_(ys[ch], non_blocking=True)
+        ev_out[ch].record(s_out)
+
+    def e2e_finish():
+        comp = torch.cuda.current_stream()
+        comp.wait_event(ev_out[0])
+        comp.wait_event(ev_out[1])
 
     for i in range(warmup):
-        e2e_step(i)
-    e2e_secs = _timed(torch, dist, steps, e2e_step)
+        e2e_step(i, 0)
+    e2e_finish()
+    # a serving loop replays its decode steps from a CUDA graph: E2E_GRAPH steps (both chains, both
+    # state parities) are captured once -- the same API calls, copies and stream dependencies -- and
+    # replayed; steps past the last whole graph run eagerly.  Exactly `steps` steps are timed.
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph):
+            for i in range(E2E_GRAPH):
+                e2e_step(i, 0)
+            e2e_finish()
+        graph.replay()
+        torch.cuda.synchronize()
+        reps, rem = divmod(steps, E2E_GRAPH)
+    except RuntimeError as e:  # no graph: every step eagerly (noted in the JSON line)
+        print(f"e2e graph capture failed, eager steps: {e}", file=sys.stderr)
+        torch.cuda.synchronize()
+        graph, reps, rem = None, 0, steps
+
+    def e2e_call(j):
+        if j < reps:
+            graph.replay()
+        else:
+            for i in range(reps * E2E_GRAPH, steps):
+                e2e_step(i, reps * E2E_GRAPH)
+            e2e_finish()
+
+    e2e_secs = _timed(torch, dist, reps + (1 if rem else 0), e2e_call)
     h2d = sum(p_.numel() for p_ in parts)
-    d2h = host_y.numel() * host_y.element_size()
-    return dict(secs=secs, e2e_secs=e2e_secs, h2d=h2d, d2h=d2h,
+    d2h = host_y[0].numel() * host_y[0].element_size()
+    return dict(secs=secs, e2e_secs=e2e_secs, h2d=h2d, d2h=d2h, e2e_graph=graph is not None,
                 state_bytes=decode_state_bytes(B, Hk, Hv, Dk, Dv),
                 alg_bytes=decode_bytes(B, Hk, Hv, Dk, Dv), shape=(B, Hk, Hv, Dk, Dv))
 
@@ -782,7 +840,7 @@ def main():
                      "frac": achieved / hbm_peak, "note": peak_note,
                      "traffic": profiled_traffic("gdn_decode_kernel",
                                                  "gated_deltanet_delta_gb300/csrc/decode.cuh")},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
+        "e2e": {"value": e2e_value, "unit": "GB/s", "graph": dec["e2e_graph"], "h2d_bytes_per_step": dec["h2d"],
                 "d2h_bytes_per_step": dec["d2h"]},
         "gpu_launches": K,
         "clocks": clocks,
