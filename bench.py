@@ -253,6 +253,25 @@ def _timed(torch, dist, steps, fn, finish=None):
     return dist.max(start.elapsed_time(end) / 1e3)
 
 
+def _timed_calls(torch, dist, steps, fn, restore):
+    """Like _timed, but restore(i) runs before call i outside the timed region: each call is
+    bracketed by its own CUDA events on the current stream (restore's work is enqueued before the
+    start event, so the stream reaches the start event only once it is done), and the sum of the
+    calls' times is returned (max over ranks)."""
+    dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        restore(i)
+        evs[i][0].record()
+        fn(i)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return dist.max(sum(a.elapsed_time(b) for a, b in evs) / 1e3)
+
+
 def bench_decode(torch, gdn, dist, steps, warmup, seed):
     c = gi.GDN_DECODE_BATCHED
     B, Hk, Hv, Dk, Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
@@ -362,9 +381,12 @@ def bench_decode(torch, gdn, dist, steps, warmup, seed):
             e2e_finish()
 
     e2e_secs = _timed(torch, dist, reps + (1 if rem else 0), e2e_call)
+    # the same steps issued eagerly, one API call (and its copies and events) at a time from Python
+    e2e_eager_secs = _timed(torch, dist, steps, lambda i: e2e_step(i, 0), finish=e2e_finish)
     h2d = sum(p_.numel() for p_ in parts)
     d2h = host_y[0].numel() * host_y[0].element_size()
-    return dict(secs=secs, e2e_secs=e2e_secs, h2d=h2d, d2h=d2h, e2e_graph=graph is not None,
+    return dict(secs=secs, e2e_secs=e2e_secs, e2e_eager_secs=e2e_eager_secs, h2d=h2d, d2h=d2h,
+                e2e_graph=graph is not None,
                 state_bytes=decode_state_bytes(B, Hk, Hv, Dk, Dv),
                 alg_bytes=decode_bytes(B, Hk, Hv, Dk, Dv), shape=(B, Hk, Hv, Dk, Dv))
 
@@ -514,14 +536,20 @@ def bench_prefill(torch, gdn, dist, steps, warmup, seed, dtype="bf16"):
                      dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    pristine = d["state_pool"].clone()
+
     def step(i):
         gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
                                 d["state_pool"], d["cache_indices"], d["cu_seqlens"], C, out=out,
                                 workspace=ws, dev_status=status)
 
+    def restore(i):  # every call starts from the same pool (the call updates it in place)
+        d["state_pool"].copy_(pristine)
+
     for i in range(warmup):
+        restore(i)
         step(i)
-    secs = _timed(torch, dist, steps, step)
+    secs = _timed_calls(torch, dist, steps, step, restore)
     return dict(secs=secs, T=T, alg_bytes=prefill_bytes(c["seqlens"], Hk, Hv, K, V),
                 flops=prefill_flops(c["seqlens"], Hv, K, V, C))
 
@@ -554,43 +582,178 @@ def bench_window(torch, gdn, dist, steps, warmup, seed, commit):
 # ------------------------------------------------------------------------------------------------
 # CPU oracle timing (the baseline; also the reference arm)
 # ------------------------------------------------------------------------------------------------
-class OracleDecodeSample:
-    """The oracle's decode step on the batched workload's shapes, timed on a bounded sample of
-    batch rows, in parallel over rows (each row: Hv heads of Dv x Dk)."""
+class OracleSample:
+    """The oracle on a bounded sample of one operation's workload, timed on this host's cores.
 
-    def __init__(self, threads: int):
-        import oracle
-        oracle.build()
-        self.oracle = oracle
-        c = gi.GDN_DECODE_BATCHED
-        self.B, self.Hk, self.Hv, self.Dk, self.Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
-        g = gi.rng(0)
-        self.t = gi.gdn_decode_token(g, self.B, self.Hk, self.Hv, self.Dk, self.Dv)
-        self.S = (g.standard_normal((self.B, self.Hv, self.Dv, self.Dk)) * 0.1)
-        self.threads = threads
-        self.next_row = 0
+    The workload is cut into independent units (a batch row, a sequence, a (sequence, head) pair:
+    whatever the oracle takes in one call); ``unit(i)`` runs unit ``i`` and ``work`` is what one unit
+    contributes to the operation's metric (bytes or tokens).  ``run`` keeps ``threads`` units in
+    flight until ``seconds`` have passed (the oracle's C code runs outside the GIL); ``run_one``
+    times units on one thread.  The oracle is run as it stands, untuned."""
 
-    def _row(self, b):
-        sl = slice(b, b + 1)
-        t = self.t
-        self.oracle.gdn_decode(self.S[sl], t["q"][sl], t["k"][sl], t["v"][sl], t["g"][sl],
-                               t["beta"][sl], self.Dk ** -0.5)
+    def __init__(self, name, unit, n_units, work, unit_desc, scale_to_metric, metric_unit):
+        self.name, self.unit, self.n_units, self.work = name, unit, n_units, work
+        self.unit_desc, self.scale, self.metric_unit = unit_desc, scale_to_metric, metric_unit
+        self.next = 0
 
-    def run(self, seconds_target: float):
-        """Returns (state GB/s, cores, description, seconds)."""
-        rows = 0
+    def run(self, seconds: float, threads: int):
+        """Returns (value in the metric's unit, units run, seconds)."""
+        done = 0
         t0 = time.perf_counter()
-        with ThreadPoolExecutor(max_workers=self.threads) as ex:
-            while time.perf_counter() - t0 < seconds_target:
-                list(ex.map(self._row, [(self.next_row + i) % self.B for i in range(self.threads)]))
-                self.next_row += self.threads
-                rows += self.threads
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            while time.perf_counter() - t0 < seconds:
+                list(ex.map(self.unit, [(self.next + i) % self.n_units for i in range(threads)]))
+                self.next += threads
+                done += threads
         secs = time.perf_counter() - t0
-        state_bytes = rows * decode_state_bytes(1, self.Hk, self.Hv, self.Dk, self.Dv)
-        desc = (f"{rows} batch rows (each {self.Hv} heads of {self.Dv}x{self.Dk}) of the "
-                f"B={self.B} decode step, fp64 oracle, {self.threads} threads over rows, "
-                f"{secs:.2f} s")
-        return state_bytes / secs / 1e9, self.threads, desc, secs
+        return done * self.work * self.scale / secs, done, secs
+
+    def run_one(self, seconds: float):
+        done = 0
+        t0 = time.perf_counter()
+        while done == 0 or time.perf_counter() - t0 < seconds:
+            self.unit(self.next % self.n_units)
+            self.next += 1
+            done += 1
+        secs = time.perf_counter() - t0
+        return done * self.work * self.scale / secs, done, secs
+
+    def baseline(self, seconds: float, threads: int) -> dict:
+        """The cpu_baseline object of this operation: all threads, then one thread."""
+        value, n, secs = self.run(seconds, threads)
+        v1, n1, secs1 = self.run_one(max(1.0, seconds / 4))
+        return {"value": value, "unit": self.metric_unit, "cores": threads, "kind": "oracle",
+                "sample": f"{n} units ({self.unit_desc}), fp64 oracle, {threads} threads over units, "
+                          f"{secs:.2f} s",
+                "one_thread": {"value": v1, "unit": self.metric_unit,
+                               "sample": f"{n1} units on 1 thread, {secs1:.2f} s"}}
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def oracle_samples() -> dict:
+    """One OracleSample per measured operation, on reduced copies of the operations' workloads
+    (the same shapes per unit, the same distributions)."""
+    import oracle
+    oracle.build()
+    out = {}
+
+    # GDN decode step: unit = one batch row (Hv heads of Dv x Dk)
+    c = gi.GDN_DECODE_BATCHED
+    B, Hk, Hv, Dk, Dv = c["B"], c["Hk"], c["Hv"], c["Dk"], c["Dv"]
+    g = gi.rng(0)
+    t = {n: _f64(x) for n, x in gi.gdn_decode_token(g, B, Hk, Hv, Dk, Dv).items()}
+    S = _f64(g.standard_normal((B, Hv, Dv, Dk)) * 0.1)
+    rows = [dict(S=np.ascontiguousarray(S[b:b + 1]),
+                 **{n: np.ascontiguousarray(x[b:b + 1]) for n, x in t.items()}) for b in range(B)]
+
+    def dec_row(b):
+        r = rows[b]
+        oracle.gdn_decode(r["S"], r["q"], r["k"], r["v"], r["g"], r["beta"], Dk ** -0.5)
+
+    desc = f"batch rows of {Hv} heads of {Dv}x{Dk}"
+    out["decode"] = OracleSample("decode", dec_row, B, decode_state_bytes(1, Hk, Hv, Dk, Dv), desc,
+                                 1e-9, "GB/s")
+    out["decode_pooled"] = OracleSample("decode_pooled", dec_row, B,
+                                        decode_bytes(B, Hk, Hv, Dk, Dv) / B, desc, 1e-9, "GB/s")
+
+    # multi-token decode: unit = one batch row stepped through T = 8 tokens
+    T8 = 8
+    toks = [{n: _f64(x) for n, x in gi.gdn_decode_token(g, 8, Hk, Hv, Dk, Dv).items()}
+            for _ in range(T8)]
+
+    def multi_row(b):
+        St = rows[b]["S"]
+        r = b % 8
+        for tk in toks:
+            St, _ = oracle.gdn_decode(St, tk["q"][r:r + 1], tk["k"][r:r + 1], tk["v"][r:r + 1],
+                                      tk["g"][r:r + 1], tk["beta"][r:r + 1], Dk ** -0.5)
+
+    out["decode_multi"] = OracleSample("decode_multi", multi_row, B, T8,
+                                       f"batch rows of {Hv} heads stepped through {T8} tokens", 1.0,
+                                       "token-steps/s")
+
+    # Comba decode step: unit = one batch row (H heads of K x V)
+    cc = gi.COMBA_DECODE
+    H, K, V = cc["H"], cc["K"], cc["V"]
+    ct = {n: _f64(x) for n, x in gi.comba_decode_token(g, 8, H, K, V).items()}
+    CS = _f64(g.standard_normal((8, H, K, V)) * 0.1)
+
+    def comba_row(b):
+        sl = slice(b, b + 1)
+        oracle.comba_decode(CS[sl], ct["q"][sl], ct["k"][sl], ct["v"][sl], ct["p"][sl],
+                            ct["beta"][sl], ct["g_log"][sl], K ** -0.5)
+
+    out["comba_decode"] = OracleSample("comba_decode", comba_row, 8, comba_bytes(1, H, K, V),
+                                       f"batch rows of {H} heads of {K}x{V}", 1e-9, "GB/s")
+
+    # Comba forward: unit = one batch row, T tokens, H heads
+    cf = gi.COMBA_FORWARD
+    fx = {n: _f64(x) for n, x in gi.comba_forward_inputs(g, 8, cf["T"], H, K, V).items()}
+
+    def cfwd_row(b):
+        sl = slice(b, b + 1)
+        oracle.comba_forward(fx["state"][sl], fx["q"][sl], fx["k"][sl], fx["v"][sl], fx["p"][sl],
+                             fx["beta"][sl], fx["g_log"][sl], K ** -0.5)
+
+    out["comba_forward"] = OracleSample("comba_forward", cfwd_row, 8, H * cf["T"],
+                                        f"batch rows of {H} heads x {cf['T']} tokens", 1.0,
+                                        "head-token steps/s")
+
+    # chunked prefill: unit = (one 512-token sequence, one value head); tokens/s = token-heads / Hv
+    pc = gi.GDN_PREFILL
+    L = 512
+    px = gi.gdn_prefill_inputs(gi.rng(2), (L,), pc["Hk"], pc["Hv"], pc["K"], pc["V"], pc["pool"])
+    pq, pk, pv, pa, pb = (_f64(px[n]) for n in ("q", "k", "v", "a", "b"))
+    slot = int(px["cache_indices"][0])
+    pS = [_f64(px["state_pool"][slot, h]) for h in range(pc["Hv"])]
+
+    def prefill_unit(h):
+        oracle.gdn_prefill_unit(pq, pk, pv, pa, pb, float(px["A_log"][h]), float(px["dt_bias"][h]),
+                                pS[h], h, pc["K"] ** -0.5)
+
+    out["prefill_chunked"] = OracleSample(
+        "prefill_chunked", prefill_unit, pc["Hv"], L,
+        f"(sequence of {L} tokens, value head) pairs of the prefill's shapes", 1.0 / pc["Hv"],
+        "tokens/s")
+
+    # Comba chunked prefill: unit = (one 512-token sequence, one head), the oracle's Comba
+    # recurrence over the sequence
+    cx = gi.comba_prefill_inputs(gi.rng(5), (L,), pc["Hv"], K, V, pc["pool"])
+    cslot = int(cx["cache_indices"][0])
+    cheads = [dict(q=_f64(cx["q"][None, :, h:h + 1]), k=_f64(cx["k"][None, :, h:h + 1]),
+                   v=_f64(cx["v"][None, :, h:h + 1]), p=_f64(cx["p"][None, :, h:h + 1]),
+                   beta=_f64(cx["beta"][None, :, h:h + 1]), g=_f64(cx["g_log"][None, :, h:h + 1]),
+                   S=_f64(cx["state_pool"][cslot, h][None, None])) for h in range(pc["Hv"])]
+
+    def comba_prefill_unit(h):
+        u = cheads[h]
+        oracle.comba_forward(u["S"], u["q"], u["k"], u["v"], u["p"], u["beta"], u["g"], K ** -0.5)
+
+    out["comba_prefill_chunked"] = OracleSample(
+        "comba_prefill_chunked", comba_prefill_unit, pc["Hv"], L,
+        f"(sequence of {L} tokens, head) pairs of the Comba prefill's shapes", 1.0 / pc["Hv"],
+        "tokens/s")
+
+    # fused window: unit = one sequence (all value heads, ntok tokens)
+    wc = gi.GDN_WINDOW
+    wx = {n: _f64(x) for n, x in gi.gdn_window_inputs(gi.rng(3), 4, wc["h_k"], wc["h_v"], wc["D"],
+                                                         wc["ntok"]).items()}
+    for commit in (False, True):
+        def win_seq(n, code=1 if commit else 0):
+            sl = slice(n, n + 1)
+            oracle.gdn_window(wx["state"][sl], wx["hist"][sl], wx["qkv"][sl], wx["alpha"][sl],
+                              wx["beta"][sl], wx["z"][sl], wx["conv_w"], wx["dt"], wx["ssm_a"],
+                              wx["gamma"], wc["h_k"], code)
+
+        name = "window_commit" if commit else "window_verify"
+        out[name] = OracleSample(
+            name, win_seq, 4, window_bytes(1, wc["h_k"], wc["h_v"], wc["D"], wc["ntok"], commit),
+            f"sequences of {wc['h_v']} value heads x {wc['ntok']} tokens", 1e-9, "GB/s")
+    out["prefill_chunked_f16"] = out["prefill_chunked"]  # the oracle widens either input type
+    return out
 
 
 def bench_comba_prefill(torch, gdn, dist, steps, warmup, seed):
@@ -610,13 +773,19 @@ def bench_comba_prefill(torch, gdn, dist, steps, warmup, seed):
                      dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    pristine = d["state_pool"].clone()
+
     def step(i):
         gdn.comba_prefill_chunked(d["q"], d["k"], d["v"], d["p"], d["beta"], d["g_log"], d["state_pool"],
                                   d["cache_indices"], d["cu_seqlens"], C, out=out, workspace=ws, dev_status=status)
 
+    def restore(i):  # every call starts from the same pool (the call updates it in place)
+        d["state_pool"].copy_(pristine)
+
     for i in range(warmup):
+        restore(i)
         step(i)
-    secs = _timed(torch, dist, steps, step)
+    secs = _timed_calls(torch, dist, steps, step, restore)
     return dict(secs=secs, T=T, alg_bytes=comba_prefill_bytes(c["seqlens"], H, K, V),
                 flops=prefill_flops(c["seqlens"], H, K, V, C))
 
@@ -823,8 +992,14 @@ def main():
 
     cpu = None
     if dist.rank == 0 and N == 1:
-        gbs, cores, desc, _ = OracleDecodeSample(os.cpu_count() or 1).run(args.cpu_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+        # the oracle beside every GPU number: the headline on args.cpu_seconds of CPU work, every
+        # other operation on a quarter of that (plus a one-thread run each)
+        threads = os.cpu_count() or 1
+        samples = oracle_samples()
+        cpu = samples["decode"].baseline(args.cpu_seconds, threads)
+        for op_name, entry in ops.items():
+            if op_name in samples and isinstance(entry, dict) and "value" in entry:
+                entry["cpu_baseline"] = samples[op_name].baseline(args.cpu_seconds / 4, threads)
 
     B, Hk, Hv, Dk, Dv = dec["shape"]
     line = {
@@ -841,7 +1016,12 @@ def main():
                      "traffic": profiled_traffic("gdn_decode_kernel",
                                                  "gated_deltanet_delta_gb300/csrc/decode.cuh")},
         "e2e": {"value": e2e_value, "unit": "GB/s", "graph": dec["e2e_graph"], "h2d_bytes_per_step": dec["h2d"],
-                "d2h_bytes_per_step": dec["d2h"]},
+                "d2h_bytes_per_step": dec["d2h"],
+                "eager_value": N * dec["state_bytes"] * K / dec["e2e_eager_secs"] / 1e9,
+                "note": "value: the steps' API calls, host copies and stream dependencies captured "
+                        "once in a CUDA graph and replayed (a device-side pipelined copy + kernel "
+                        "figure; the per-call host work runs only at capture); eager_value: every "
+                        "step issued from Python through the C ABI"},
         "gpu_launches": K,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -860,16 +1040,18 @@ def main_reference(args):
         return
     threads = os.cpu_count() or 1
     per_step = max(0.05, min(1.0, 60.0 / max(1, args.steps + args.warmup)))
-    sample = OracleDecodeSample(threads)
+    sample = oracle_samples()["decode"]
     for _ in range(args.warmup):
-        sample.run(per_step)
-    vals, secs = [], 0.0
-    desc = ""
+        sample.run(per_step, threads)
+    vals, secs, units = [], 0.0, 0
     for _ in range(args.steps):
-        v, cores, desc, s = sample.run(per_step)
+        v, n, s = sample.run(per_step, threads)
         vals.append(v)
         secs += s
+        units += n
     value = statistics.median(vals)
+    desc = (f"{units} {sample.unit_desc} over {args.steps} steps of {per_step:.2f} s, fp64 oracle, "
+            f"{threads} threads over units")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
