@@ -21,12 +21,13 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT 
 GDN_BF16, GDN_F32 = 0, 1
 STATUS_BAD_CACHE_INDEX = 1
 STATUS_BAD_SEQLENS = 2
+STATUS_TIMEOUT = 4
 
 # Every symbol that include/gdn.h declares.
 ABI_SYMBOLS = ("gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_pooled", "comba_decode_step", "comba_forward",
                "gdn_prefill_workspace_size",
                "gdn_prefill_chunked", "gdn_prefill_chunked_f16", "gdn_prefill_chunked_noalloc",
-               "comba_prefill_chunked", "gdn_window_fused",
+               "comba_prefill_chunked", "gdn_window_fused", "gdn_prefill_set_wait_limit",
                "gdn_status_string", "gdn_last_error")
 
 
@@ -79,12 +80,20 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_chunked_noalloc.restype = I
         lib.gdn_window_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, U, F, P]
         lib.gdn_window_fused.restype = I
+        lib.gdn_prefill_set_wait_limit.argtypes = [ctypes.c_uint32]
+        lib.gdn_prefill_set_wait_limit.restype = None
         lib.gdn_status_string.argtypes = [I]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         _lib = lib
         return lib
+
+
+def set_prefill_wait_limit(polls: int) -> None:
+    """Bound every device-side wait of the prefill kernels to `polls` mbarrier polls (0: the
+    built-in limits).  A wait that runs out sets STATUS_TIMEOUT in the call's dev_status."""
+    load().gdn_prefill_set_wait_limit(int(polls))
 
 
 def last_error() -> str:

@@ -327,6 +327,17 @@ struct CombaIn {
     const void* beta;
     const float* g;
 };
+namespace {
+// The prefill kernels' wait limit (gdn_prefill_set_wait_limit): 0 means the built-in limits.
+std::atomic<uint32_t> g_prefill_wait_polls{0};
+constexpr uint32_t kPrefillBusyPolls = 1u << 26;   // seconds of busy polling
+constexpr uint32_t kPrefillSleepPolls = 1u << 22;  // polls with a 1 us suspend hint: seconds
+}  // namespace
+
+extern "C" void gdn_prefill_set_wait_limit(uint32_t polls) {
+    g_prefill_wait_polls.store(polls, std::memory_order_relaxed);
+}
+
 static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const void* k, const void* v,
                                 const void* a, const void* b, const float* A_log, const float* dt_bias,
                                 float* state_pool, int pool_size, const int64_t* cache_indices,
@@ -394,6 +405,9 @@ static gdn_status prefill_entry(const char* fn, bool f16, const void* q, const v
     p.Hv = Hv;
     p.scale = scale;
     p.eps = 1e-6f;
+    const uint32_t polls = g_prefill_wait_polls.load(std::memory_order_relaxed);
+    p.wait_polls = polls ? polls : kPrefillBusyPolls;
+    p.sleep_polls = polls ? polls : kPrefillSleepPolls;
     const cudaError_t e =
         gdn::launch_prefill(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), f16, cb != nullptr);
     if (e != cudaSuccess)

@@ -137,6 +137,11 @@ struct PrefillArgs {
     int max_splits;        // 0: no sequence is split
     int nsm;               // multiprocessors of the device (the split rule's measure of width)
     float scale, eps;
+    // polls of each device-side wait of the preparation and sequential kernels before it gives up
+    // (sets GDN_STATUS_TIMEOUT and stops the CTA); the waits that drain copies and products still
+    // in flight after such a give-up keep their own fixed limits
+    uint32_t wait_polls;   // busy polls (control and producer lanes, the preparation kernel)
+    uint32_t sleep_polls;  // polls with a 1 us suspend hint (worker warps)
 };
 
 // A prefill chunk record: everything a chunk contributes that does not depend on the state, laid

@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
     do {
         // ---- 1. wait for the rows, zero the rows past the sequence end, row norms
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, 0, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&bar_kq, 0, a.wait_polls);
             if (!__syncthreads_and(ok ? 1 : 0)) {  // give the copies one more bounded wait
                 if (tid == 0) tc::mbar_wait(&bar_kq, 0, kWaitLimit);
                 timed_out = true;
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             if (t == 0) vec[V_GL] = __expf(Gf[jg][L - 1]);
         }
         {
-            const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, kWaitLimit);
+            const bool ok = tid != 0 || tc::mbar_wait(&mbar, 0, a.wait_polls);
             if (!__syncthreads_and(ok ? 1 : 0)) {
                 if (tid == 0) tc::mbar_wait(&mbar, 0, kWaitLimit);
                 timed_out = true;
@@ -983,13 +983,13 @@ __global__ void __launch_bounds__(pf::NTS, 1)
     // control: a bounded wait on phase `parity` of barrier i; on a timeout it raises the abort flag,
     // and it gives up once someone else has
     auto wait_bar = [&](int i, uint32_t parity) -> bool {
-        if (tc::mbar_wait_or_abort(&bars[i], parity, kWaitLimit, &abort_flag)) return true;
+        if (tc::mbar_wait_or_abort(&bars[i], parity, a.wait_polls, &abort_flag)) return true;
         abort_flag = 1;
         return false;
     };
     // workers: the whole warp waits, converged, parked between polls
     auto warp_wait = [&](int i, uint32_t parity) -> bool {
-        bool ok = tc::mbar_sleep_wait(&bars[i], parity, kSleepWaitLimit, 1000u, &abort_flag);
+        bool ok = tc::mbar_sleep_wait(&bars[i], parity, a.sleep_polls, 1000u, &abort_flag);
         ok = __all_sync(kFullMask, ok ? 1 : 0) != 0;
         if (!ok && lane == 0) abort_flag = 1;
         tc::fence_after();
@@ -1737,9 +1737,22 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
             tc::mbar_expect_tx(&bars[O_FULL + s], 32768);
             tc::bulk_load(sb + FX_O + 32768u * s, src, 32768, &bars[O_FULL + s]);
         };
+        // barriers with a copy or a product of this lane in flight, and the parity of the last
+        // phase issued on each (for the bounded drain after a give-up)
+        uint32_t inflight = 0, lastpar = 0;
+        auto mark = [&](int i, uint32_t parity) {
+            inflight |= 1u << i;
+            lastpar = (lastpar & ~(1u << i)) | (parity << i);
+        };
         if (lane == 0) {
-            for (int i = 0; i < n && i < FX_RING; ++i) fetch_f(i);
-            for (int i = 0; i < n && i < 2; ++i) fetch_o(i);
+            for (int i = 0; i < n && i < FX_RING; ++i) {
+                fetch_f(i);
+                mark(F_FULL + i % FX_RING, (i / FX_RING) & 1);
+            }
+            for (int i = 0; i < n && i < 2; ++i) {
+                fetch_o(i);
+                mark(O_FULL + (i & 1), (i >> 1) & 1);
+            }
         }
         __syncwarp();
         tc::fence_before();
@@ -1751,25 +1764,26 @@ __global__ void __launch_bounds__(pf::FX_NT, 1) gdn_prefill_fixup_kernel(const _
                 if (i >= 2 && !ctl_wait(D_FREE + b, ((i - 2) >> 1) & 1)) break;
                 tc::fence_after();
                 products(b, s, false);
+                mark(MMA_DONE + b, (i >> 1) & 1);
                 if (i >= 1) {
                     // the F buffer of chunk i - 1 once its products are done, and the O' buffer of
                     // chunk i - 1 once the output warps have read it
                     if (i - 1 + FX_RING < n) {
                         if (!ctl_wait(MMA_DONE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
                         fetch_f(i - 1 + FX_RING);
+                        mark(F_FULL + (i - 1 + FX_RING) % FX_RING, ((i - 1 + FX_RING) / FX_RING) & 1);
                     }
                     if (i + 1 < n) {
                         if (!ctl_wait(O_FREE + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
                         fetch_o(i + 1);
+                        mark(O_FULL + ((i + 1) & 1), ((i + 1) >> 1) & 1);
                     }
                 }
             }
-            if (abort_flag) {  // one more bounded wait on every copy and product that may be in flight
-                for (int s = 0; s < FX_RING; ++s) tc::mbar_wait(&bars[F_FULL + s], 0, 1u << 20);
-                for (int b = 0; b < 2; ++b) {
-                    tc::mbar_wait(&bars[MMA_DONE + b], 0, 1u << 20);
-                    tc::mbar_wait(&bars[O_FULL + b], 0, 1u << 20);
-                }
+            if (abort_flag) {  // one more bounded wait on the last phase of every barrier with a copy
+                               // or a product in flight
+                for (int i = 0; i < FX_NBAR; ++i)
+                    if (inflight & (1u << i)) tc::mbar_wait(&bars[i], (lastpar >> i) & 1u, 1u << 20);
             }
         }
         __syncwarp();

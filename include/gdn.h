@@ -339,6 +339,20 @@ gdn_status gdn_window_fused(float* state, const float* hist, float* hist_out, co
                             const float* gamma, float* y, int N, int h_k, int h_v, int ntok,
                             unsigned commit, float eps, gdn_stream_t stream);
 
+/*
+ * gdn_prefill_set_wait_limit -- bound every device-side wait of the prefill kernels
+ * (gdn_prefill_chunked, _f16, _noalloc and comba_prefill_chunked: the chunk preparation and the
+ * chunk recurrence) to `polls` polls of its mbarrier instead of the built-in limits (seconds of
+ * waiting).  No page has a counterpart: this is the knob of the failure path.  A wait that runs out
+ * sets GDN_STATUS_TIMEOUT in the call's dev_status and its CTA stops after one more bounded wait
+ * for the copies and products it has in flight, so the call returns with that status and partial
+ * results (the state of a CTA that gave up is not written back; outputs may be partly written) and
+ * the device stays usable.  A limit small enough to run out on a healthy GPU (say 1) is for tests
+ * of that path; a caller may also use a tighter limit than the default as a watchdog.  0 restores
+ * the built-in limits.  Process-wide; it applies to calls launched after it returns.
+ */
+void gdn_prefill_set_wait_limit(uint32_t polls);
+
 /* Static description of a status code. */
 const char* gdn_status_string(gdn_status status);
 
