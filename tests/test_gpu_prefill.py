@@ -109,6 +109,40 @@ def test_full_workload_sampled_units():
             assert np.array_equal(pool[s], x["state_pool"][s].astype(np.float64))
 
 
+def test_full_workload_mild_gates_every_head_of_the_split_sequence():
+    # the benchmark's lengths (4096 + 2048 + 1024 + 8192) and heads with slow decay, so that the
+    # state carried across chunks -- and across the split of the 8192-token sequence into two
+    # halves that the fix-up recombines -- matters: all 32 heads of that sequence, and a sample of
+    # the others, against the oracle (run over the heads in parallel)
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    c = gi.GDN_PREFILL
+    x = gi.gdn_prefill_inputs(gi.rng(9), c["seqlens"], c["Hk"], c["Hv"], c["K"], c["V"], c["pool"],
+                              mild_gates=True)
+    d = _to_dev(x)
+    scale = 128 ** -0.5
+    out, st = _gpu(d, scale)
+    assert st == 0
+    o, pool = host(out), host(d["state_pool"])
+    cu, ci = x["cu_seqlens"], x["cache_indices"]
+    seq = {n: {k: np.ascontiguousarray(x[k][cu[n]:cu[n + 1]], dtype=np.float64)
+               for k in ("q", "k", "v", "a", "b")} for n in range(len(c["seqlens"]))}
+    units = [(3, h) for h in range(c["Hv"])] + [(0, 0), (1, 17), (2, 31)]
+
+    def ref(unit):
+        n, h = unit
+        z = seq[n]
+        return oracle.gdn_prefill_unit(z["q"], z["k"], z["v"], z["a"], z["b"], x["A_log"][h],
+                                       x["dt_bias"][h], x["state_pool"][ci[n], h], h, scale)
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        refs = list(ex.map(ref, units))
+    for (n, h), (S, o_ref) in zip(units, refs):
+        sl = slice(cu[n], cu[n + 1])
+        assert max_rel_err(o[sl, h], o_ref) <= OUT_TOL, (n, h)
+        assert max_rel_err(pool[ci[n], h], S) <= STATE_TOL, (n, h)
+
+
 @pytest.mark.parametrize("Hk,Hv", [(3, 3), (1, 4)])
 def test_key_head_sharing_ratios(Hk, Hv):
     # Hv / Hk = 1 (no sharing) and 4, over several chunks and a short tail

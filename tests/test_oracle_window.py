@@ -175,3 +175,27 @@ def test_bad_commit_codes_are_rejected():
     for bad in (2, 0x100, 0x104, 0x200 | 1):
         with pytest.raises(ValueError):
             _run(x, 1, bad)
+
+
+def test_silu_and_the_l2_norm_eps_against_hand_values():
+    # Two channels per head (D = 2), identity taps, a zero state and beta_raw = 0 (beta = 1/2): one
+    # committed token leaves S[i][j] = k^_i * beta * v_j with v = SiLU(x_v) and k^ = k / sqrt(|k|^2
+    # + eps), k = SiLU(x_k).  The values are worked out by hand, not by the oracle's formulas:
+    #   SiLU(1) = sigma(1) = 0.7310585786300049,  SiLU(-2) = -2 sigma(-2) = -0.2384058440442351,
+    #   SiLU(-30) = -30 / (1 + e^30) = -30 * 9.357622968840175e-14.
+    # x_k = -30 makes |k|^2 ~ 1.6e-23, far below eps = 1e-6, so k^ = k / sqrt(eps) = 1000 k: a norm
+    # without eps (unit k^) or with eps / 128 (k^ larger by sqrt(128)) misses by orders of magnitude.
+    D = 2
+    x = _inputs(6, D=D)
+    x["state"][:] = 0.0
+    x["beta"][:] = 0.0
+    w = np.zeros((3 * D, 4), np.float32)
+    w[:, 3] = 1.0
+    x["qkv"][0, 0] = np.array([0.5, 0.25, -30.0, -30.0, 1.0, -2.0], np.float32)
+    S, _, _ = _run(x, 1, 1, conv_w=w)
+    v = np.array([0.7310585786300049, -0.2384058440442351])
+    k = -30.0 * 9.357622968840175e-14
+    k_hat = k / np.sqrt(2 * k * k + 1e-6)
+    assert abs(k_hat / (1000.0 * k) - 1.0) < 1e-15
+    want = np.array([[k_hat * 0.5 * v[0], k_hat * 0.5 * v[1]]] * 2)  # rows i (key), columns j
+    np.testing.assert_allclose(S[0, :, 0, :], want, rtol=1e-12, atol=0)

@@ -2,11 +2,14 @@
 device memory belongs to another allocator, or allocation is not allowed where they run).  It uses
 the library's fixed 64 MiB device scratch instead of a caller-owned workspace.
 
-The GPU test runs two calls in a row through the C ABI, the second with a different batch so that
-whatever the first left in the shared scratch would show if it were read, and compares outputs and
-final states with gdn_prefill_chunked's on the same inputs, within the prefill parity tolerances.
-This file is named to be collected last: it needs nothing from the other tests and passes alone in a
-fresh process as well as after them.
+The GPU tests run calls in a row through the C ABI, each with a different batch so that whatever an
+earlier call left in the shared scratch would show if it were read.  Every call is checked against
+the oracle (per sequence, the prefill tolerances) and against gdn_prefill_chunked given a workspace
+of exactly 64 MiB: with the same workspace size both take the same split decision and run the same
+kernels, so their outputs and pools must agree bit for bit.  One batch has a long sequence that is
+split inside the 64 MiB; another is too large for the split scratch but not for the records, so it
+runs unsplit.  This file is named to be collected last: it needs nothing from the other tests and
+passes alone in a fresh process as well as after them.
 """
 import ctypes
 
@@ -16,10 +19,12 @@ import torch
 
 import gdn_inputs as gi
 import gated_deltanet_delta_gb300 as gdn
+import oracle
 from parity import max_rel_err
 
 OUT_TOL, STATE_TOL = 5e-3, 2e-3
 SCRATCH = 64 << 20
+SCALE = 128 ** -0.5
 
 
 def _dev(x):
@@ -33,30 +38,76 @@ def _dev(x):
 def _run(fn, d, pool, **kw):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = fn(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], pool,
-             d["cache_indices"], d["cu_seqlens"], 64, dev_status=status, **kw)
+             d["cache_indices"], d["cu_seqlens"], 64, scale=SCALE, dev_status=status, **kw)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    return out.float().cpu().numpy()
+    return out
+
+
+def _check_oracle(x, pool_before, out, pool_after):
+    """Per sequence: outputs and the final state against the oracle run from pool_before; slots no
+    sequence references unchanged bit for bit."""
+    pool_ref, out_ref, st = oracle.gdn_prefill(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"],
+                                               x["dt_bias"], pool_before, x["cache_indices"],
+                                               x["cu_seqlens"], SCALE)
+    assert st == 0
+    o = out.float().cpu().numpy().astype(np.float64)
+    pool = pool_after.cpu().numpy().astype(np.float64)
+    cu, ci = x["cu_seqlens"], [int(c) for c in x["cache_indices"]]
+    for n, slot in enumerate(ci):
+        if cu[n + 1] > cu[n]:
+            assert max_rel_err(o[cu[n]:cu[n + 1]], out_ref[cu[n]:cu[n + 1]]) <= OUT_TOL, n
+            assert max_rel_err(pool[slot], pool_ref[slot]) <= STATE_TOL, n
+    for s in range(pool.shape[0]):
+        if s not in ci:
+            assert np.array_equal(pool[s], pool_before[s].astype(np.float64)), s
+
+
+def _both(x, pool_na, pool_ws):
+    """One call of each entry point on the same inputs and equal pools; returns the no-alloc
+    output after checking it against the oracle and, bit for bit, against the 64 MiB workspace."""
+    d = _dev(x)
+    before = pool_na.cpu().numpy()
+    assert torch.equal(pool_na, pool_ws)
+    ws = torch.empty(SCRATCH, dtype=torch.uint8, device="cuda")
+    ref = _run(gdn.gdn_prefill_chunked, d, pool_ws, workspace=ws)
+    got = _run(gdn.gdn_prefill_chunked_noalloc, d, pool_na)
+    _check_oracle(x, before, got, pool_na)
+    assert torch.equal(got, ref)
+    assert torch.equal(pool_na, pool_ws)
+    return got
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
+def test_noalloc_on_calls_in_a_row_matches_the_oracle_and_the_workspace_entry_point():
     gdn.load()
     Hk, Hv, pool_size = 2, 4, 6
     g = gi.rng(2024)
-    x1 = gi.gdn_prefill_inputs(g, [300, 64, 1000, 17], Hk, Hv, 128, 128, pool=pool_size)
+    # call 1: the 1000-token sequence (16 chunks) dominates and is split; its whole workspace,
+    # split scratch included, fits the 64 MiB
+    x1 = gi.gdn_prefill_inputs(g, [300, 64, 1000, 17], Hk, Hv, 128, 128, pool=pool_size, mild_gates=True)
+    # call 2 continues slots 1 and 3 with another batch
     x2 = gi.gdn_prefill_inputs(g, [17, 1000, 130], Hk, Hv, 128, 128, pool=pool_size)
-    x2["cache_indices"] = np.array([4, 1, 3], dtype=np.int64)  # the second call continues slots 1 and 3
+    x2["cache_indices"] = np.array([4, 1, 3], dtype=np.int64)
     assert gdn.gdn_prefill_workspace_size(4, x1["T"], Hk, Hv, 128, 128, 64) <= SCRATCH
     assert gdn.gdn_prefill_workspace_size(3, x2["T"], Hk, Hv, 128, 128, 64) <= SCRATCH
-    pool_ref = torch.from_numpy(x1["state_pool"]).float().cuda()
-    pool_na = pool_ref.clone()
-    d1, d2 = _dev(x1), _dev(x2)
-    for d in (d1, d2):
-        ref = _run(gdn.gdn_prefill_chunked, d, pool_ref)
-        got = _run(gdn.gdn_prefill_chunked_noalloc, d, pool_na)
-        assert max_rel_err(got, ref) <= OUT_TOL
-        assert max_rel_err(pool_na.cpu().numpy(), pool_ref.cpu().numpy()) <= STATE_TOL
+    pool_na = torch.from_numpy(x1["state_pool"]).float().cuda()
+    pool_ws = pool_na.clone()
+    for x in (x1, x2):
+        _both(x, pool_na, pool_ws)
+
+
+@pytest.mark.gpu
+def test_noalloc_runs_unsplit_when_only_the_records_fit():
+    gdn.load()
+    # one 2944-token sequence with Hv = 16: its records fit the 64 MiB, its split scratch does not
+    Hk, Hv = 8, 16
+    x = gi.gdn_prefill_inputs(gi.rng(77), [2944], Hk, Hv, 128, 128, pool=2, mild_gates=True)
+    lay_full = gdn.gdn_prefill_workspace_size(1, x["T"], Hk, Hv, 128, 128, 64)
+    assert lay_full > SCRATCH
+    pool_na = torch.from_numpy(x["state_pool"]).float().cuda()
+    pool_ws = pool_na.clone()
+    _both(x, pool_na, pool_ws)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
