@@ -293,7 +293,10 @@ gdn_status comba_prefill_chunked(const void* q, const void* k, const void* v, co
  *     T = 3,000 tokens over a few sequences with Hv = 16.  Long sequences are split only when the
  *     whole gdn_prefill_workspace_size(...) fits.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
- *     that device current) and keeps it; make that first call before any stream capture.
+ *     that device current) and keeps it; make that first call before any stream capture.  The
+ *     address kept is the one in the device's primary context (the CUDA runtime's default), so
+ *     every call must run in that context: a caller that makes its own driver-API context on the
+ *     same device current (cuCtxCreate, cuCtxPushCurrent) must not use this entry point.
  *   - Every call on a device shares the one array.  Nothing in it has to start at zero: each call
  *     writes everything it reads.  Calls whose kernels overlap on the GPU (different streams, no
  *     ordering between them) race on the array and give undefined results; order them on one stream.

@@ -1,8 +1,10 @@
 """Comparators used by the parity tests.
 
 max_rel_err is the tolerance metric: max |x - ref| / max |ref| over a whole tensor (an elementwise
-relative error is ill-posed where the reference crosses zero).  rel_frobenius is the metric of the
-KBench Comba spec (correctness_md): |x - ref|_F / |ref|_F.
+relative error is ill-posed where the reference crosses zero).  max_rel_err_slices applies the same
+metric to every slice along the leading axes (per head, per sequence and head) and returns the
+worst, so that a head whose outputs are small beside the tensor's largest cannot hide its error.
+rel_frobenius is the metric of the KBench Comba spec (correctness_md): |x - ref|_F / |ref|_F.
 """
 import numpy as np
 
@@ -18,6 +20,17 @@ def max_rel_err(x, ref) -> float:
     if den == 0.0:
         return num
     return num / den
+
+
+def max_rel_err_slices(x, ref, lead: int) -> float:
+    """The worst max_rel_err over the slices x[i0, .., i_{lead-1}] (the first `lead` axes index the
+    slices, the rest is compared as one tensor)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    n = int(np.prod(x.shape[:lead])) if lead else 1
+    xs, rs = x.reshape(n, -1), ref.reshape(n, -1)
+    return max((max_rel_err(xs[i], rs[i]) for i in range(n)), default=0.0)
 
 
 def rel_frobenius(x, ref) -> float:

@@ -11,7 +11,7 @@ import gdn_inputs as gi
 import gated_deltanet_delta_gb300 as gdn
 import oracle
 from gpu_util import dev, host, library, sample_heads
-from parity import bf16_neighbours_ok, max_rel_err
+from parity import bf16_neighbours_ok, max_rel_err, max_rel_err_slices
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -52,6 +52,8 @@ def test_tiny_workload_warmed_by_oracle():
     S1, y32 = _gpu_step(Sd, t, scale)
     assert max_rel_err(host(S1), ref_S) <= TOL
     assert max_rel_err(host(y32), ref_y) <= TOL
+    assert max_rel_err_slices(host(S1), ref_S, 2) <= TOL   # per (batch row, value head)
+    assert max_rel_err_slices(host(y32), ref_y, 2) <= TOL
     _, ybf = _gpu_step(Sd, t, scale, y_dtype=torch.bfloat16)
     assert bf16_neighbours_ok(host(ybf), ref_y)
     assert np.array_equal(host(Sd), S)   # functional: the input state is untouched

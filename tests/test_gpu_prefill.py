@@ -12,7 +12,7 @@ import gdn_inputs as gi
 import gated_deltanet_delta_gb300 as gdn
 import oracle
 from gpu_util import dev, host, library
-from parity import max_rel_err
+from parity import max_rel_err, max_rel_err_slices
 
 pytestmark = pytest.mark.gpu
 OUT_TOL, STATE_TOL = 5e-3, 2e-3
@@ -56,6 +56,11 @@ def _check_all(x, d, out, scale):
         if cu[n + 1] > cu[n]:
             assert max_rel_err(o[cu[n]:cu[n + 1]], out_ref[cu[n]:cu[n + 1]]) <= OUT_TOL, n
             assert max_rel_err(pool[slot], pool_ref[slot]) <= STATE_TOL, n
+            # and per value head of the sequence
+            o_h = np.moveaxis(o[cu[n]:cu[n + 1]], 1, 0)
+            r_h = np.moveaxis(out_ref[cu[n]:cu[n + 1]], 1, 0)
+            assert max_rel_err_slices(o_h, r_h, 1) <= OUT_TOL, n
+            assert max_rel_err_slices(pool[slot], pool_ref[slot], 1) <= STATE_TOL, n
         else:
             assert np.array_equal(pool[slot], x["state_pool"][slot].astype(np.float64))
     for s in range(pool.shape[0]):
