@@ -929,9 +929,9 @@ def main():
                          "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
                          "frac": roof / t1, "note": peak_note,
                          "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
-                         "traffic": profiled_traffic("gdn_prefill_call",
-                                                     "gated_deltanet_delta_gb300/csrc/prefill.cuh")
-                         if key == "prefill" else None}}
+                         "traffic": profiled_traffic({"prefill": "gdn_prefill_call",
+                                                      "comba_prefill": "comba_prefill_call"}.get(key, ""),
+                                                     "gated_deltanet_delta_gb300/csrc/prefill.cuh")}}
     for key in ("window_verify", "window_commit"):
         w = extra.get(key, {})
         if "secs" in w:
@@ -942,9 +942,9 @@ def main():
                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
                                      "unit": "GB/s", "frac": gbs / hbm_peak, "note": peak_note,
                                      "traffic": profiled_traffic(
-                                         "gdn_window_kernel",
-                                         "gated_deltanet_delta_gb300/csrc/window.cuh")
-                                     if key == "window_verify" else None}}
+                                         "gdn_window_kernel" if key == "window_verify"
+                                         else "gdn_window_kernel_commit",
+                                         "gated_deltanet_delta_gb300/csrc/window.cuh")}}
         elif key in extra:
             ops[key] = w
 
@@ -956,7 +956,9 @@ def main():
             "workload": f"gdn decode, {dm['T']} tokens per call, B64 Hk16 Hv32 D128",
             "value": N * dm["B"] * dm["T"] / t1, "unit": "token-steps/s", "us_per_call": t1 * 1e6,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+                         "frac": gbs / hbm_peak, "note": peak_note,
+                         "traffic": profiled_traffic("gdn_decode_multi_kernel",
+                                                     "gated_deltanet_delta_gb300/csrc/decode.cuh")}}
     dp = extra.get("decode_pooled", {})
     if "secs" in dp:
         t1 = dp["secs"] / K
@@ -965,7 +967,9 @@ def main():
             "workload": "gdn decode on a 128-slot pool, B64 Hk16 Hv32 D128", "value": N * gbs,
             "unit": "GB/s", "us_per_step": t1 * 1e6,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "note": peak_note, "traffic": None}}
+                         "frac": gbs / hbm_peak, "note": peak_note,
+                         "traffic": profiled_traffic("gdn_decode_kernel_pooled",
+                                                     "gated_deltanet_delta_gb300/csrc/decode.cuh")}}
     cf = extra.get("comba_forward", {})
     if "secs" in cf:
         t1 = cf["secs"] / max(3, K // 5)
