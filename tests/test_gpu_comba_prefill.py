@@ -12,7 +12,7 @@ import gdn_inputs as gi
 import gated_deltanet_delta_gb300 as gdn
 import oracle
 from gpu_util import dev, host, library
-from parity import max_rel_err
+from parity import max_rel_err, max_rel_err_slices
 
 pytestmark = pytest.mark.gpu
 OUT_TOL, STATE_TOL = 5e-3, 2e-3
@@ -59,6 +59,9 @@ def _check_all(x, d, out, scale):
                                         x["g_log"][None, sl], scale)
         assert max_rel_err(o[sl], o_ref[0]) <= OUT_TOL, n
         assert max_rel_err(pool[slot], S[0]) <= STATE_TOL, n
+        # and per head of the sequence
+        assert max_rel_err_slices(np.moveaxis(o[sl], 1, 0), np.moveaxis(o_ref[0], 1, 0), 1) <= OUT_TOL, n
+        assert max_rel_err_slices(pool[slot], S[0], 1) <= STATE_TOL, n
     for s in range(pool.shape[0]):
         if s not in ci:
             assert np.array_equal(pool[s], x["state_pool"][s].astype(np.float64)), s

@@ -12,7 +12,7 @@ import gdn_inputs as gi
 import gated_deltanet_delta_gb300 as gdn
 import oracle
 from gpu_util import dev, host, library
-from parity import max_rel_err
+from parity import max_rel_err, max_rel_err_slices
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -51,8 +51,11 @@ def test_full_workload(commit):
     S, ho, y = _gpu(d, c["h_k"], commit)
     rS, rho, ry = _oracle(x, c["h_k"], commit)
     assert max_rel_err(host(y), ry) <= TOL
+    # and per (sequence, value head): y [N, ntok, h_v, D], state [N, D, h_v, D]
+    assert max_rel_err_slices(np.moveaxis(host(y), 2, 1), np.moveaxis(ry, 2, 1), 2) <= TOL
     if commit:
         assert max_rel_err(host(S), rS) <= TOL
+        assert max_rel_err_slices(np.moveaxis(host(S), 2, 1), np.moveaxis(rS, 2, 1), 2) <= TOL
         assert np.array_equal(host(ho), rho)
     else:
         assert np.array_equal(host(S), x["state"].astype(np.float64))
