@@ -168,3 +168,12 @@ def test_comba_forward_validation(lib):
     assert call(out=ctypes.c_void_p((1 << 20) + 64)) == gdn.GDN_ERR_INVALID_ARG       # o overlaps state
     assert call(B=-1) == gdn.GDN_ERR_INVALID_ARG
     assert call(B=0, state=N, ptr=N, out=N) == gdn.GDN_OK                               # no heads: no-op
+
+
+def test_prefill_wait_limit_is_a_host_setting(lib):
+    # a process-wide host value read at launch: setting and restoring it needs no GPU
+    gdn.set_prefill_wait_limit(1)
+    gdn.set_prefill_wait_limit(1 << 30)
+    gdn.set_prefill_wait_limit(0)
+    lib.gdn_prefill_set_wait_limit(ctypes.c_uint32(0xFFFFFFFF))
+    lib.gdn_prefill_set_wait_limit(ctypes.c_uint32(0))
