@@ -109,13 +109,17 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def profiled_traffic(kernel: str, source: str):
+def profiled_traffic(kernel: str, source):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the kernel
-    source has changed since the counters were taken."""
+    source has changed since the counters were taken.  `source` is one file or a tuple of files
+    (the kernel and the launch code that picks its shape), hashed concatenated in that order."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
-        with open(os.path.join(ROOT, source), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for src in ((source,) if isinstance(source, str) else source):
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()[:16]
         with open(path) as f:
             for line in f:
                 parts = line.split()
@@ -958,7 +962,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "note": peak_note,
                          "traffic": profiled_traffic("gdn_decode_multi_kernel",
-                                                     "gated_deltanet_delta_gb300/csrc/decode.cuh")}}
+                                                     ("gated_deltanet_delta_gb300/csrc/decode.cuh",
+                                                      "gated_deltanet_delta_gb300/csrc/decode.cu"))}}
     dp = extra.get("decode_pooled", {})
     if "secs" in dp:
         t1 = dp["secs"] / K
@@ -969,7 +974,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "note": peak_note,
                          "traffic": profiled_traffic("gdn_decode_kernel_pooled",
-                                                     "gated_deltanet_delta_gb300/csrc/decode.cuh")}}
+                                                     ("gated_deltanet_delta_gb300/csrc/decode.cuh",
+                                                      "gated_deltanet_delta_gb300/csrc/decode.cu"))}}
     cf = extra.get("comba_forward", {})
     if "secs" in cf:
         t1 = cf["secs"] / max(3, K // 5)
@@ -1018,7 +1024,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "note": peak_note,
                      "traffic": profiled_traffic("gdn_decode_kernel",
-                                                 "gated_deltanet_delta_gb300/csrc/decode.cuh")},
+                                                 ("gated_deltanet_delta_gb300/csrc/decode.cuh",
+                                                  "gated_deltanet_delta_gb300/csrc/decode.cu"))},
         "e2e": {"value": e2e_value, "unit": "GB/s", "graph": dec["e2e_graph"], "h2d_bytes_per_step": dec["h2d"],
                 "d2h_bytes_per_step": dec["d2h"],
                 "eager_value": N * dec["state_bytes"] * K / dec["e2e_eager_secs"] / 1e9,
