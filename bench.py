@@ -934,6 +934,7 @@ def main():
                          "frac": roof / t1, "note": peak_note,
                          "roofline_us": roof * 1e6, "hbm_us": t_hbm * 1e6, "tensor_us": t_tc * 1e6,
                          "traffic": profiled_traffic({"prefill": "gdn_prefill_call",
+                                                      "prefill_f16": "gdn_prefill_f16_call",
                                                       "comba_prefill": "comba_prefill_call"}.get(key, ""),
                                                      "gated_deltanet_delta_gb300/csrc/prefill.cuh")}}
     for key in ("window_verify", "window_commit"):
