@@ -698,6 +698,23 @@ __global__ void __launch_bounds__(pf::PNT, 5)
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 const int s0 = 32 * hf + 16 * qq;
+                // this warp's rows are t = (row & 32) .. + 31 (of Lm or of M~): columns s0 .. s0 + 15
+                // all past them are zero in both (warps 4 and 6), so that block is only written
+                if (s0 >= (row & 32) + 32) {
+                    if (row < C) {
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4)
+                            *reinterpret_cast<float4*>(Ls + row * LST + s0 + 4 * i4) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            *reinterpret_cast<uint4*>(sm + P_X + tc::sw_chunk(row - C, s0 / 8 + c, 64)) = z;
+                            *reinterpret_cast<uint4*>(sm + P_X + 8192 + tc::sw_chunk(row - C, s0 / 8 + c, 64)) = z;
+                        }
+                    }
+                    continue;
+                }
                 float g[16];
                 tc::ld16(trow + P_TM_G + s0, g);
                 tc::wait_ld();
@@ -823,13 +840,15 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                     make_float4(-a01.x, -a01.y, -a23.x, -a23.y);
             }
             __syncthreads();
-            const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
-            {  // Z = Lm_bl T_tl (all 256 threads)
-                const float* Lr = Ls + (32 + rC) * LST;
-                const float* Tc = Ls + cC;
+            {  // Z = Lm_bl T_tl (all 256 threads: lane = row, warp = group of four columns).  T_tl is
+               // lower triangular, so column group 4 warp .. + 3 takes rows k >= 4 warp only
+                const int r1 = lane, c1 = 4 * warp;
+                const float* Lr = Ls + (32 + r1) * LST;
+                const float* Tc = Ls + c1;
                 float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
+                    if (k4 < warp) continue;
                     const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
                     const float lk[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -840,15 +859,18 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                         a23 = __ffma2_rn(l2, make_float2(t4.z, t4.w), a23);
                     }
                 }
-                *reinterpret_cast<float4*>(Zs + rC * ZST + cC) = make_float4(a01.x, a01.y, a23.x, a23.y);
+                *reinterpret_cast<float4*>(Zs + r1 * ZST + c1) = make_float4(a01.x, a01.y, a23.x, a23.y);
             }
             __syncthreads();
-            {  // T_bl = -T_br Z, over Lm_bl
+            const int rC = (tid >> 3) & 31, cC = 4 * (tid & 7);
+            {  // T_bl = -T_br Z, over Lm_bl (warp = rows 4 warp .. + 3; T_br is lower triangular, so
+               // the products stop at k = 4 warp + 3)
                 const float* Tr = Ls + (32 + rC) * LST + 32;
                 const float* Zc = Zs + cC;
                 float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
+                    if (k4 > warp) break;
                     const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
                     const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
 #pragma unroll
