@@ -800,13 +800,17 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             }
             __syncthreads();
             float* Zs = Xs;
-            const int pB = tid >> 6, rB = (tid >> 2) & 15, cB = 4 * (tid & 3);
-            if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p}
-                const float* Lr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB;
-                const float* Tc = Ls + (32 * pB) * LST + 32 * pB + cB;
+            // the 64 threads of product p: warp half hB = (tid >> 5) & 1
+            const int pB = tid >> 6, hB = (tid >> 5) & 1, rB = (tid >> 2) & 15, cB = 4 * (tid & 3);
+            if (pB < 2) {  // X_p = Lm_{2p+1,2p} T_{2p,2p} (lane & 15 = row, columns 8 hB + 4 (lane >> 4)
+                           // .. + 3; T_{2p,2p} is lower triangular, so rows k >= 8 hB only)
+                const int r1 = lane & 15, c1 = 8 * hB + 4 * (lane >> 4);
+                const float* Lr = Ls + (32 * pB + 16 + r1) * LST + 32 * pB;
+                const float* Tc = Ls + (32 * pB) * LST + 32 * pB + c1;
                 float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
+                    if (k4 < 2 * hB) continue;
                     const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
                     const float lk[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -817,15 +821,17 @@ __global__ void __launch_bounds__(pf::PNT, 5)
                         a23 = __ffma2_rn(l2, make_float2(t4.z, t4.w), a23);
                     }
                 }
-                *reinterpret_cast<float4*>(Zs + (16 * pB + rB) * ZST + cB) = make_float4(a01.x, a01.y, a23.x, a23.y);
+                *reinterpret_cast<float4*>(Zs + (16 * pB + r1) * ZST + c1) = make_float4(a01.x, a01.y, a23.x, a23.y);
             }
             __syncthreads();
-            if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p}
+            if (pB < 2) {  // T_{2p+1,2p} = -T_{2p+1,2p+1} X_p, over Lm_{2p+1,2p} (rows 8 hB .. + 7;
+                           // T_{2p+1,2p+1} is lower triangular, so k <= 8 hB + 7)
                 const float* Tr = Ls + (32 * pB + 16 + rB) * LST + 32 * pB + 16;
                 const float* Xc = Zs + (16 * pB) * ZST + cB;
                 float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
+                    if (k4 > 2 * hB + 1) break;
                     const float4 tr = *reinterpret_cast<const float4*>(Tr + 4 * k4);
                     const float tk[4] = {tr.x, tr.y, tr.z, tr.w};
 #pragma unroll
@@ -886,25 +892,40 @@ __global__ void __launch_bounds__(pf::PNT, 5)
             __syncthreads();
 
             // ---- 7. Tw = T diag(beta gamma rk), Tu = T diag(beta) as hi / lo parts of the input type
-            //         (rows t, K-major), to the record: item e is chunk e & 7 of row (e >> 3) & 63 of
-            //         side e >> 9, so 8 consecutive threads write one row's 128 bytes
+            //         (rows t, K-major), to the record, in warp tiles of 8 rows x 4 16-byte chunks
+            //         (lane: row 8 rb + (lane >> 2), chunk 4 ch + (lane & 3); a row's 4 chunks fill
+            //         whole 32-byte sectors).  T is lower triangular, so on each side the 4 tiles with
+            //         ch = 1 and rb < 4 are zero.  Warp w converts (side 0 and side 1, rb 4 + w / 2,
+            //         ch w % 2) and (side w / 4, rb w % 4, ch 0), and stores the zero tile
+            //         (side w / 4, rb w % 4, ch 1).
+            {
+                const int lr = lane >> 2, lc = lane & 3;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int e = tid + PNT * k;
-                const int cc = e & 7, t = (e >> 3) & (C - 1);
-                const bool w_side = (e >> 9) == 0;
-                uint8_t* base = recj + REC_T4 + (w_side ? 0u : 16384u);
-                const float* wsrc = w_side ? wwsj : wusj;
-                const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
-                const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
-                const float4 wa = *reinterpret_cast<const float4*>(wsrc + cc * 8);
-                const float4 wb = *reinterpret_cast<const float4*>(wsrc + cc * 8 + 4);
-                const float x8[8] = {ta.x * wa.x, ta.y * wa.y, ta.z * wa.z, ta.w * wa.w,
-                                     tb.x * wb.x, tb.y * wb.y, tb.z * wb.z, tb.w * wb.w};
-                uint4 th, tl;
-                split_in_x8<F16>(x8, th, tl);
-                *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
-                *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
+                for (int k = 0; k < 3; ++k) {
+                    const int side = k < 2 ? k : warp >> 2;
+                    const int rb = k < 2 ? 4 + (warp >> 1) : warp & 3;
+                    const int ch = k < 2 ? warp & 1 : 0;
+                    const int t = 8 * rb + lr, cc = 4 * ch + lc;
+                    uint8_t* base = recj + REC_T4 + (side == 0 ? 0u : 16384u);
+                    const float* wsrc = side == 0 ? wwsj : wusj;
+                    const float4 ta = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8);
+                    const float4 tb = *reinterpret_cast<const float4*>(Ls + t * LST + cc * 8 + 4);
+                    const float4 wa = *reinterpret_cast<const float4*>(wsrc + cc * 8);
+                    const float4 wb = *reinterpret_cast<const float4*>(wsrc + cc * 8 + 4);
+                    const float x8[8] = {ta.x * wa.x, ta.y * wa.y, ta.z * wa.z, ta.w * wa.w,
+                                         tb.x * wb.x, tb.y * wb.y, tb.z * wb.z, tb.w * wb.w};
+                    uint4 th, tl;
+                    split_in_x8<F16>(x8, th, tl);
+                    *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = th;
+                    *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = tl;
+                }
+                {  // this warp's zero tile: side warp >> 2, rb = warp & 3, ch = 1
+                    const int t = 8 * (warp & 3) + lr, cc = 4 + lc;
+                    uint8_t* base = recj + REC_T4 + ((warp >> 2) == 0 ? 0u : 16384u);
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(base + tc::sw_chunk(t, cc, 64)) = z;
+                    *reinterpret_cast<uint4*>(base + 8192 + tc::sw_chunk(t, cc, 64)) = z;
+                }
             }
             __syncthreads();  // this head's reads of Lm, T and the scratch are done
         }
