@@ -87,6 +87,10 @@ struct WindowArgs {
     float* y;
     int h_k, h_v, ntok, commit_at;
     float eps;
+    // CTAs stagger_lo .. 2 stagger_lo - 1 (the second CTA slot of each SM in the first wave) start
+    // stagger_cycles later; 0: no delay
+    int stagger_lo;
+    long long stagger_cycles;
 };
 
 // The sequential kernel's schedule.  A task is one chain of chunks, run for every value head: a

@@ -69,6 +69,14 @@ __global__ void __launch_bounds__(kWinThreads, 2) gdn_window_kernel(const Window
     __shared__ float zs[TK * D];                // the epilogue's z and gamma, fetched up front
     __shared__ float gs[D];
 
+    // The CTAs of one wave run in lock step (each streams its head's state, then computes with HBM
+    // idle); the second CTA slot of each SM starts a little later in the first wave, and the slots
+    // stay offset as later CTAs take their places, so one slot's state stream overlaps the other's
+    // arithmetic.  A bounded delay on the clock: nothing is waited for.
+    if (a.stagger_cycles > 0 && int(blockIdx.x) >= a.stagger_lo && int(blockIdx.x) < 2 * a.stagger_lo) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < a.stagger_cycles) __nanosleep(256);
+    }
     const int unit = blockIdx.x;  // n * h_v + h
     const int h = unit % a.h_v;
     const int n = unit / a.h_v;
