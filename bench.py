@@ -949,7 +949,8 @@ def main():
                                      "traffic": profiled_traffic(
                                          "gdn_window_kernel" if key == "window_verify"
                                          else "gdn_window_kernel_commit",
-                                         "gated_deltanet_delta_gb300/csrc/window.cuh")}}
+                                         ("gated_deltanet_delta_gb300/csrc/window.cuh",
+                                          "gated_deltanet_delta_gb300/csrc/window.cu"))}}
         elif key in extra:
             ops[key] = w
 
