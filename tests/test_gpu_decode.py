@@ -198,7 +198,8 @@ def test_pooled_decode_gathers_and_scatters_its_slots(Dk):
 
 
 @pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv", [(2, 1, 2, 4, 128, 128), (3, 37, 1, 2, 128, 100),
-                                             (1, 16, 2, 2, 64, 64), (2, 9, 1, 1, 256, 40)])
+                                             (1, 16, 2, 2, 64, 64), (2, 9, 1, 1, 256, 40),
+                                             (2, 33, 1, 2, 64, 48), (1, 20, 1, 1, 256, 72)])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_multi_token_steps_equal_a_chain_of_steps(B, T, Hk, Hv, Dk, Dv, in_place):
     # [gated_delta.rs] mt_gated_delta_chunk: the decode recurrence wrapped in a loop over t
