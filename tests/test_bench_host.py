@@ -1,5 +1,6 @@
 """Host-side logic of bench.py, on CPU: the algorithmic byte and flop counts, the rank plumbing of
-multi-process runs (world size 2 over gloo), and the reference arm's JSON line."""
+multi-process runs (world size 2 over gloo), the reference arm's JSON line, and the lookup of
+profiled DRAM traffic by source hash."""
 import json
 import os
 import socket
@@ -98,3 +99,25 @@ def test_reference_arm_prints_one_line():
                         "--steps", "3", "--warmup", "3"], capture_output=True, text=True, env=env,
                        timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_traffic_rows_follow_their_sources(tmp_path, monkeypatch):
+    # a row counts only while the hash of its source (one file, or several hashed in order) matches
+    import hashlib
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "k.cuh").write_bytes(b"kernel v1")
+    (tmp_path / "k.cu").write_bytes(b"launch v1")
+    one = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    two = hashlib.sha256(b"kernel v1" + b"launch v1").hexdigest()[:16]
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# kernel sha bytes\n"
+        f"single_kernel {one} 123 capture\n"
+        f"pair_kernel {two} 456 capture\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("single_kernel", "k.cuh") == 123
+    assert bench.profiled_traffic("pair_kernel", ("k.cuh", "k.cu")) == 456
+    assert bench.profiled_traffic("pair_kernel", ("k.cu", "k.cuh")) is None  # order matters
+    assert bench.profiled_traffic("pair_kernel", "k.cuh") is None
+    (tmp_path / "k.cu").write_bytes(b"launch v2")  # the launch shape changed: the row is stale
+    assert bench.profiled_traffic("pair_kernel", ("k.cuh", "k.cu")) is None
+    assert bench.profiled_traffic("missing", "nope.cuh") is None
